@@ -1,0 +1,377 @@
+"""Benchmark of the MSA decode step on GB300.
+
+One step = one decode pass over a batch: insert the step's new K/V/index-key
+tokens (with quantisation), score every candidate block, select the top
+blocks, run split-K sparse GQA and its combine. The default workload is
+batch 32 x 32,768-token contexts, 1 query token, 64/4/4 heads, FP8 index keys,
+bf16 KV, top-16 blocks.
+
+Prints one JSON line (rank 0). ``value`` is query-tokens/s over all ranks with
+the inputs already resident in HBM; ``e2e`` is the same metric through the
+public API with the per-step inputs copied from pinned host memory and the
+output copied back inside the timed region. The L2 is flushed (a 512 MB write)
+before every timed step. ``--impl reference`` times the fp64 CPU oracle instead,
+on a bounded sample of the same workload.
+
+Multi-GPU (torchrun): every rank runs its own full copy of the workload (the
+requests are independent; no data-path collective), so scaling is weak and
+``value`` sums the query tokens of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MSA decode query-tokens/s at 1 GB300; achieved HBM GB/s vs peak per kernel"
+FALLBACK_HBM_GBS = 6800.0
+
+# ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the index-score
+# kernel, keyed by the hash of the sources it was measured on (a changed kernel
+# reports null until it is measured again).
+NCU_TRAFFIC = {}
+
+
+def _src_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "block_sparse_attention_07_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def workload_desc(w):
+    ctx = f"context {w.ctx}" if w.ctx else f"context U[{w.ctx_range[0]},{w.ctx_range[1]}]"
+    return (f"msa_decode_{w.name}: batch {w.batch}, {ctx}, q_len {w.q_len}, {w.n_heads} q / {w.n_kv_heads} kv / "
+            f"{w.n_idx_heads} index heads, head_dim {w.head_dim}, block {w.block_size}, top-{w.topk} incl. local, "
+            f"{'FP8 E4M3' if w.idx_dtype == 'fp8' else 'fp32'} index keys, {w.kv_dtype} KV")
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------- rank logic --
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_seconds: float, local_units: int, world: int, device=None):
+    """Max time and summed units over ranks (identity for one rank)."""
+    if world == 1:
+        return local_seconds, local_units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=device)
+    u = torch.tensor([float(local_units)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(u.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------- clocks --
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), hw=parts[5], hwt=parts[6], swt=parts[7],
+                                 pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = sorted({name for r in rows for name, key in (("hw_slowdown", "hw"),
+                                                              ("hw_thermal_slowdown", "hwt"),
+                                                              ("sw_thermal_slowdown", "swt"),
+                                                              ("sw_power_cap", "pcap"))
+                          if r[key].lower() == "active"})
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- byte models --
+def index_bytes(dw):
+    """Algorithmic bytes of one index-score launch: every scored block's FP8 keys and
+    per-token scales for all index heads, the index queries, the score rows."""
+    w = dw.w
+    units = sum(max(0, (int(L) - 1) // w.block_size) for L in dw.lens)
+    per_unit = w.n_idx_heads * w.block_size * (w.head_dim * (1 if w.idx_dtype == "fp8" else 4)
+                                               + (4 if w.idx_dtype == "fp8" else 0))
+    q = dw.q_idx.numel() * dw.q_idx.element_size()
+    scores = dw.scores.numel() * 4
+    return units * per_unit + q + scores
+
+
+def attention_bytes(dw, sel):
+    """Algorithmic bytes of one sparse-GQA launch: the union over positions of the
+    selected blocks' K and V for each (request, KV head), plus q and out."""
+    w = dw.w
+    per_tok = 2 * w.head_dim * 2 if w.kv_dtype == "bf16" else 2 * (w.head_dim // 2 + w.head_dim // 16)
+    total = 0
+    for bi in range(sel.shape[0]):
+        L = int(dw.lens[bi])
+        for g in range(sel.shape[2]):
+            blocks = np.unique(sel[bi, :, g][sel[bi, :, g] >= 0])
+            toks = sum(min(w.block_size, L - int(b) * w.block_size) for b in blocks)
+            total += toks * per_tok
+    return total + 2 * dw.q.numel() * 2
+
+
+# ------------------------------------------------------------------ our arm --
+def run_ours(args, world, rank, local):
+    import torch
+    from block_sparse_attention_07_gb300 import synth
+    from block_sparse_attention_07_gb300.workload import DeviceWorkload
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = synth.WORKLOADS[args.workload]
+    dw = DeviceWorkload(w, dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    B, Q = len(dw.which), w.q_len
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        dw.step()
+    torch.cuda.synchronize(dev)
+    assert dw.check_flags() == 0, "device flags raised during warm-up"
+
+    names = ("insert", "index_score", "select", "sparse_gqa")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.15)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.fill_(float(s))
+        e = ev[s]
+        e[0].record(stream)
+        dw.insert_step_tokens()
+        e[1].record(stream)
+        dw.index_score()
+        e[2].record(stream)
+        dw.select()
+        e[3].record(stream)
+        dw.attend()
+        e[4].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    launches = args.steps * 5          # insert, index, select, attention, combine
+    per = {n: [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)] for i, n in enumerate(names)}
+    step_ms = [sum(per[n][s] for n in names) for s in range(args.steps)]
+    local_s = sum(step_ms) / 1e3
+    tot_s, tot_units = aggregate(local_s, B * Q * args.steps, world, dev)
+    value = tot_units / tot_s
+
+    # end to end through the public API: per-step inputs from pinned host memory,
+    # output back to pinned host memory, inside the timed region.
+    host_in = {k: getattr(dw, k).cpu().pin_memory() for k in
+               ("q", "q_idx", "new_k", "new_v", "new_idx", "new_slots", "block_table_d", "seq_lens_d")}
+    host_out = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for k, t in host_in.items():
+            getattr(dw, k).copy_(t, non_blocking=True)
+        dw.step()
+        host_out.copy_(dw.out, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    for _ in range(args.warmup):
+        e2e_step()
+    e2e_ms = []
+    barrier(world)
+    for s in range(args.steps):
+        flush.fill_(float(s))
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        e2e_step()
+        e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e_tot, _ = aggregate(sum(e2e_ms) / 1e3, 0, world, dev)
+    assert dw.check_flags() == 0, "device flags raised"
+
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peaks()
+    ib = index_bytes(dw)
+    idx_ms = statistics.mean(per["index_score"])
+    achieved = ib / (idx_ms / 1e3) / 1e9
+    sel = dw.selected.cpu().numpy()
+    ab = attention_bytes(dw, sel)
+    att_ms = statistics.mean(per["sparse_gqa"])
+    traffic = NCU_TRAFFIC.get(_src_hash("index_score.cu", "msa_device.cuh"))
+    line = {
+        "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": statistics.mean(step_ms), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8/bf16 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": workload_desc(w), "global_batch": B * world, "q_len": Q, "l2": "flushed (512 MB write) before every step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "index_score", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": ib, "avg_launch_ms": idx_ms},
+        "kernels_ms": {n: statistics.mean(v) for n, v in per.items()},
+        "sparse_gqa_roofline": {"achieved": ab / (att_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                                "frac": ab / (att_ms / 1e3) / 1e9 / peak, "algorithmic_bytes_per_launch": ab},
+        "e2e": {"value": B * Q * args.steps * world / e2e_tot, "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_requests)
+    return line
+
+
+# ---------------------------------------------------------- oracle / CPU --
+def cpu_baseline(w, n_requests, budget_s=20.0):
+    """The fp64 oracle as it stands, single-threaded, on a bounded sample of requests."""
+    from block_sparse_attention_07_gb300 import synth
+    from oracle import run as orun
+    lens = synth.seq_lens(w)
+    kg = kv = float(np.float32(synth.NVFP4_SYNTH_GLOBAL)) if w.kv_dtype == "nvfp4" else 1.0
+    spent, done = 0.0, 0
+    for b in range(min(n_requests, w.batch)):
+        req = synth.request(w, b, int(lens[b]))
+        t0 = time.perf_counter()
+        orun.run_request(req, int(lens[b]), w.topk, w.softmax_scale, w.block_size, w.idx_dtype, w.kv_dtype, kg, kv)
+        spent += time.perf_counter() - t0
+        done += 1
+        if spent > budget_s:
+            break
+    return {"value": done * w.q_len / spent, "unit": "query-tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {w.batch} requests of the same workload, all stages, fp64 numpy, 1 thread",
+            "seconds": spent}
+
+
+def run_reference(args, world, rank):
+    from block_sparse_attention_07_gb300 import synth
+    from oracle import run as orun
+    if rank != 0:
+        return None
+    w = synth.WORKLOADS[args.workload]
+    lens = synth.seq_lens(w)
+    kg = kv = float(np.float32(synth.NVFP4_SYNTH_GLOBAL)) if w.kv_dtype == "nvfp4" else 1.0
+    reqs = {}
+
+    def one(s):
+        b = s % w.batch
+        if b not in reqs:
+            reqs[b] = synth.request(w, b, int(lens[b]))
+        t0 = time.perf_counter()
+        orun.run_request(reqs[b], int(lens[b]), w.topk, w.softmax_scale, w.block_size, w.idx_dtype, w.kv_dtype,
+                         kg, kv)
+        return time.perf_counter() - t0
+
+    for s in range(args.warmup):
+        one(s)
+    times = [one(s) for s in range(args.steps)]
+    value = len(times) * w.q_len / sum(times)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(w), "global_batch": w.batch, "q_len": w.q_len,
+                   "step": "one request of the batch per step (bounded sample), all stages"},
+        "cpu_baseline": {"value": value, "unit": "query-tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "one request of the workload per step, fp64 numpy, 1 thread"},
+        "e2e": {"value": value, "unit": "query-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--workload", default="b32_32k")
+    ap.add_argument("--cpu-requests", type=int, default=6)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "reference":
+            if rank != 0:
+                return 0
+            world = 1
+        else:
+            import torch
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+    line = run_reference(args, world, rank) if args.impl == "reference" else run_ours(args, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl != "reference":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,361 @@
+// Stage 1 of MSA decode: block scoring by the index heads.
+//
+// "MiniMax M3 vLLM サポート：…" (agentlenshq.com), section "MSA 実行プロセス",
+// step 1: a small index head scores every candidate KV block. The block score
+// is the maximum over the block's tokens of s_t * (q_idx . k_t). Following
+// "vLLM、AMD Instinct MI355X上で…" (news.ainew.jp), question 2, each index key
+// is loaded once for all query positions of its request, and no positive
+// score scale is applied.
+//
+// FP8 path (the hot one): a persistent kernel, one CTA per SM. Work units are
+// the (request, block) pairs that some position of the request can select.
+// A producer thread streams each unit's page (I heads x 128 tokens x 128 B of
+// E4M3 keys, contiguous, plus I x 512 B of per-token scales) into a ring of
+// shared-memory stages with bulk copies completed on mbarriers. One consumer
+// warp per index head turns 16 tokens x 16 dims of keys into an fp16 mma A
+// fragment (cvt e4m3x2 -> f16x2 is exact), multiplies by the Q positions'
+// index queries (the 8 columns of m16n8k16; fp16 after an exact power-of-two
+// rescale of each query row), applies the per-token scale and keeps the running
+// max. The dims a thread feeds to the mma are a fixed permutation of 0..127,
+// applied identically to keys and queries, so each thread reads whole 16-byte
+// runs of a key row.
+#include "msa_internal.h"
+
+namespace msa {
+
+constexpr int kIdxStages = 3;
+constexpr int kMaxIdxHeads = 4;
+constexpr uint32_t kFull = 0xffffffffu;
+
+struct IdxParams {
+  const void* q;
+  const void* keys;
+  const float* scale;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  float* scores;
+  uint32_t* flags;
+  int B, Q, I, NB, P;
+};
+
+// Blocks of request b that some query position can select: every n < l_last,
+// l_last being the local block of the last position. -1 for an invalid length.
+__device__ __forceinline__ int units_of(int L, int Q, int NB) {
+  if (L < Q || L > NB * kBlock || L < 1) return -1;
+  return (L - 1) / kBlock;
+}
+
+// Exclusive prefix of units_of over the batch, computed by one warp into pref[0..B].
+__device__ void build_prefix(const IdxParams& p, int* pref, bool report) {
+  const int lane = threadIdx.x & 31;
+  int run = 0;
+  if (lane == 0) pref[0] = 0;
+  for (int base = 0; base < p.B; base += 32) {
+    const int b = base + lane;
+    int u = 0;
+    if (b < p.B) {
+      u = units_of(p.seq_lens[b], p.Q, p.NB);
+      if (u < 0) {
+        if (report) set_flag(p.flags, MSA_FLAG_BAD_SEQLEN);
+        u = 0;
+      }
+    }
+    int incl = u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (b < p.B) pref[b + 1] = run + incl;
+    run += __shfl_sync(kFull, incl, 31);
+  }
+}
+
+// Largest b with pref[b] <= u (u < pref[B]).
+__device__ __forceinline__ int find_request(const int* pref, int B, int64_t u) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pref[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Sets scores[b, j, g, n] = -inf for every n >= units(b) (never written by a unit).
+__device__ void fill_tails(const IdxParams& p, const int* pref) {
+  const int64_t per_b = static_cast<int64_t>(p.Q) * p.I * p.NB;
+  const int64_t total = per_b * p.B;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; x < total; x += stride) {
+    const int b = static_cast<int>(x / per_b);
+    const int n = static_cast<int>(x % p.NB);
+    if (n >= pref[b + 1] - pref[b]) p.scores[x] = -INFINITY;
+  }
+}
+
+template <int kStages>
+__global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_kernel(IdxParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_fp8[];
+  uint8_t* smem = smem_fp8;
+  const int I = p.I;
+  const uint32_t key_bytes = static_cast<uint32_t>(I) * kBlock * kDim;   // I x 16 KB
+  const uint32_t scale_bytes = static_cast<uint32_t>(I) * kBlock * 4;    // I x 512 B
+  const uint32_t stage_bytes = key_bytes + scale_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * stage_bytes);
+  uint64_t* empty = full + kStages;
+  int* valid = reinterpret_cast<int*>(empty + kStages);
+  int* pref = valid + kStages;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) build_prefix(p, pref, blockIdx.x == 0);
+  if (threadIdx.x == 32) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_addr(&full[s]), 1);
+      mbar_init(smem_addr(&empty[s]), I);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  fill_tails(p, pref);
+
+  const int64_t U = pref[p.B];
+  const int64_t u0 = U * blockIdx.x / gridDim.x, u1 = U * (blockIdx.x + 1) / gridDim.x;
+  if (u0 >= u1) return;
+  const int b_first = find_request(pref, p.B, u0);
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer --
+    if (lane != 0) return;
+    const uint64_t pol = l2_evict_first_policy();
+    const uint8_t* keys = static_cast<const uint8_t*>(p.keys);
+    int b = b_first;
+    int64_t i = 0;
+    for (int64_t u = u0; u < u1; ++u, ++i) {
+      while (u >= pref[b + 1]) ++b;
+      const int n = static_cast<int>(u - pref[b]);
+      const int s = static_cast<int>(i % kStages);
+      const uint32_t ph = static_cast<uint32_t>((i / kStages) & 1);
+      if (!mbar_wait(smem_addr(&empty[s]), ph ^ 1)) {
+        set_flag(p.flags, MSA_FLAG_TIMEOUT);
+        break;
+      }
+      const int page = p.block_table[static_cast<int64_t>(b) * p.NB + n];
+      const uint32_t fb = smem_addr(&full[s]);
+      if (page < 0 || page >= p.P) {
+        set_flag(p.flags, MSA_FLAG_BAD_PAGE);
+        valid[s] = 0;
+        mbar_arrive(fb);
+      } else {
+        valid[s] = 1;
+        const uint32_t dst = smem_addr(smem + s * stage_bytes);
+        mbar_arrive_expect_tx(fb, stage_bytes);
+        bulk_g2s(dst, keys + static_cast<int64_t>(page) * key_bytes, key_bytes, fb, pol);
+        bulk_g2s(dst + key_bytes, p.scale + static_cast<int64_t>(page) * I * kBlock, scale_bytes, fb, pol);
+      }
+    }
+    // Do not leave while copies into this CTA's shared memory may be in flight.
+    const int64_t first = i > kStages ? i - kStages : 0;
+    for (int64_t k = first; k < i; ++k)
+      if (!mbar_wait(smem_addr(&full[k % kStages]), static_cast<uint32_t>((k / kStages) & 1))) break;
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers --
+  const int g = warp - 1;
+  const int gr = lane >> 2, c = lane & 3;
+  const uint16_t* qbase = static_cast<const uint16_t*>(p.q);
+  uint32_t qb[8][2];
+  float inv_col0 = 0.f, inv_col1 = 0.f;
+  int ell_col0 = 0, ell_col1 = 0;
+  int cur_b = -1;
+  int b = b_first;
+  int64_t i = 0;
+  for (int64_t u = u0; u < u1; ++u, ++i) {
+    while (u >= pref[b + 1]) ++b;
+    const int n = static_cast<int>(u - pref[b]);
+    const int L = p.seq_lens[b];
+    if (b != cur_b) {
+      // Index-query fragment of position gr for this request and head.
+      float qv[32];
+      if (gr < p.Q) {
+        const uint16_t* qp = qbase + ((static_cast<int64_t>(b) * p.Q + gr) * I + g) * kDim;
+        const uint4 a0 = *reinterpret_cast<const uint4*>(qp + 16 * c);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(qp + 16 * c + 8);
+        const uint4 a2 = *reinterpret_cast<const uint4*>(qp + 64 + 16 * c);
+        const uint4 a3 = *reinterpret_cast<const uint4*>(qp + 64 + 16 * c + 8);
+        const uint32_t w[16] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w,
+                                a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          qv[2 * k] = bf16_bits_to_f32(w[k] & 0xFFFF);
+          qv[2 * k + 1] = bf16_bits_to_f32(w[k] >> 16);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) qv[k] = 0.f;
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(qv[k]));
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+      const int sh = fp16_shift_for(amax);
+      const float f = exp2_int(sh);
+      const float inv = gr < p.Q ? exp2_int(-sh) : 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        qb[s][0] = pack_f16x2(qv[4 * s] * f, qv[4 * s + 1] * f);
+        qb[s][1] = pack_f16x2(qv[4 * s + 2] * f, qv[4 * s + 3] * f);
+      }
+      inv_col0 = __shfl_sync(kFull, inv, 8 * c);
+      inv_col1 = __shfl_sync(kFull, inv, 8 * c + 4);
+      ell_col0 = (L - p.Q + 2 * c) / kBlock;
+      ell_col1 = (L - p.Q + 2 * c + 1) / kBlock;
+      cur_b = b;
+    }
+
+    const int s = static_cast<int>(i % kStages);
+    if (!mbar_wait(smem_addr(&full[s]), static_cast<uint32_t>((i / kStages) & 1))) {
+      if (lane == 0) set_flag(p.flags, MSA_FLAG_TIMEOUT);
+      break;
+    }
+    float m0 = -INFINITY, m1 = -INFINITY;
+    if (valid[s]) {
+      const uint8_t* kb = smem + s * stage_bytes + g * (kBlock * kDim);
+      const float* sc = reinterpret_cast<const float*>(smem + s * stage_bytes + key_bytes) + g * kBlock;
+#pragma unroll 2
+      for (int t = 0; t < 8; ++t) {
+        const uint8_t* r0 = kb + (16 * t + gr) * kDim + 16 * c;
+        const uint4 x0 = *reinterpret_cast<const uint4*>(r0);
+        const uint4 x1 = *reinterpret_cast<const uint4*>(r0 + 64);
+        const uint4 y0 = *reinterpret_cast<const uint4*>(r0 + 8 * kDim);
+        const uint4 y1 = *reinterpret_cast<const uint4*>(r0 + 8 * kDim + 64);
+        const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const uint32_t yw[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t a[4] = {e4m3x2_to_f16x2(static_cast<uint16_t>(xw[k] & 0xFFFF)),
+                                 e4m3x2_to_f16x2(static_cast<uint16_t>(yw[k] & 0xFFFF)),
+                                 e4m3x2_to_f16x2(static_cast<uint16_t>(xw[k] >> 16)),
+                                 e4m3x2_to_f16x2(static_cast<uint16_t>(yw[k] >> 16))};
+          mma_f16(acc, a, qb[k][0], qb[k][1]);
+        }
+        const float s0 = sc[16 * t + gr], s1 = sc[16 * t + gr + 8];
+        m0 = fmaxf(m0, fmaxf(acc[0] * s0, acc[2] * s1));
+        m1 = fmaxf(m1, fmaxf(acc[1] * s0, acc[3] * s1));
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      m0 = fmaxf(m0, __shfl_xor_sync(kFull, m0, o));
+      m1 = fmaxf(m1, __shfl_xor_sync(kFull, m1, o));
+    }
+    if (gr == 0) {
+      const int64_t base = (static_cast<int64_t>(b) * p.Q) * I + g;
+      const int j0 = 2 * c, j1 = 2 * c + 1;
+      if (j0 < p.Q) p.scores[(base + static_cast<int64_t>(j0) * I) * p.NB + n] = n < ell_col0 ? m0 * inv_col0 : -INFINITY;
+      if (j1 < p.Q) p.scores[(base + static_cast<int64_t>(j1) * I) * p.NB + n] = n < ell_col1 ? m1 * inv_col1 : -INFINITY;
+    }
+  }
+}
+
+// fp32 keys and queries (small workloads): one warp per (request, block, head);
+// each lane scores 4 tokens with plain fp32 FMAs.
+__global__ void __launch_bounds__(128) index_score_f32_kernel(IdxParams p) {
+  extern __shared__ __align__(16) uint8_t smem_f32[];
+  uint8_t* smem = smem_f32;
+  int* pref = reinterpret_cast<int*>(smem);
+  float* qsh = reinterpret_cast<float*>(smem + ((static_cast<size_t>(p.B) + 1) * 4 + 15) / 16 * 16);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) build_prefix(p, pref, blockIdx.x == 0);
+  __syncthreads();
+  fill_tails(p, pref);
+  float* qw = qsh + warp * 8 * kDim;
+  const int64_t total = static_cast<int64_t>(pref[p.B]) * p.I;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const float* qg = static_cast<const float*>(p.q);
+  const float* keys = static_cast<const float*>(p.keys);
+  for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp; w < total; w += nwarps) {
+    const int64_t v = w / p.I;
+    const int g = static_cast<int>(w % p.I);
+    const int b = find_request(pref, p.B, v);
+    const int n = static_cast<int>(v - pref[b]);
+    const int L = p.seq_lens[b];
+    __syncwarp();
+    for (int x = lane; x < p.Q * kDim; x += 32) {
+      const int j = x / kDim, d = x % kDim;
+      qw[x] = qg[((static_cast<int64_t>(b) * p.Q + j) * p.I + g) * kDim + d];
+    }
+    __syncwarp();
+    const int page = p.block_table[static_cast<int64_t>(b) * p.NB + n];
+    float best[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) best[j] = -INFINITY;
+    if (page < 0 || page >= p.P) {
+      if (lane == 0) set_flag(p.flags, MSA_FLAG_BAD_PAGE);
+    } else {
+      for (int k = 0; k < 4; ++k) {
+        const float4* row = reinterpret_cast<const float4*>(
+            keys + ((static_cast<int64_t>(page) * p.I + g) * kBlock + lane + 32 * k) * kDim);
+        float dot[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int d4 = 0; d4 < kDim / 4; ++d4) {
+          const float4 kv = row[d4];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (j < p.Q) {
+              const float* qj = qw + j * kDim + 4 * d4;
+              dot[j] = fmaf(kv.x, qj[0], dot[j]);
+              dot[j] = fmaf(kv.y, qj[1], dot[j]);
+              dot[j] = fmaf(kv.z, qj[2], dot[j]);
+              dot[j] = fmaf(kv.w, qj[3], dot[j]);
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) best[j] = fmaxf(best[j], dot[j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      for (int o = 16; o > 0; o >>= 1) best[j] = fmaxf(best[j], __shfl_xor_sync(kFull, best[j], o));
+    if (lane < p.Q) {
+      float val = best[0];
+#pragma unroll
+      for (int j = 1; j < 8; ++j)
+        if (lane == j) val = best[j];
+      const int ell = (L - p.Q + lane) / kBlock;
+      p.scores[((static_cast<int64_t>(b) * p.Q + lane) * p.I + g) * p.NB + n] = n < ell ? val : -INFINITY;
+    }
+  }
+}
+
+cudaError_t launch_index_score(const IndexArgs& a, cudaStream_t stream, DispatchRecord* rec) {
+  IdxParams p{a.q, a.keys, a.scale, a.block_table, a.seq_lens, a.scores, a.flags, a.B, a.Q, a.I, a.NB, a.P};
+  const int sms = device_sm_count();
+  cudaError_t err;
+  if (a.fp8) {
+    const size_t stage = static_cast<size_t>(a.I) * kBlock * kDim + static_cast<size_t>(a.I) * kBlock * 4;
+    const size_t smem = kIdxStages * stage + 2 * kIdxStages * 8 + kIdxStages * 4 + (a.B + 1) * 4;
+    err = cudaFuncSetAttribute(index_score_fp8_kernel<kIdxStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    const int grid = sms;
+    index_score_fp8_kernel<kIdxStages><<<grid, 32 * (1 + a.I), smem, stream>>>(p);
+    rec->set("index_score fp8_mma_f16 grid=%d block=%d smem=%zu stages=%d q_len=%d idx_heads=%d", grid,
+             32 * (1 + a.I), smem, kIdxStages, a.Q, a.I);
+  } else {
+    const size_t smem = ((static_cast<size_t>(a.B) + 1) * 4 + 15) / 16 * 16 + 4 * 8 * kDim * 4;
+    err = cudaFuncSetAttribute(index_score_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    const int grid = sms * 4;
+    index_score_f32_kernel<<<grid, 128, smem, stream>>>(p);
+    rec->set("index_score f32_fma grid=%d block=128 smem=%zu q_len=%d idx_heads=%d", grid, smem, a.Q, a.I);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace msa

@@ -1,0 +1,240 @@
+// C ABI of libmsa.so (declared in include/msa.h): host-side validation,
+// the thread-local dispatch record, and the launches. Nothing here allocates
+// device memory and nothing synchronises except msa_read_device_flags.
+#include <cstring>
+
+#include "msa_internal.h"
+
+namespace msa {
+
+static thread_local DispatchRecord g_record = {"(no launch yet)"};
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape rules shared by every entry point.
+static msa_status_t check_dims(const msa_dims_t* d) {
+  if (d == nullptr) return MSA_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->q_len < 1 || d->n_heads < 1 || d->n_kv_heads < 1 || d->n_idx_heads < 1 ||
+      d->head_dim < 1 || d->block_size < 1 || d->max_blocks_per_seq < 1 || d->num_pages < 1 || d->topk < 1 ||
+      d->local_blocks < 0)
+    return MSA_ERR_INVALID_ARG;
+  if (!(d->softmax_scale > 0.f) || d->softmax_scale != d->softmax_scale) return MSA_ERR_INVALID_ARG;
+  if (d->head_dim != kDim || d->block_size != kBlock || d->local_blocks != 1) return MSA_ERR_UNSUPPORTED;
+  if (d->n_idx_heads != d->n_kv_heads || d->n_heads != d->n_kv_heads * kGroup) return MSA_ERR_UNSUPPORTED;
+  if (d->topk > 16 || d->q_len > 8 || d->n_idx_heads > 4 || d->batch > 4096) return MSA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d->max_blocks_per_seq) * kBlock > INT32_MAX) return MSA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d->num_pages) * d->n_kv_heads * kBlock > INT32_MAX) return MSA_ERR_UNSUPPORTED;
+  return MSA_OK;
+}
+
+static msa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
+
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" {
+
+int msa_abi_version(void) { return MSA_ABI_VERSION; }
+
+const char* msa_status_string(msa_status_t s) {
+  switch (s) {
+    case MSA_OK: return "MSA_OK";
+    case MSA_ERR_INVALID_ARG: return "MSA_ERR_INVALID_ARG";
+    case MSA_ERR_UNSUPPORTED: return "MSA_ERR_UNSUPPORTED";
+    case MSA_ERR_CUDA: return "MSA_ERR_CUDA";
+    case MSA_ERR_WORKSPACE: return "MSA_ERR_WORKSPACE";
+    case MSA_ERR_DEVICE_FLAG: return "MSA_ERR_DEVICE_FLAG";
+  }
+  return "MSA_ERR_UNKNOWN";
+}
+
+msa_status_t msa_get_last_dispatch(char* buf, size_t len) {
+  if (buf == nullptr || len == 0) return MSA_ERR_INVALID_ARG;
+  strncpy(buf, g_record.text, len - 1);
+  buf[len - 1] = '\0';
+  return MSA_OK;
+}
+
+msa_status_t msa_kv_insert_quant(const msa_dims_t* dims, const void* k_new, const void* v_new,
+                                 const void* idx_k_new, msa_dtype_t idx_new_dtype, const int64_t* slot_mapping,
+                                 int32_t num_tokens, const msa_kv_cache_t* cache,
+                                 const msa_index_cache_t* idx_cache, uint32_t* dev_flags, void* stream) {
+  msa_status_t st = check_dims(dims);
+  if (st != MSA_OK) return st;
+  if (num_tokens < 0 || cache == nullptr || dev_flags == nullptr) return MSA_ERR_INVALID_ARG;
+  if (num_tokens == 0) {
+    g_record.set("kv_insert empty");
+    return MSA_OK;
+  }
+  if (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr || cache->k == nullptr || cache->v == nullptr)
+    return MSA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(cache->k) || !aligned16(cache->v))
+    return MSA_ERR_INVALID_ARG;
+  InsertArgs a;
+  memset(&a, 0, sizeof(a));
+  if (cache->dtype == MSA_NVFP4) {
+    if (cache->k_scale == nullptr || cache->v_scale == nullptr) return MSA_ERR_INVALID_ARG;
+    if (!(cache->k_global > 0.f) || !(cache->v_global > 0.f) || cache->k_global > 3.0e38f ||
+        cache->v_global > 3.0e38f)
+      return MSA_ERR_INVALID_ARG;
+    a.kv_nvfp4 = 1;
+  } else if (cache->dtype != MSA_BF16) {
+    return MSA_ERR_UNSUPPORTED;
+  }
+  if (idx_k_new != nullptr) {
+    if (idx_cache == nullptr || idx_cache->keys == nullptr || !aligned16(idx_k_new) || !aligned16(idx_cache->keys))
+      return MSA_ERR_INVALID_ARG;
+    if (idx_cache->dtype == MSA_FP8_E4M3) {
+      if (idx_cache->scale == nullptr) return MSA_ERR_INVALID_ARG;
+      if (idx_new_dtype != MSA_F32 && idx_new_dtype != MSA_BF16) return MSA_ERR_UNSUPPORTED;
+      a.idx_fp8 = 1;
+    } else if (idx_cache->dtype == MSA_F32) {
+      if (idx_new_dtype != MSA_F32) return MSA_ERR_UNSUPPORTED;
+    } else {
+      return MSA_ERR_UNSUPPORTED;
+    }
+    a.idx_new = idx_k_new;
+    a.idx_new_bf16 = idx_new_dtype == MSA_BF16;
+    a.idx_keys = idx_cache->keys;
+    a.idx_scale = idx_cache->scale;
+  }
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.slots = slot_mapping;
+  a.T = num_tokens;
+  a.G = dims->n_kv_heads;
+  a.num_slots = static_cast<int64_t>(dims->num_pages) * kBlock;
+  a.k = cache->k;
+  a.v = cache->v;
+  a.k_scale = cache->k_scale;
+  a.v_scale = cache->v_scale;
+  a.k_global = cache->k_global;
+  a.v_global = cache->v_global;
+  a.flags = dev_flags;
+  return cuda_status(launch_kv_insert(a, static_cast<cudaStream_t>(stream), &g_record));
+}
+
+msa_status_t msa_index_score(const msa_dims_t* dims, const void* idx_q, msa_dtype_t q_dtype,
+                             const msa_index_cache_t* idx_cache, const int32_t* block_table,
+                             const int32_t* seq_lens, float* scores, uint32_t* dev_flags, void* stream) {
+  msa_status_t st = check_dims(dims);
+  if (st != MSA_OK) return st;
+  if (idx_q == nullptr || idx_cache == nullptr || idx_cache->keys == nullptr || block_table == nullptr ||
+      seq_lens == nullptr || scores == nullptr || dev_flags == nullptr)
+    return MSA_ERR_INVALID_ARG;
+  if (!aligned16(idx_q) || !aligned16(idx_cache->keys)) return MSA_ERR_INVALID_ARG;
+  IndexArgs a;
+  a.fp8 = 0;
+  if (idx_cache->dtype == MSA_FP8_E4M3) {
+    if (q_dtype != MSA_BF16) return MSA_ERR_UNSUPPORTED;
+    if (idx_cache->scale == nullptr || !aligned16(idx_cache->scale)) return MSA_ERR_INVALID_ARG;
+    a.fp8 = 1;
+  } else if (idx_cache->dtype == MSA_F32) {
+    if (q_dtype != MSA_F32) return MSA_ERR_UNSUPPORTED;
+  } else {
+    return MSA_ERR_UNSUPPORTED;
+  }
+  a.q = idx_q;
+  a.keys = idx_cache->keys;
+  a.scale = idx_cache->scale;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.scores = scores;
+  a.flags = dev_flags;
+  a.B = dims->batch;
+  a.Q = dims->q_len;
+  a.I = dims->n_idx_heads;
+  a.NB = dims->max_blocks_per_seq;
+  a.P = dims->num_pages;
+  return cuda_status(launch_index_score(a, static_cast<cudaStream_t>(stream), &g_record));
+}
+
+msa_status_t msa_select_blocks(const msa_dims_t* dims, const float* scores, const int32_t* seq_lens,
+                               int32_t* selected, uint32_t* dev_flags, void* stream) {
+  msa_status_t st = check_dims(dims);
+  if (st != MSA_OK) return st;
+  if (scores == nullptr || seq_lens == nullptr || selected == nullptr || dev_flags == nullptr)
+    return MSA_ERR_INVALID_ARG;
+  SelectArgs a{scores, seq_lens, selected, dev_flags, dims->batch, dims->q_len, dims->n_idx_heads,
+               dims->max_blocks_per_seq, dims->topk};
+  return cuda_status(launch_select_blocks(a, static_cast<cudaStream_t>(stream), &g_record));
+}
+
+size_t msa_sparse_gqa_workspace_size(const msa_dims_t* dims, msa_dtype_t kv_dtype) {
+  (void)kv_dtype;
+  if (check_dims(dims) != MSA_OK) return 0;
+  return gqa_workspace_bytes(dims->batch, dims->q_len, dims->n_kv_heads, dims->topk);
+}
+
+msa_status_t msa_sparse_gqa_decode(const msa_dims_t* dims, const void* q, const msa_kv_cache_t* cache,
+                                   const int32_t* block_table, const int32_t* seq_lens, const int32_t* selected,
+                                   void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                   uint32_t* dev_flags, void* stream) {
+  msa_status_t st = check_dims(dims);
+  if (st != MSA_OK) return st;
+  if (q == nullptr || cache == nullptr || cache->k == nullptr || cache->v == nullptr || block_table == nullptr ||
+      seq_lens == nullptr || selected == nullptr || out == nullptr || dev_flags == nullptr)
+    return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(cache->k) || !aligned16(cache->v)) return MSA_ERR_INVALID_ARG;
+  GqaArgs a;
+  memset(&a, 0, sizeof(a));
+  if (cache->dtype == MSA_NVFP4) {
+    if (cache->k_scale == nullptr || cache->v_scale == nullptr || !aligned16(cache->k_scale) ||
+        !aligned16(cache->v_scale))
+      return MSA_ERR_INVALID_ARG;
+    if (!(cache->k_global > 0.f) || !(cache->v_global > 0.f)) return MSA_ERR_INVALID_ARG;
+    a.nvfp4 = 1;
+  } else if (cache->dtype != MSA_BF16) {
+    return MSA_ERR_UNSUPPORTED;
+  }
+  const size_t need = gqa_workspace_bytes(dims->batch, dims->q_len, dims->n_kv_heads, dims->topk);
+  if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MSA_ERR_WORKSPACE;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = cache->k;
+  a.v = cache->v;
+  a.k_scale = static_cast<const uint8_t*>(cache->k_scale);
+  a.v_scale = static_cast<const uint8_t*>(cache->v_scale);
+  a.k_global = cache->k_global;
+  a.v_global = cache->v_global;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.selected = selected;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.workspace = static_cast<float*>(workspace);
+  a.flags = dev_flags;
+  a.B = dims->batch;
+  a.Q = dims->q_len;
+  a.H = dims->n_heads;
+  a.G = dims->n_kv_heads;
+  a.NB = dims->max_blocks_per_seq;
+  a.P = dims->num_pages;
+  a.K = dims->topk;
+  a.softmax_scale = dims->softmax_scale;
+  return cuda_status(launch_sparse_gqa(a, static_cast<cudaStream_t>(stream), &g_record));
+}
+
+msa_status_t msa_read_device_flags(const uint32_t* dev_flags, uint32_t* host_flags, void* stream) {
+  if (dev_flags == nullptr || host_flags == nullptr) return MSA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(host_flags, dev_flags, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MSA_ERR_CUDA;
+  return *host_flags != 0 ? MSA_ERR_DEVICE_FLAG : MSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,95 @@
+// Internal interface between the C ABI (msa_api.cu) and the kernel launchers.
+#pragma once
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cuda_runtime.h>
+
+#include "msa_device.cuh"
+
+namespace msa {
+
+// Thread-local record of what actually launched ("configured != executed").
+struct DispatchRecord {
+  char text[512];
+  void set(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(text, sizeof(text), fmt, ap);
+    va_end(ap);
+  }
+};
+
+int device_sm_count();
+
+struct InsertArgs {
+  const void* k_new;
+  const void* v_new;
+  const void* idx_new;
+  int idx_new_bf16;
+  const int64_t* slots;
+  int T, G;
+  int64_t num_slots;
+  int kv_nvfp4;
+  void* k;
+  void* v;
+  void* k_scale;
+  void* v_scale;
+  float k_global, v_global;
+  int idx_fp8;
+  void* idx_keys;
+  float* idx_scale;
+  uint32_t* flags;
+};
+
+struct IndexArgs {
+  const void* q;          // [B, Q, I, D] f32 or bf16
+  const void* keys;       // [P, I, BS, D] f32 or u8
+  const float* scale;     // [P, I, BS] (fp8 only)
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  float* scores;          // [B, Q, I, NB]
+  uint32_t* flags;
+  int B, Q, I, NB, P;
+  int fp8;
+};
+
+struct SelectArgs {
+  const float* scores;
+  const int32_t* seq_lens;
+  int32_t* selected;
+  uint32_t* flags;
+  int B, Q, I, NB, K;
+};
+
+struct GqaArgs {
+  const uint16_t* q;       // bf16 [B, Q, H, D]
+  int nvfp4;
+  const void* k;           // bf16 [P, G, BS, D] or u8 [P, G, BS, D/2]
+  const void* v;
+  const uint8_t* k_scale;  // nvfp4 [P, G, BS, D/16]
+  const uint8_t* v_scale;
+  float k_global, v_global;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int32_t* selected;  // [B, Q, G, K]
+  uint16_t* out;            // bf16 [B, Q, H, D]
+  float* lse;               // [B, Q, H] or null
+  float* workspace;
+  uint32_t* flags;
+  int B, Q, H, G, NB, P, K;
+  float softmax_scale;
+};
+
+// Floats per split-K partial: o [16 heads][128 dims], then m [16], then l [16].
+constexpr int kPartialFloats = kGroup * kDim + 2 * kGroup;
+
+size_t gqa_workspace_bytes(int B, int Q, int G, int K);
+
+cudaError_t launch_kv_insert(const InsertArgs& a, cudaStream_t stream, DispatchRecord* rec);
+cudaError_t launch_index_score(const IndexArgs& a, cudaStream_t stream, DispatchRecord* rec);
+cudaError_t launch_select_blocks(const SelectArgs& a, cudaStream_t stream, DispatchRecord* rec);
+cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRecord* rec);
+
+}  // namespace msa

@@ -1,0 +1,623 @@
+// Stage 3 of MSA decode: sparse GQA over the selected blocks, split-K, with a
+// log-sum-exp combine.
+//
+// "MiniMax M3 vLLM サポート：…" (agentlenshq.com), section "MSA 実行プロセス",
+// step 3: online-softmax attention over the selected KV blocks only; section
+// "EAGLE3 を用いた投機的デコード": a decode-only split-K path that serves every
+// decode_query_len. "vLLM、AMD Instinct MI355X上で…", question 1: 64 query
+// heads share 4 KV heads, so the 16 heads of a KV head form one M=16 tile.
+//
+// Work items are (row, selection slot) pairs, row = (request, KV head,
+// position) with the positions of one (request, KV head) adjacent so that
+// shared pages are still in L2. A persistent grid gives each CTA a contiguous
+// item range; whenever the row changes inside the range the CTA merges its
+// four warps' online-softmax states and writes either the final output (the
+// CTA covered the whole row) or a partial (o, m, l) that the combine kernel
+// merges. A producer thread fetches each selected page: bf16 K/V through
+// 2-D tensor maps with 128-byte swizzle (conflict-free ldmatrix), NVFP4 K/V as
+// four contiguous bulk copies that the consumers expand to fp16 tiles in the
+// same swizzled layout (e2m1 x e4m3 is exact in fp16; the fp32 global scales
+// are applied to the logits and the output). Each of the four consumer warps
+// owns 32 tokens of every block: QK^T and PV run on m16n8k16 tensor-core mma.
+// All waits are bounded; a kernel never traps.
+#include <cuda.h>
+
+#include "msa_internal.h"
+
+namespace msa {
+
+constexpr int kGqaStages = 3;
+constexpr int kCWarps = 4;
+constexpr int kBoxBytes = kBlock * 64 * 2;       // 128 rows x 128 B (64 fp16/bf16)
+constexpr int kTileBytes = 4 * kBoxBytes;        // K lo/hi + V lo/hi = 64 KB
+constexpr int kFp4StageBytes = 2 * (kBlock * kDim / 2 + kBlock * kDim / 16);  // 18 KB
+constexpr uint32_t kAll = 0xffffffffu;
+constexpr float kLn2 = 0.693147180559945309f;
+
+struct GqaParams {
+  const uint16_t* q;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int32_t* selected;
+  uint16_t* out;
+  float* lse;
+  float* ws;
+  uint32_t* flags;
+  const uint8_t* k4;
+  const uint8_t* v4;
+  const uint8_t* ks;
+  const uint8_t* vs;
+  float k_global, v_global;
+  float scale_log2;
+  int B, Q, H, G, NB, P, K;
+  int64_t W;  // items = B * G * Q * K
+};
+
+struct SmemLayout {
+  uint32_t stages, tiles, comb_o, comb_ml, bars;
+  uint32_t total;
+};
+
+template <bool kFp4>
+__host__ __device__ constexpr SmemLayout gqa_layout() {
+  SmemLayout s{};
+  s.stages = 0;
+  const uint32_t stage_bytes = kFp4 ? kFp4StageBytes : kTileBytes;
+  s.tiles = s.stages + kGqaStages * stage_bytes;
+  s.comb_o = s.tiles + (kFp4 ? 2 * kTileBytes : 0);
+  s.comb_ml = s.comb_o + kCWarps * kGroup * kDim * 4;
+  s.bars = s.comb_ml + kCWarps * kGroup * 2 * 4;
+  s.total = s.bars + (2 * kGqaStages + 2) * 8;
+  return s;
+}
+
+// First CTA whose item range contains item x (ranges are [W*c/C, W*(c+1)/C)).
+__host__ __device__ __forceinline__ int cta_of(int64_t x, int64_t W, int C) {
+  return static_cast<int>(((x + 1) * C + W - 1) / W) - 1;
+}
+
+struct Item {
+  int b, g, j, blk, page;
+  bool valid;
+  int64_t row;  // enumeration row (b, g, j)
+};
+
+// Decodes item x and checks it against the device-side invariants. Only the
+// producer reports problems, so each is flagged once per CTA visit.
+__device__ __forceinline__ Item decode_item(const GqaParams& p, int64_t x, bool report) {
+  Item it;
+  it.row = x / p.K;
+  const int e = static_cast<int>(x % p.K);
+  it.j = static_cast<int>(it.row % p.Q);
+  it.g = static_cast<int>((it.row / p.Q) % p.G);
+  it.b = static_cast<int>(it.row / (static_cast<int64_t>(p.Q) * p.G));
+  it.valid = false;
+  it.page = -1;
+  it.blk = p.selected[((static_cast<int64_t>(it.b) * p.Q + it.j) * p.G + it.g) * p.K + e];
+  if (it.blk < 0) return it;
+  const int L = p.seq_lens[it.b];
+  if (L < p.Q || L > p.NB * kBlock || L < 1) {
+    if (report) set_flag(p.flags, MSA_FLAG_BAD_SEQLEN);
+    return it;
+  }
+  const int ell = (L - p.Q + it.j) / kBlock;
+  if (it.blk > ell) {
+    if (report) set_flag(p.flags, MSA_FLAG_BAD_BLOCK);
+    return it;
+  }
+  it.page = p.block_table[static_cast<int64_t>(it.b) * p.NB + it.blk];
+  if (it.page < 0 || it.page >= p.P) {
+    if (report) set_flag(p.flags, MSA_FLAG_BAD_PAGE);
+    return it;
+  }
+  it.valid = true;
+  return it;
+}
+
+// Consumer-group barrier on an mbarrier (count = 4 warps), bounded in time.
+__device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  const bool ok = mbar_wait(bar, phase);
+  phase ^= 1;
+  return ok;
+}
+
+__device__ __forceinline__ uint32_t swz(uint32_t box, int row, int chunk) {
+  return box + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+template <bool kFp4>
+__global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
+    sparse_gqa_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, GqaParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  constexpr SmemLayout Ly = gqa_layout<kFp4>();
+  constexpr uint32_t kStageBytes = kFp4 ? kFp4StageBytes : kTileBytes;
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base - raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + Ly.bars);
+  uint64_t* empty = full + kGqaStages;
+  uint64_t* gbar = empty + kGqaStages;   // [0]: partials written, [1]: partials read / tile ready
+  float* comb_o = reinterpret_cast<float*>(sm + Ly.comb_o);
+  float* comb_m = reinterpret_cast<float*>(sm + Ly.comb_ml);
+  float* comb_l = comb_m + kCWarps * kGroup;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGqaStages; ++s) {
+      mbar_init(smem_addr(&full[s]), 1);
+      mbar_init(smem_addr(&empty[s]), kCWarps);
+    }
+    mbar_init(smem_addr(&gbar[0]), kCWarps);
+    mbar_init(smem_addr(&gbar[1]), kCWarps);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int C = gridDim.x;
+  const int64_t x0 = p.W * blockIdx.x / C, x1 = p.W * (blockIdx.x + 1) / C;
+  if (x0 >= x1) return;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer --
+    if (lane != 0) return;
+    const uint64_t pol = l2_evict_first_policy();
+    int64_t i = 0;
+    for (int64_t x = x0; x < x1; ++x) {
+      const Item it = decode_item(p, x, true);
+      if (!it.valid) continue;
+      const int s = static_cast<int>(i % kGqaStages);
+      if (!mbar_wait(smem_addr(&empty[s]), static_cast<uint32_t>(((i / kGqaStages) & 1) ^ 1))) {
+        set_flag(p.flags, MSA_FLAG_TIMEOUT);
+        break;
+      }
+      const uint32_t fb = smem_addr(&full[s]);
+      const uint32_t dst = base + Ly.stages + s * kStageBytes;
+      const int64_t ph = static_cast<int64_t>(it.page) * p.G + it.g;   // (page, kv head) slab
+      mbar_arrive_expect_tx(fb, kStageBytes);
+      if (!kFp4) {
+        const int y = static_cast<int>(ph * kBlock);
+        tma_load_2d(dst, &tk, 0, y, fb);
+        tma_load_2d(dst + kBoxBytes, &tk, 64, y, fb);
+        tma_load_2d(dst + 2 * kBoxBytes, &tv, 0, y, fb);
+        tma_load_2d(dst + 3 * kBoxBytes, &tv, 64, y, fb);
+      } else {
+        constexpr uint32_t cb = kBlock * kDim / 2, sb = kBlock * kDim / 16;
+        bulk_g2s(dst, p.k4 + ph * cb, cb, fb, pol);
+        bulk_g2s(dst + cb, p.ks + ph * sb, sb, fb, pol);
+        bulk_g2s(dst + cb + sb, p.v4 + ph * cb, cb, fb, pol);
+        bulk_g2s(dst + 2 * cb + sb, p.vs + ph * sb, sb, fb, pol);
+      }
+      ++i;
+    }
+    const int64_t first = i > kGqaStages ? i - kGqaStages : 0;
+    for (int64_t k = first; k < i; ++k)
+      if (!mbar_wait(smem_addr(&full[k % kGqaStages]), static_cast<uint32_t>((k / kGqaStages) & 1))) break;
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers --
+  const int w = warp - 1;          // token slice [32w, 32w + 32) of every block
+  const int ct = threadIdx.x - 32; // 0..127
+  const int gr = lane >> 2, c = lane & 3;
+  uint32_t gph[2] = {0u, 0u};
+
+  uint32_t qf[8][4];
+  float o[16][4];
+  float m_r[2], l_r[2], mul_r[2];
+  int64_t seg_row = -1;
+  int seg_b = 0, seg_g = 0, seg_j = 0, seg_p = 0, seg_ell = 0;
+  int64_t i = 0;
+  bool ok = true;
+
+  auto begin_segment = [&](const Item& it) {
+    seg_row = it.row;
+    seg_b = it.b; seg_g = it.g; seg_j = it.j;
+    const int L = p.seq_lens[it.b];
+    seg_p = L - p.Q + it.j;
+    seg_ell = seg_p / kBlock;
+    const uint16_t* qh = p.q + ((static_cast<int64_t>(it.b) * p.Q + it.j) * p.H + static_cast<int64_t>(it.g) * kGroup) * kDim;
+    float qv[2][32];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint16_t* row = qh + (gr + 8 * r) * kDim + 16 * s + 2 * c;
+        const uint32_t lo = *reinterpret_cast<const uint32_t*>(row);
+        const uint32_t hi = *reinterpret_cast<const uint32_t*>(row + 8);
+        qv[r][4 * s + 0] = bf16_bits_to_f32(lo & 0xFFFF);
+        qv[r][4 * s + 1] = bf16_bits_to_f32(lo >> 16);
+        qv[r][4 * s + 2] = bf16_bits_to_f32(hi & 0xFFFF);
+        qv[r][4 * s + 3] = bf16_bits_to_f32(hi >> 16);
+      }
+    }
+    float f[2] = {1.f, 1.f};
+    if (kFp4) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(qv[r][k]));
+        amax = fmaxf(amax, __shfl_xor_sync(kAll, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(kAll, amax, 2));
+        const int sh = fp16_shift_for(amax);
+        f[r] = exp2_int(sh);
+        mul_r[r] = p.scale_log2 * p.k_global * exp2_int(-sh);
+      }
+    } else {
+      mul_r[0] = mul_r[1] = p.scale_log2;
+    }
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      if (kFp4) {
+        qf[s][0] = pack_f16x2(qv[0][4 * s] * f[0], qv[0][4 * s + 1] * f[0]);
+        qf[s][1] = pack_f16x2(qv[1][4 * s] * f[1], qv[1][4 * s + 1] * f[1]);
+        qf[s][2] = pack_f16x2(qv[0][4 * s + 2] * f[0], qv[0][4 * s + 3] * f[0]);
+        qf[s][3] = pack_f16x2(qv[1][4 * s + 2] * f[1], qv[1][4 * s + 3] * f[1]);
+      } else {
+        qf[s][0] = pack_bf16x2(qv[0][4 * s], qv[0][4 * s + 1]);
+        qf[s][1] = pack_bf16x2(qv[1][4 * s], qv[1][4 * s + 1]);
+        qf[s][2] = pack_bf16x2(qv[0][4 * s + 2], qv[0][4 * s + 3]);
+        qf[s][3] = pack_bf16x2(qv[1][4 * s + 2], qv[1][4 * s + 3]);
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    m_r[0] = m_r[1] = -INFINITY;
+    l_r[0] = l_r[1] = 0.f;
+  };
+
+  // Merges the four warps' states of the current row; writes the final output
+  // when this CTA covered the whole row, a split-K partial otherwise.
+  auto end_segment = [&]() -> bool {
+    float lt[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float v = l_r[r];
+      v += __shfl_xor_sync(kAll, v, 1);
+      v += __shfl_xor_sync(kAll, v, 2);
+      lt[r] = v;
+    }
+    float* mo = comb_o + w * kGroup * kDim;
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      *reinterpret_cast<float2*>(mo + gr * kDim + 8 * n + 2 * c) = make_float2(o[n][0], o[n][1]);
+      *reinterpret_cast<float2*>(mo + (gr + 8) * kDim + 8 * n + 2 * c) = make_float2(o[n][2], o[n][3]);
+    }
+    if (c == 0) {
+      comb_m[w * kGroup + gr] = m_r[0];
+      comb_m[w * kGroup + gr + 8] = m_r[1];
+      comb_l[w * kGroup + gr] = lt[0];
+      comb_l[w * kGroup + gr + 8] = lt[1];
+    }
+    if (!group_sync(smem_addr(&gbar[0]), gph[0], lane)) return false;
+    const int hh = ct >> 3, d0 = (ct & 7) * 16;
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kCWarps; ++k) M = fmaxf(M, comb_m[k * kGroup + hh]);
+    float fw[kCWarps];
+    float Ls = 0.f;
+#pragma unroll
+    for (int k = 0; k < kCWarps; ++k) {
+      fw[k] = M == -INFINITY ? 0.f : exp2f(comb_m[k * kGroup + hh] - M);
+      Ls += fw[k] * comb_l[k * kGroup + hh];
+    }
+    float acc[16];
+#pragma unroll
+    for (int d = 0; d < 16; ++d) {
+      float v = 0.f;
+#pragma unroll
+      for (int k = 0; k < kCWarps; ++k) v += fw[k] * comb_o[(k * kGroup + hh) * kDim + d0 + d];
+      acc[d] = v * (kFp4 ? p.v_global : 1.f);
+    }
+    const int64_t r = seg_row;
+    const bool whole = x0 <= r * p.K && (r + 1) * p.K <= x1;
+    const int64_t head = (static_cast<int64_t>(seg_b) * p.Q + seg_j) * p.H + static_cast<int64_t>(seg_g) * kGroup + hh;
+    if (whole) {
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+      uint32_t packed[8];
+#pragma unroll
+      for (int d = 0; d < 8; ++d) packed[d] = pack_bf16x2(acc[2 * d] * inv, acc[2 * d + 1] * inv);
+      uint4* dst = reinterpret_cast<uint4*>(p.out + head * kDim + d0);
+      dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+      if (p.lse != nullptr && (ct & 7) == 0) p.lse[head] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+    } else {
+      const int slot = static_cast<int>(blockIdx.x) - cta_of(r * p.K, p.W, C);
+      float* part = p.ws + (r * p.K + slot) * static_cast<int64_t>(kPartialFloats);
+      float4* dst = reinterpret_cast<float4*>(part + hh * kDim + d0);
+#pragma unroll
+      for (int d = 0; d < 4; ++d) dst[d] = make_float4(acc[4 * d], acc[4 * d + 1], acc[4 * d + 2], acc[4 * d + 3]);
+      if ((ct & 7) == 0) {
+        part[kGroup * kDim + hh] = M;
+        part[kGroup * kDim + kGroup + hh] = Ls;
+      }
+    }
+    return group_sync(smem_addr(&gbar[1]), gph[1], lane);
+  };
+
+  for (int64_t x = x0; x < x1 && ok; ++x) {
+    const Item it = decode_item(p, x, false);
+    if (it.row != seg_row) {
+      if (seg_row >= 0 && !end_segment()) { ok = false; break; }
+      begin_segment(it);
+    }
+    if (!it.valid) continue;
+    const int s = static_cast<int>(i % kGqaStages);
+    if (!mbar_wait(smem_addr(&full[s]), static_cast<uint32_t>((i / kGqaStages) & 1))) { ok = false; break; }
+    uint32_t kt = base + Ly.stages + s * kStageBytes;   // bf16 tile: K lo, K hi, V lo, V hi
+    if (kFp4) {
+      // Expand this page's NVFP4 K and V into the fp16 tile (one token row per thread).
+      const uint32_t tile = base + Ly.tiles + static_cast<uint32_t>(i & 1) * kTileBytes;
+      const uint8_t* st = sm + Ly.stages + s * kStageBytes;
+      const int t = ct;
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+        const uint8_t* codes = st + kv * (kBlock * kDim / 2 + kBlock * kDim / 16);
+        const uint8_t* scl = codes + kBlock * kDim / 2;
+        const uint32_t dbox = tile + kv * 2 * kBoxBytes;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int qq = (q + (t >> 1)) & 3;      // rotate 16-byte chunks: no bank conflicts
+          const uint4 cw = *reinterpret_cast<const uint4*>(codes + t * 64 + qq * 16);
+          const uint16_t sc2 = *reinterpret_cast<const uint16_t*>(scl + t * 8 + 2 * qq);
+          const uint32_t s2 = e4m3x2_to_f16x2(sc2);
+          const __half2 sa = __half2half2(__ushort_as_half(static_cast<unsigned short>(s2 & 0xFFFF)));
+          const __half2 sb = __half2half2(__ushort_as_half(static_cast<unsigned short>(s2 >> 16)));
+          const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {            // 8 codes -> 8 fp16 -> one 16-byte chunk
+            uint32_t h[4];
+            e2m1x4_to_f16x2x2(static_cast<uint16_t>(words[k] & 0xFFFF), h[0], h[1]);
+            e2m1x4_to_f16x2x2(static_cast<uint16_t>(words[k] >> 16), h[2], h[3]);
+            const __half2 scl2 = k < 2 ? sa : sb;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h[e]), scl2);
+              h[e] = *reinterpret_cast<uint32_t*>(&v);
+            }
+            const int chunk = 4 * qq + k;          // dims 8*chunk .. 8*chunk+7
+            const uint32_t a = swz(dbox + (chunk >> 3) * kBoxBytes, t, chunk & 7);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(h[0]), "r"(h[1]), "r"(h[2]),
+                         "r"(h[3])
+                         : "memory");
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+      if (!group_sync(smem_addr(&gbar[1]), gph[1], lane)) { ok = false; break; }
+      kt = tile;
+    }
+
+    // ---- S = Q K^T for this warp's 32 tokens (4 n-tiles of 8 tokens).
+    float sc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+      const int tok = 32 * w + 8 * nt + (lane & 7);
+#pragma unroll
+      for (int sp = 0; sp < 4; ++sp) {
+        const int chunk = 4 * sp + (lane >> 3);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(swz(kt + (chunk >> 3) * kBoxBytes, tok, chunk & 7), b0, b1, b2, b3);
+        if (kFp4) {
+          mma_f16(sc[nt], qf[2 * sp], b0, b1);
+          mma_f16(sc[nt], qf[2 * sp + 1], b2, b3);
+        } else {
+          mma_bf16(sc[nt], qf[2 * sp], b0, b1);
+          mma_bf16(sc[nt], qf[2 * sp + 1], b2, b3);
+        }
+      }
+    }
+    // ---- causal limit inside the local block
+    if (it.blk == seg_ell) {
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int t0 = it.blk * kBlock + 32 * w + 8 * nt + 2 * c;
+        if (t0 > seg_p) { sc[nt][0] = -INFINITY; sc[nt][2] = -INFINITY; }
+        if (t0 + 1 > seg_p) { sc[nt][1] = -INFINITY; sc[nt][3] = -INFINITY; }
+      }
+    }
+    // ---- online softmax (log2 domain), rows gr and gr + 8
+    float pr[4][4];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) mx = fmaxf(mx, fmaxf(sc[nt][2 * r], sc[nt][2 * r + 1]));
+      mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 2));
+      const float mnew = fmaxf(m_r[r], mx * mul_r[r]);
+      const float alpha = mnew == -INFINITY ? 1.f : exp2f(m_r[r] - mnew);
+      float ls = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float v = sc[nt][2 * r + e];
+          const float pv = (v == -INFINITY || mnew == -INFINITY) ? 0.f : exp2f(v * mul_r[r] - mnew);
+          pr[nt][2 * r + e] = pv;
+          ls += pv;
+        }
+      }
+      l_r[r] = l_r[r] * alpha + ls;
+      m_r[r] = mnew;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        o[n][2 * r] *= alpha;
+        o[n][2 * r + 1] *= alpha;
+      }
+    }
+    // ---- O += P V (2 k-steps of 16 tokens, 16 n-tiles of 8 dims)
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      uint32_t a[4];
+      if (kFp4) {
+        a[0] = pack_f16x2(pr[2 * kk][0], pr[2 * kk][1]);
+        a[1] = pack_f16x2(pr[2 * kk][2], pr[2 * kk][3]);
+        a[2] = pack_f16x2(pr[2 * kk + 1][0], pr[2 * kk + 1][1]);
+        a[3] = pack_f16x2(pr[2 * kk + 1][2], pr[2 * kk + 1][3]);
+      } else {
+        a[0] = pack_bf16x2(pr[2 * kk][0], pr[2 * kk][1]);
+        a[1] = pack_bf16x2(pr[2 * kk][2], pr[2 * kk][3]);
+        a[2] = pack_bf16x2(pr[2 * kk + 1][0], pr[2 * kk + 1][1]);
+        a[3] = pack_bf16x2(pr[2 * kk + 1][2], pr[2 * kk + 1][3]);
+      }
+      const int tok = 32 * w + 16 * kk + 8 * ((lane >> 3) & 1) + (lane & 7);
+#pragma unroll
+      for (int np = 0; np < 8; ++np) {
+        const int chunk = 2 * np + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(swz(kt + 2 * kBoxBytes + (chunk >> 3) * kBoxBytes, tok, chunk & 7), b0, b1, b2, b3);
+        if (kFp4) {
+          mma_f16(o[2 * np], a, b0, b1);
+          mma_f16(o[2 * np + 1], a, b2, b3);
+        } else {
+          mma_bf16(o[2 * np], a, b0, b1);
+          mma_bf16(o[2 * np + 1], a, b2, b3);
+        }
+      }
+    }
+    if (!kFp4) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+    }
+    ++i;
+  }
+  if (ok && seg_row >= 0) ok = end_segment();
+  if (!ok && lane == 0) set_flag(p.flags, MSA_FLAG_TIMEOUT);
+}
+
+// Merges the split-K partials of every (row, head) whose row spans several CTAs.
+__global__ void __launch_bounds__(256) gqa_combine_kernel(GqaParams p, int C) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t rows = p.W / p.K;
+  if (wid >= rows * kGroup) return;
+  const int64_t r = wid / kGroup;
+  const int hh = static_cast<int>(wid % kGroup);
+  const int first = cta_of(r * p.K, p.W, C), last = cta_of(r * p.K + p.K - 1, p.W, C);
+  if (first == last) return;   // written directly by the attention kernel
+  const int j = static_cast<int>(r % p.Q);
+  const int g = static_cast<int>((r / p.Q) % p.G);
+  const int b = static_cast<int>(r / (static_cast<int64_t>(p.Q) * p.G));
+  const float* base = p.ws + r * p.K * static_cast<int64_t>(kPartialFloats);
+  const int n = last - first + 1;
+  float M = -INFINITY;
+  for (int s = 0; s < n; ++s) M = fmaxf(M, base[s * kPartialFloats + kGroup * kDim + hh]);
+  float Ls = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) {
+    for (int s = 0; s < n; ++s) {
+      const float* part = base + s * kPartialFloats;
+      const float f = exp2f(part[kGroup * kDim + hh] - M);
+      Ls += f * part[kGroup * kDim + kGroup + hh];
+      const float4 v = *reinterpret_cast<const float4*>(part + hh * kDim + 4 * lane);
+      acc.x += f * v.x; acc.y += f * v.y; acc.z += f * v.z; acc.w += f * v.w;
+    }
+  }
+  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+  const int64_t head = (static_cast<int64_t>(b) * p.Q + j) * p.H + static_cast<int64_t>(g) * kGroup + hh;
+  uint2 packed = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  *reinterpret_cast<uint2*>(p.out + head * kDim + 4 * lane) = packed;
+  if (p.lse != nullptr && lane == 0) p.lse[head] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+}
+
+size_t gqa_workspace_bytes(int B, int Q, int G, int K) {
+  return static_cast<size_t>(B) * Q * G * K * kPartialFloats * sizeof(float);
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up through the runtime so the
+// library does not link libcuda directly.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D map over a bf16 cache [P*G*BS rows, 128 dims]; 128-row x 64-dim boxes, 128 B swizzle.
+static cudaError_t make_kv_map(CUtensorMap* map, const void* base, int64_t rows) {
+  EncodeTiledFn fn = encode_tiled();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlock)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRecord* rec) {
+  GqaParams p;
+  p.q = a.q;
+  p.block_table = a.block_table;
+  p.seq_lens = a.seq_lens;
+  p.selected = a.selected;
+  p.out = a.out;
+  p.lse = a.lse;
+  p.ws = a.workspace;
+  p.flags = a.flags;
+  p.k4 = static_cast<const uint8_t*>(a.k);
+  p.v4 = static_cast<const uint8_t*>(a.v);
+  p.ks = a.k_scale;
+  p.vs = a.v_scale;
+  p.k_global = a.k_global;
+  p.v_global = a.v_global;
+  p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
+  p.B = a.B; p.Q = a.Q; p.H = a.H; p.G = a.G; p.NB = a.NB; p.P = a.P; p.K = a.K;
+  p.W = static_cast<int64_t>(a.B) * a.G * a.Q * a.K;
+  if (p.W == 0) {
+    rec->set("sparse_gqa empty");
+    return cudaSuccess;
+  }
+  CUtensorMap tk, tv;
+  memset(&tk, 0, sizeof(tk));
+  memset(&tv, 0, sizeof(tv));
+  const int64_t rows = static_cast<int64_t>(a.P) * a.G * kBlock;
+  cudaError_t err;
+  if (!a.nvfp4) {
+    if ((err = make_kv_map(&tk, a.k, rows)) != cudaSuccess) return err;
+    if ((err = make_kv_map(&tv, a.v, rows)) != cudaSuccess) return err;
+  }
+  const int sms = device_sm_count();
+  const int C = static_cast<int>(p.W < sms ? p.W : sms);
+  const size_t smem = (a.nvfp4 ? gqa_layout<true>().total : gqa_layout<false>().total) + 1024;
+  if (a.nvfp4) {
+    err = cudaFuncSetAttribute(sparse_gqa_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    sparse_gqa_kernel<true><<<C, 32 * (1 + kCWarps), smem, stream>>>(tk, tv, p);
+  } else {
+    err = cudaFuncSetAttribute(sparse_gqa_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    sparse_gqa_kernel<false><<<C, 32 * (1 + kCWarps), smem, stream>>>(tk, tv, p);
+  }
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  const int64_t warps = (p.W / p.K) * kGroup;
+  const int64_t cgrid = (warps + 7) / 8;
+  gqa_combine_kernel<<<static_cast<unsigned>(cgrid), 256, 0, stream>>>(p, C);
+  rec->set("sparse_gqa %s split_k persistent grid=%d block=%d smem=%zu stages=%d items=%lld + combine grid=%lld",
+           a.nvfp4 ? "nvfp4_dequant_f16_mma" : "bf16_tma_mma", C, 32 * (1 + kCWarps), smem, kGqaStages,
+           static_cast<long long>(p.W), static_cast<long long>(cgrid));
+  return cudaGetLastError();
+}
+
+}  // namespace msa

@@ -1,0 +1,125 @@
+"""Device-resident MSA decode workloads built from the seeded generator.
+
+Allocates the paged caches and per-step buffers with torch (device memory
+only), fills the caches through the library's own insert/quantise kernel, and
+runs decode steps through the C ABI. Nothing here computes any part of the
+method on the host.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import msa, synth
+
+
+def _bf16(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+
+class DeviceWorkload:
+    """All device state of one workload: caches, queries, block table, outputs.
+
+    ``which`` restricts the batch to a subset of requests (keeping their
+    seeded streams), so tests can run full-length requests of a large workload.
+    """
+
+    def __init__(self, w: synth.Workload, device="cuda", which=None, lens=None, workers: int = 8):
+        self.w = w
+        self.device = torch.device(device)
+        full_lens = synth.seq_lens(w) if lens is None else np.asarray(lens, dtype=np.int32)
+        self.which = list(range(w.batch)) if which is None else list(which)
+        self.lens = full_lens[self.which].astype(np.int32)
+        B = len(self.which)
+        sub = synth.scaled(w, batch=B)
+        self.block_table, self.num_pages = synth.page_table(sub, self.lens)
+        nb = int(self.block_table.shape[1])
+        self.dims = msa.make_dims(B, w.q_len, w.n_heads, w.n_kv_heads, w.n_idx_heads, w.head_dim, w.block_size,
+                                  nb, self.num_pages, w.topk, 1, w.softmax_scale)
+        dev = self.device
+        P, G, I, D, BS, Q, H = self.num_pages, w.n_kv_heads, w.n_idx_heads, w.head_dim, w.block_size, w.q_len, w.n_heads
+        if w.kv_dtype == "bf16":
+            self.cache = msa.KVCache(msa.BF16, torch.zeros((P, G, BS, D), dtype=torch.bfloat16, device=dev),
+                                     torch.zeros((P, G, BS, D), dtype=torch.bfloat16, device=dev))
+        else:
+            g = float(np.float32(synth.NVFP4_SYNTH_GLOBAL))
+            self.cache = msa.KVCache(msa.NVFP4, torch.zeros((P, G, BS, D // 2), dtype=torch.uint8, device=dev),
+                                     torch.zeros((P, G, BS, D // 2), dtype=torch.uint8, device=dev),
+                                     torch.zeros((P, G, BS, D // 16), dtype=torch.uint8, device=dev),
+                                     torch.zeros((P, G, BS, D // 16), dtype=torch.uint8, device=dev), g, g)
+        if w.idx_dtype == "f32":
+            self.idx_cache = msa.IndexCache(msa.F32, torch.zeros((P, I, BS, D), dtype=torch.float32, device=dev))
+            self.q_idx_dtype = msa.F32
+            self.idx_new_dtype = msa.F32
+        else:
+            self.idx_cache = msa.IndexCache(msa.FP8_E4M3, torch.zeros((P, I, BS, D), dtype=torch.uint8, device=dev),
+                                            torch.zeros((P, I, BS), dtype=torch.float32, device=dev))
+            self.q_idx_dtype = msa.BF16
+            self.idx_new_dtype = msa.BF16
+        self.flags = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.seq_lens_d = torch.from_numpy(self.lens).to(dev)
+        self.block_table_d = torch.from_numpy(self.block_table).to(dev)
+
+        q = np.empty((B, Q, H, D), dtype=np.uint16)
+        qi = np.empty((B, Q, I, D), dtype=np.float32 if w.idx_dtype == "f32" else np.uint16)
+        # the last Q tokens of each request: the tokens a decode step inserts
+        new_k = np.empty((B, Q, G, D), dtype=np.uint16)
+        new_v = np.empty((B, Q, G, D), dtype=np.uint16)
+        new_i = np.empty((B, Q, I, D), dtype=qi.dtype)
+        new_slots = np.empty((B, Q), dtype=np.int64)
+        for bi, (b, r) in enumerate(synth.requests(w, full_lens, self.which, workers=workers)):
+            L = int(full_lens[b])
+            q[bi] = r["q"]
+            qi[bi] = r["q_idx"]
+            slots = synth.slot_mapping(sub, self.block_table, bi, L)
+            new_k[bi], new_v[bi], new_i[bi] = r["k"][L - Q:], r["v"][L - Q:], r["idx_k"][L - Q:]
+            new_slots[bi] = slots[L - Q:]
+            self._insert(r["k"], r["v"], r["idx_k"], slots)
+        self.q = _bf16(q).to(dev)
+        self.q_idx = (torch.from_numpy(qi) if w.idx_dtype == "f32" else _bf16(qi)).to(dev)
+        self.new_k = _bf16(new_k.reshape(B * Q, G, D)).to(dev)
+        self.new_v = _bf16(new_v.reshape(B * Q, G, D)).to(dev)
+        self.new_idx = (torch.from_numpy(new_i) if w.idx_dtype == "f32" else _bf16(new_i)).reshape(B * Q, I, D).to(dev)
+        self.new_slots = torch.from_numpy(new_slots.reshape(-1)).to(dev)
+        self.scores = torch.empty((B, Q, I, nb), dtype=torch.float32, device=dev)
+        self.selected = torch.empty((B, Q, I, w.topk), dtype=torch.int32, device=dev)
+        self.out = torch.empty((B, Q, H, D), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((B, Q, H), dtype=torch.float32, device=dev)
+        ws = msa.sparse_gqa_workspace_size(self.dims, self.cache.dtype)
+        self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize(dev)
+
+    def _insert(self, k, v, idx, slots):
+        dev = self.device
+        kd = _bf16(k).to(dev)
+        vd = _bf16(v).to(dev)
+        idd = (torch.from_numpy(idx) if idx.dtype == np.float32 else _bf16(idx)).to(dev)
+        sd = torch.from_numpy(slots).to(dev)
+        msa.kv_insert_quant(self.dims, kd, vd, idd, self.idx_new_dtype, sd, self.cache, self.idx_cache, self.flags)
+
+    # ------------------------------------------------------------ stages --
+    def insert_step_tokens(self, stream=None):
+        msa.kv_insert_quant(self.dims, self.new_k, self.new_v, self.new_idx, self.idx_new_dtype, self.new_slots,
+                            self.cache, self.idx_cache, self.flags, stream)
+
+    def index_score(self, stream=None):
+        msa.index_score(self.dims, self.q_idx, self.q_idx_dtype, self.idx_cache, self.block_table_d,
+                        self.seq_lens_d, self.scores, self.flags, stream)
+
+    def select(self, stream=None):
+        msa.select_blocks(self.dims, self.scores, self.seq_lens_d, self.selected, self.flags, stream)
+
+    def attend(self, stream=None, selected=None):
+        msa.sparse_gqa_decode(self.dims, self.q, self.cache, self.block_table_d, self.seq_lens_d,
+                              self.selected if selected is None else selected, self.out, self.lse, self.workspace,
+                              self.flags, stream)
+
+    def step(self, stream=None):
+        """One decode step: insert this step's tokens, score, select, attend."""
+        self.insert_step_tokens(stream)
+        self.index_score(stream)
+        self.select(stream)
+        self.attend(stream)
+
+    def check_flags(self) -> int:
+        return msa.read_device_flags(self.flags)

@@ -1,0 +1,217 @@
+/*
+ * msa.h — C ABI of libmsa.so: the decode hot path of MiniMax Sparse Attention
+ * (MSA) on one GB300 GPU (sm_103a).
+ *
+ * The method (sources named by page title and section):
+ *   "MiniMax M3 vLLM サポート：1M トークンマルチモーダル推論の Day-0 サービング"
+ *   (agentlenshq.com), section "MSA 実行プロセス": every query token goes
+ *   through 1) block scoring by a small index head, 2) top-k block selection
+ *   with local_blocks=1, 3) sparse GQA with online softmax over the selected
+ *   blocks only; section "KV キャッシュ統合": the KV data stays an ordinary
+ *   paged cache; section "EAGLE3 を用いた投機的デコード": a decode-only split-K
+ *   path serves a unified decode_query_len (speculative verification).
+ *   "MiniMax-M3.1-Flash Day-0 対応" (aisoku.org), section "MSAの仕組み":
+ *   128-token blocks, top blocks plus the most recent block, at most 2,048 keys
+ *   per query; section "何が新しいか": NVFP4 KV cache.
+ *   "vLLM、AMD Instinct MI355X上でMiniMax M3のボトルネック最適化手法を公開"
+ *   (news.ainew.jp), question 1: 64 query heads, 4 KV heads, 4 index heads;
+ *   question 2: the indexer covers all draft positions of a request per key
+ *   load and drops the positive score scale; question 5: a keys-only index
+ *   cache sits beside the K/V cache.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named in a struct or argument list are DEVICE pointers unless
+ *     the comment says "host". All memory is owned by the caller; the library
+ *     allocates nothing and keeps no pointer after a call returns.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream). Only msa_read_device_flags
+ *     synchronises.
+ *   - Host-side validation runs before any launch. A status other than MSA_OK
+ *     means nothing was launched (MSA_ERR_CUDA: a launch was attempted and the
+ *     CUDA runtime reported an error).
+ *   - Inputs that only the device can check (page ids in the block table,
+ *     selected block ids, context lengths, cache slots) are checked by the
+ *     kernels: an offending block or token is skipped and a bit is OR-ed into
+ *     `*dev_flags` (a caller-owned device uint32 that the caller zeroes). No
+ *     kernel traps, and every wait inside a kernel is bounded in time.
+ *   - Shapes: B batch, Q query positions per request (decode_query_len), H
+ *     query heads, G KV heads, I index heads (I == G), D head_dim (128),
+ *     BS block size (128), P pages, NB max_blocks_per_seq, K topk.
+ *     Query j of request b sits at position p = seq_lens[b] - Q + j; its
+ *     local block is p / BS.
+ *   - The dispatch record (msa_get_last_dispatch) is thread-local and names
+ *     the kernel variant and launch shape that actually ran.
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MSA_ABI_VERSION 1
+
+typedef enum {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
+  MSA_ERR_UNSUPPORTED = 2,   /* valid request outside what the kernels implement */
+  MSA_ERR_CUDA = 3,          /* the CUDA runtime reported an error at launch */
+  MSA_ERR_WORKSPACE = 4,     /* workspace null or smaller than msa_sparse_gqa_workspace_size */
+  MSA_ERR_DEVICE_FLAG = 5    /* msa_read_device_flags found a kernel-reported problem */
+} msa_status_t;
+
+typedef enum {
+  MSA_F32 = 0,
+  MSA_BF16 = 1,
+  MSA_FP8_E4M3 = 2,
+  MSA_NVFP4 = 3
+} msa_dtype_t;
+
+/* Bits a kernel may OR into *dev_flags. */
+#define MSA_FLAG_BAD_PAGE      0x1u  /* block_table entry outside [0, num_pages) */
+#define MSA_FLAG_BAD_BLOCK     0x2u  /* selected block id beyond the query's local block */
+#define MSA_FLAG_BAD_SEQLEN    0x4u  /* seq_lens[b] < q_len or > max_blocks_per_seq * BS */
+#define MSA_FLAG_BAD_SLOT      0x8u  /* slot_mapping entry >= num_pages * BS */
+#define MSA_FLAG_TIMEOUT       0x10u /* a bounded wait inside a kernel gave up */
+#define MSA_FLAG_Q_RANGE       0x20u /* an index-query row too large for the fp16 operand path */
+
+/* Problem shape (host struct). block_size must be 128, head_dim 128,
+ * local_blocks 1, n_idx_heads == n_kv_heads, n_heads % n_kv_heads == 0,
+ * 1 <= topk <= 16, 1 <= q_len <= 8. */
+typedef struct {
+  int32_t batch;               /* B */
+  int32_t q_len;               /* Q, query positions per request */
+  int32_t n_heads;             /* H */
+  int32_t n_kv_heads;          /* G */
+  int32_t n_idx_heads;         /* I */
+  int32_t head_dim;            /* D */
+  int32_t block_size;          /* BS */
+  int32_t max_blocks_per_seq;  /* NB, columns of block_table and scores */
+  int32_t num_pages;           /* P */
+  int32_t topk;                /* K, blocks selected per (b, j, head), local block included */
+  int32_t local_blocks;        /* must be 1 */
+  float softmax_scale;         /* logits = softmax_scale * q.k */
+} msa_dims_t;
+
+/* Paged K/V cache of one layer (host struct holding device pointers).
+ *   MSA_BF16:  k, v  = bf16 [P, G, BS, D]; k_scale = v_scale = NULL.
+ *   MSA_NVFP4: k, v  = uint8 [P, G, BS, D/2] E2M1 pairs, low nibble = even
+ *              element; k_scale, v_scale = uint8 E4M3 [P, G, BS, D/16], one
+ *              per 16 consecutive elements; k_global, v_global = fp32
+ *              per-tensor scales (host values, > 0).
+ *   value = e2m1 * e4m3_scale * global. 16-byte aligned pointers. */
+typedef struct {
+  msa_dtype_t dtype;
+  void* k;
+  void* v;
+  void* k_scale;
+  void* v_scale;
+  float k_global;
+  float v_global;
+} msa_kv_cache_t;
+
+/* Keys-only index cache of one layer (host struct holding device pointers).
+ *   MSA_F32:      keys = fp32 [P, I, BS, D]; scale = NULL.
+ *   MSA_FP8_E4M3: keys = uint8 E4M3 [P, I, BS, D]; scale = fp32 [P, I, BS],
+ *                 one per (token, index head); key value = e4m3 * scale.
+ *   16-byte aligned pointers. */
+typedef struct {
+  msa_dtype_t dtype;
+  void* keys;
+  float* scale;
+} msa_index_cache_t;
+
+/* ABI version of the loaded library (MSA_ABI_VERSION at build time). */
+int msa_abi_version(void);
+
+/* Human-readable name of a status. Never NULL. */
+const char* msa_status_string(msa_status_t status);
+
+/* Copies the thread-local record of the last kernel launch into buf (NUL
+ * terminated, truncated to len). */
+msa_status_t msa_get_last_dispatch(char* buf, size_t len);
+
+/*
+ * Cache insertion and quantisation: writes num_tokens new tokens into the
+ * paged caches. The pages give the caches (paged KV, a keys-only index cache,
+ * NVFP4 KV, an FP8 indexer on the roadmap) but no quantisation rule; the rule
+ * implemented is:
+ *   FP8 index keys: s = amax / 448 over the token's D values of that head (fp32,
+ *     IEEE division), code = E4M3_RNE_satfinite(x / s); s = 0 -> codes 0.
+ *   NVFP4 K/V: per 16 values sb = E4M3_RNE((amax16 / 6) / global),
+ *     code = E2M1_RNE_satfinite(x / (sb * global)); sb == 0 -> codes 0.
+ *   bf16 K/V and fp32 index keys are copied.
+ * k_new, v_new: bf16 [T, G, D]. idx_k_new: [T, I, D] of idx_new_dtype
+ * (MSA_F32 or MSA_BF16; MSA_BF16 requires an FP8 index cache), or NULL to
+ * leave the index cache untouched (idx_cache may then be NULL).
+ * slot_mapping: int64 [T], slot = page * BS + offset; a negative slot skips
+ * the token; slot >= P * BS skips it and sets MSA_FLAG_BAD_SLOT.
+ */
+msa_status_t msa_kv_insert_quant(const msa_dims_t* dims, const void* k_new, const void* v_new,
+                                 const void* idx_k_new, msa_dtype_t idx_new_dtype,
+                                 const int64_t* slot_mapping, int32_t num_tokens,
+                                 const msa_kv_cache_t* cache, const msa_index_cache_t* idx_cache,
+                                 uint32_t* dev_flags, void* stream);
+
+/*
+ * Stage 1, block scoring ("MSA 実行プロセス" step 1). For every request b,
+ * position j, index head g and block n < l_j (the query's local block):
+ *   scores[b, j, g, n] = max over the block's 128 tokens t of s_t * (q_idx[b, j, g] . k_t)
+ * with s_t the key's per-token scale (1 for fp32 keys); no other scale is
+ * applied (a positive constant cannot change the selection). All other
+ * entries up to max_blocks_per_seq are set to -inf. All Q positions of a
+ * request are computed from one load of each index key.
+ * idx_q: [B, Q, I, D] in q_dtype (MSA_F32 with an MSA_F32 index cache,
+ * MSA_BF16 with an MSA_FP8_E4M3 one). block_table: int32 [B, NB].
+ * seq_lens: int32 [B]. scores: fp32 [B, Q, I, NB].
+ */
+msa_status_t msa_index_score(const msa_dims_t* dims, const void* idx_q, msa_dtype_t q_dtype,
+                             const msa_index_cache_t* idx_cache, const int32_t* block_table,
+                             const int32_t* seq_lens, float* scores, uint32_t* dev_flags,
+                             void* stream);
+
+/*
+ * Stage 2, block selection ("MSA 実行プロセス" step 2, local_blocks=1). For
+ * every (b, j, g): order the candidates n < l_j by score (higher first, then
+ * lower block id), keep the first min(K-1, l_j), add l_j, and write them in
+ * ascending order followed by -1 padding: selected int32 [B, Q, G, K].
+ * Scores are compared as exact fp32 values (NaN counts as -inf).
+ */
+msa_status_t msa_select_blocks(const msa_dims_t* dims, const float* scores, const int32_t* seq_lens,
+                               int32_t* selected, uint32_t* dev_flags, void* stream);
+
+/* Bytes of device workspace msa_sparse_gqa_decode needs for this shape. */
+size_t msa_sparse_gqa_workspace_size(const msa_dims_t* dims, msa_dtype_t kv_dtype);
+
+/*
+ * Stage 3, sparse GQA decode ("MSA 実行プロセス" step 3; split-K decode path
+ * of "EAGLE3 を用いた投機的デコード"). For every query head h of position j of
+ * request b, with KV head g = h / (H / G), over the tokens t of the blocks in
+ * selected[b, j, g, :] (entries < 0 ignored) with t <= p:
+ *   out[b, j, h] = sum_t softmax_t(softmax_scale * q . k_t) * v_t
+ *   lse[b, j, h] = log sum_t exp(softmax_scale * q . k_t)
+ * The work is split over the selected blocks and the partial results merged
+ * with a log-sum-exp combine. K/V are read from bf16 or NVFP4 pages and
+ * dequantised in the kernel.
+ * q: bf16 [B, Q, H, D]. out: bf16 [B, Q, H, D]. lse: fp32 [B, Q, H] or NULL.
+ * workspace: device scratch of at least msa_sparse_gqa_workspace_size bytes,
+ * 256-byte aligned; its contents need no initialisation and are not
+ * meaningful after the call.
+ */
+msa_status_t msa_sparse_gqa_decode(const msa_dims_t* dims, const void* q, const msa_kv_cache_t* cache,
+                                   const int32_t* block_table, const int32_t* seq_lens,
+                                   const int32_t* selected, void* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, uint32_t* dev_flags, void* stream);
+
+/* Synchronises `stream`, copies *dev_flags to *host_flags (host pointer) and
+ * returns MSA_ERR_DEVICE_FLAG if any bit is set, MSA_OK otherwise. */
+msa_status_t msa_read_device_flags(const uint32_t* dev_flags, uint32_t* host_flags, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */

@@ -25,7 +25,7 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+def e4m3_from_fields(codes: np.ndarray) -> np.ndarray:
     """E4M3 byte -> fp64, by the bit-field definition."""
     c = np.asarray(codes).astype(np.int64)
     sign = np.where(c & 0x80, -1.0, 1.0)
@@ -36,7 +36,7 @@ def e4m3_decode(codes: np.ndarray) -> np.ndarray:
     return sign * mag
 
 
-def e2m1_decode(nibbles: np.ndarray) -> np.ndarray:
+def e2m1_from_fields(nibbles: np.ndarray) -> np.ndarray:
     """E2M1 nibble -> fp64, by the bit-field definition (bias 1, 1 mantissa bit)."""
     c = np.asarray(nibbles).astype(np.int64) & 0xF
     sign = np.where(c & 0x8, -1.0, 1.0)
@@ -44,6 +44,19 @@ def e2m1_decode(nibbles: np.ndarray) -> np.ndarray:
     m = (c & 0x1).astype(np.float64)
     mag = np.where(e == 0, (m / 2.0) * 2.0 ** 0, (1.0 + m / 2.0) * np.power(2.0, (e - 1).astype(np.float64)))
     return sign * mag
+
+
+# Decoding large arrays goes through the tables of all codes built from the definitions above.
+_E4M3_TABLE = e4m3_from_fields(np.arange(256))
+_E2M1_TABLE = e2m1_from_fields(np.arange(16))
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    return _E4M3_TABLE[np.asarray(codes).astype(np.uint8)]
+
+
+def e2m1_decode(nibbles: np.ndarray) -> np.ndarray:
+    return _E2M1_TABLE[np.asarray(nibbles).astype(np.uint8) & 0xF]
 
 
 # Non-negative finite values, indexed by code (ascending in value).

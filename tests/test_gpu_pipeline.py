@@ -1,0 +1,69 @@
+"""Parity of the whole decode step (insert, score, select, attend) against the oracle.
+
+Reduced-size versions of every workload (several tiles, ragged tails) are
+checked request by request; the full-size workloads run in the same launch
+configuration as the benchmark and are checked on sampled requests.
+"""
+import numpy as np
+import pytest
+
+from block_sparse_attention_07_gb300 import synth
+
+import parity
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+
+REDUCED = {
+    "tiny": W["tiny"],
+    "b32_32k": synth.scaled(W["b32_32k"], batch=3, ctx=2000),
+    "ragged": synth.scaled(W["ragged"], batch=5, ctx_range=(300, 5000)),
+    "spec8": synth.scaled(W["spec8"], batch=3, ctx=3000),
+    "nvfp4_256k": synth.scaled(W["nvfp4_256k"], batch=2, ctx=3000),
+}
+
+
+@pytest.mark.parametrize("name", list(REDUCED))
+def test_reduced_workload(name):
+    w = REDUCED[name]
+    dw = parity.build(w)
+    parity.verify_workload(dw, w, synth.seq_lens(w))
+
+
+EDGE_LENS = {
+    # (workload base, lengths): L < 128 (no candidates), exact multiples +-1,
+    # fewer candidates than k-1, long enough for a full top-16.
+    "short_and_multiples": ("b32_32k", [1, 5, 127, 128, 129, 255, 256, 257, 1919, 1920, 1921, 2100]),
+    "spec_straddle": ("spec8", [8, 9, 130, 135, 136, 1028, 2948, 2951, 2952]),
+    "nvfp4_edges": ("nvfp4_256k", [1, 128, 129, 1500, 2049]),
+    "tiny_f32_edges": ("tiny", [1, 200, 4095]),
+}
+
+
+@pytest.mark.parametrize("case", list(EDGE_LENS))
+def test_edge_lengths(case):
+    base, lens = EDGE_LENS[case]
+    w = synth.scaled(W[base], batch=len(lens), ctx=None, ctx_range=None)
+    lens = np.array(lens, dtype=np.int32)
+    dw = parity.build(w, lens=lens)
+    parity.verify_workload(dw, w, lens)
+
+
+@pytest.mark.parametrize("topk", [1, 2, 7, 16])
+def test_topk_values(topk):
+    w = synth.scaled(W["b32_32k"], batch=2, ctx=3100, topk=topk)
+    dw = parity.build(w)
+    parity.verify_workload(dw, w, synth.seq_lens(w))
+
+
+@pytest.mark.parametrize("name", list(W))
+def test_full_size_sampled(name):
+    """Full-size workload, benchmark launch configuration, two sampled requests."""
+    w = W[name]
+    dw = parity.build(w)
+    lens = synth.seq_lens(w)
+    dw.step()
+    dw.step()          # a second step (the benchmark repeats steps) gives the same result
+    sample = [0, len(dw.which) - 1]
+    parity.verify_workload(dw, w, lens, sample=sample, run_step=False)
