@@ -182,6 +182,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = synth.WORKLOADS[args.workload]
+    if args.batch:
+        w = synth.scaled(w, batch=args.batch)
     dw = DeviceWorkload(w, dev)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
@@ -348,6 +350,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--workload", default="b32_32k")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch size (smaller profiling cases)")
     ap.add_argument("--cpu-requests", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
