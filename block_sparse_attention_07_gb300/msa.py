@@ -25,7 +25,7 @@ FLAG_BAD_PAGE, FLAG_BAD_BLOCK, FLAG_BAD_SEQLEN, FLAG_BAD_SLOT, FLAG_TIMEOUT, FLA
 # Every function include/msa.h declares.
 EXPORTED = ("msa_abi_version", "msa_status_string", "msa_get_last_dispatch", "msa_kv_insert_quant",
             "msa_index_score", "msa_select_blocks", "msa_sparse_gqa_workspace_size", "msa_sparse_gqa_decode",
-            "msa_read_device_flags")
+            "msa_sparse_gqa_decode_noalloc", "msa_read_device_flags")
 
 
 class Dims(ctypes.Structure):
@@ -70,6 +70,8 @@ def _load():
     lib.msa_sparse_gqa_workspace_size.argtypes = [ctypes.POINTER(Dims), ctypes.c_int]
     lib.msa_sparse_gqa_decode.argtypes = [ctypes.POINTER(Dims), vp, ctypes.POINTER(_KVCache), vp, vp, vp, vp, vp,
                                           vp, sz, vp, vp]
+    lib.msa_sparse_gqa_decode_noalloc.argtypes = [ctypes.POINTER(Dims), vp, ctypes.POINTER(_KVCache), vp, vp, vp,
+                                                  vp, vp, vp, vp]
     lib.msa_read_device_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
     for name in EXPORTED:
         if name != "msa_abi_version" and name != "msa_status_string":
@@ -178,6 +180,17 @@ def sparse_gqa_decode(dims: Dims, q, cache: KVCache, block_table, seq_lens, sele
                                    _ptr(seq_lens), _ptr(selected), _ptr(out), _ptr(lse), _ptr(workspace), nbytes,
                                    _ptr(flags), _stream(stream))
     _check(st, "msa_sparse_gqa_decode")
+
+
+def sparse_gqa_decode_noalloc(dims: Dims, q, cache: KVCache, block_table, seq_lens, selected, out, lse, flags,
+                              stream=None):
+    """msa_sparse_gqa_decode without a workspace argument, for callers that cannot allocate
+    device memory; its scratch is a fixed 64 MiB array inside the library (see include/msa.h)."""
+    kc = cache.c()
+    st = lib.msa_sparse_gqa_decode_noalloc(ctypes.byref(dims), _ptr(q), ctypes.byref(kc), _ptr(block_table),
+                                           _ptr(seq_lens), _ptr(selected), _ptr(out), _ptr(lse), _ptr(flags),
+                                           _stream(stream))
+    _check(st, "msa_sparse_gqa_decode_noalloc")
 
 
 def read_device_flags(flags, stream=None) -> int:

@@ -206,6 +206,26 @@ msa_status_t msa_sparse_gqa_decode(const msa_dims_t* dims, const void* q, const 
                                    const int32_t* selected, void* out, float* lse, void* workspace,
                                    size_t workspace_bytes, uint32_t* dev_flags, void* stream);
 
+/*
+ * Allocation-free variant of msa_sparse_gqa_decode. The pages have no
+ * counterpart: it exists for callers that cannot allocate device memory (a
+ * process whose allocator owns all device memory, a plugin that receives only
+ * its input and output buffers, tooling that must not change the device's
+ * memory footprint). Same arguments and results as msa_sparse_gqa_decode,
+ * without the workspace: the split-K partials go to a 64 MiB array inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits. The first call on a device looks up that array's address (make it
+ * before any stream capture on that device). All calls on a device share the
+ * array, so calls whose kernels overlap on the GPU race; nothing in it needs
+ * to start at zero. Shapes that need more than 64 MiB
+ * (B * Q * G * topk * 8,320 bytes) return MSA_ERR_WORKSPACE without launching.
+ * Calls no allocating routine.
+ */
+msa_status_t msa_sparse_gqa_decode_noalloc(const msa_dims_t* dims, const void* q, const msa_kv_cache_t* cache,
+                                           const int32_t* block_table, const int32_t* seq_lens,
+                                           const int32_t* selected, void* out, float* lse, uint32_t* dev_flags,
+                                           void* stream);
+
 /* Synchronises `stream`, copies *dev_flags to *host_flags (host pointer) and
  * returns MSA_ERR_DEVICE_FLAG if any bit is set, MSA_OK otherwise. */
 msa_status_t msa_read_device_flags(const uint32_t* dev_flags, uint32_t* host_flags, void* stream);
