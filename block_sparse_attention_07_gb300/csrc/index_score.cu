@@ -125,38 +125,55 @@ __global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_ke
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer --
-    if (lane != 0) return;
+    // The whole warp fetches the page ids of the next 32 units at once (one
+    // chunk ahead); lane 0 issues the copies.
     const uint64_t pol = l2_evict_first_policy();
     const uint8_t* keys = static_cast<const uint8_t*>(p.keys);
-    int b = b_first;
+    auto page_of = [&](int64_t u) -> int {
+      if (u >= u1) return -1;
+      const int bb = find_request(pref, p.B, u);
+      return p.block_table[static_cast<int64_t>(bb) * p.NB + (u - pref[bb])];
+    };
+    int cur = page_of(u0 + lane);
     int64_t i = 0;
-    for (int64_t u = u0; u < u1; ++u, ++i) {
-      while (u >= pref[b + 1]) ++b;
-      const int n = static_cast<int>(u - pref[b]);
-      const int s = static_cast<int>(i % kStages);
-      const uint32_t ph = static_cast<uint32_t>((i / kStages) & 1);
-      if (!mbar_wait(smem_addr(&empty[s]), ph ^ 1)) {
-        set_flag(p.flags, MSA_FLAG_TIMEOUT);
-        break;
+    bool ok = true;
+    for (int64_t base = u0; base < u1 && ok; base += 32) {
+      const int nxt = page_of(base + 32 + lane);
+      const int n = static_cast<int>(u1 - base < 32 ? u1 - base : 32);
+      for (int k = 0; k < n; ++k) {
+        const int page = __shfl_sync(kFull, cur, k);
+        if (lane == 0) {
+          const int s = static_cast<int>(i % kStages);
+          if (!mbar_wait(smem_addr(&empty[s]), static_cast<uint32_t>(((i / kStages) & 1) ^ 1))) {
+            set_flag(p.flags, MSA_FLAG_TIMEOUT);
+            ok = false;
+          } else {
+            const uint32_t fb = smem_addr(&full[s]);
+            if (page < 0 || page >= p.P) {
+              set_flag(p.flags, MSA_FLAG_BAD_PAGE);
+              valid[s] = 0;
+              mbar_arrive(fb);
+            } else {
+              valid[s] = 1;
+              const uint32_t dst = smem_addr(smem + s * stage_bytes);
+              mbar_arrive_expect_tx(fb, stage_bytes);
+              bulk_g2s(dst, keys + static_cast<int64_t>(page) * key_bytes, key_bytes, fb, pol);
+              bulk_g2s(dst + key_bytes, p.scale + static_cast<int64_t>(page) * I * kBlock, scale_bytes, fb, pol);
+            }
+          }
+        }
+        ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        ++i;
       }
-      const int page = p.block_table[static_cast<int64_t>(b) * p.NB + n];
-      const uint32_t fb = smem_addr(&full[s]);
-      if (page < 0 || page >= p.P) {
-        set_flag(p.flags, MSA_FLAG_BAD_PAGE);
-        valid[s] = 0;
-        mbar_arrive(fb);
-      } else {
-        valid[s] = 1;
-        const uint32_t dst = smem_addr(smem + s * stage_bytes);
-        mbar_arrive_expect_tx(fb, stage_bytes);
-        bulk_g2s(dst, keys + static_cast<int64_t>(page) * key_bytes, key_bytes, fb, pol);
-        bulk_g2s(dst + key_bytes, p.scale + static_cast<int64_t>(page) * I * kBlock, scale_bytes, fb, pol);
-      }
+      cur = nxt;
     }
     // Do not leave while copies into this CTA's shared memory may be in flight.
-    const int64_t first = i > kStages ? i - kStages : 0;
-    for (int64_t k = first; k < i; ++k)
-      if (!mbar_wait(smem_addr(&full[k % kStages]), static_cast<uint32_t>((k / kStages) & 1))) break;
+    if (lane == 0) {
+      const int64_t first = i > kStages ? i - kStages : 0;
+      for (int64_t k = first; k < i; ++k)
+        if (!mbar_wait(smem_addr(&full[k % kStages]), static_cast<uint32_t>((k / kStages) & 1))) break;
+    }
     return;
   }
 
@@ -173,8 +190,8 @@ __global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_ke
   for (int64_t u = u0; u < u1; ++u, ++i) {
     while (u >= pref[b + 1]) ++b;
     const int n = static_cast<int>(u - pref[b]);
-    const int L = p.seq_lens[b];
     if (b != cur_b) {
+      const int L = p.seq_lens[b];
       // Index-query fragment of position gr for this request and head.
       float qv[32];
       if (gr < p.Q) {

@@ -76,41 +76,48 @@ __host__ __device__ __forceinline__ int cta_of(int64_t x, int64_t W, int C) {
   return static_cast<int>(((x + 1) * C + W - 1) / W) - 1;
 }
 
-struct Item {
-  int b, g, j, blk, page;
-  bool valid;
-  int64_t row;  // enumeration row (b, g, j)
+struct RowPos {
+  int b, g, j;
 };
 
-// Decodes item x and checks it against the device-side invariants. Only the
-// producer reports problems, so each is flagged once per CTA visit.
-__device__ __forceinline__ Item decode_item(const GqaParams& p, int64_t x, bool report) {
-  Item it;
-  it.row = x / p.K;
+// (request, KV head, position) of enumeration row r; positions are adjacent.
+__device__ __forceinline__ RowPos row_pos(const GqaParams& p, int64_t r) {
+  RowPos o;
+  o.j = static_cast<int>(r % p.Q);
+  o.g = static_cast<int>((r / p.Q) % p.G);
+  o.b = static_cast<int>(r / (static_cast<int64_t>(p.Q) * p.G));
+  return o;
+}
+
+struct ItemInfo {
+  int blk, page, valid;
+};
+
+// Selected block, page and validity of item x (x >= x1: an empty slot). Checks
+// the device-side invariants; only the producer reports problems.
+__device__ __forceinline__ ItemInfo load_item(const GqaParams& p, int64_t x, int64_t x1, bool report) {
+  ItemInfo it{-1, -1, 0};
+  if (x >= x1) return it;
+  const int64_t r = x / p.K;
   const int e = static_cast<int>(x % p.K);
-  it.j = static_cast<int>(it.row % p.Q);
-  it.g = static_cast<int>((it.row / p.Q) % p.G);
-  it.b = static_cast<int>(it.row / (static_cast<int64_t>(p.Q) * p.G));
-  it.valid = false;
-  it.page = -1;
-  it.blk = p.selected[((static_cast<int64_t>(it.b) * p.Q + it.j) * p.G + it.g) * p.K + e];
+  const RowPos rp = row_pos(p, r);
+  it.blk = p.selected[((static_cast<int64_t>(rp.b) * p.Q + rp.j) * p.G + rp.g) * p.K + e];
   if (it.blk < 0) return it;
-  const int L = p.seq_lens[it.b];
+  const int L = p.seq_lens[rp.b];
   if (L < p.Q || L > p.NB * kBlock || L < 1) {
     if (report) set_flag(p.flags, MSA_FLAG_BAD_SEQLEN);
     return it;
   }
-  const int ell = (L - p.Q + it.j) / kBlock;
-  if (it.blk > ell) {
+  if (it.blk > (L - p.Q + rp.j) / kBlock) {
     if (report) set_flag(p.flags, MSA_FLAG_BAD_BLOCK);
     return it;
   }
-  it.page = p.block_table[static_cast<int64_t>(it.b) * p.NB + it.blk];
+  it.page = p.block_table[static_cast<int64_t>(rp.b) * p.NB + it.blk];
   if (it.page < 0 || it.page >= p.P) {
     if (report) set_flag(p.flags, MSA_FLAG_BAD_PAGE);
     return it;
   }
-  it.valid = true;
+  it.valid = 1;
   return it;
 }
 
@@ -134,8 +141,8 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
   constexpr SmemLayout Ly = gqa_layout<kFp4>();
   constexpr uint32_t kStageBytes = kFp4 ? kFp4StageBytes : kTileBytes;
   const uint32_t raw = smem_addr(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* sm = smem_raw + (base - raw);
+  const uint32_t base_addr = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base_addr - raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + Ly.bars);
   uint64_t* empty = full + kGqaStages;
   uint64_t* gbar = empty + kGqaStages;   // [0]: partials written, [1]: partials read / tile ready
@@ -161,39 +168,55 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
-    if (lane != 0) return;
+    // The warp fetches the next 32 items' block, page and validity at once
+    // (one chunk ahead); lane 0 issues the copies.
     const uint64_t pol = l2_evict_first_policy();
+    ItemInfo cur = load_item(p, x0 + lane, x1, true);
     int64_t i = 0;
-    for (int64_t x = x0; x < x1; ++x) {
-      const Item it = decode_item(p, x, true);
-      if (!it.valid) continue;
-      const int s = static_cast<int>(i % kGqaStages);
-      if (!mbar_wait(smem_addr(&empty[s]), static_cast<uint32_t>(((i / kGqaStages) & 1) ^ 1))) {
-        set_flag(p.flags, MSA_FLAG_TIMEOUT);
-        break;
+    bool ok = true;
+    for (int64_t base = x0; base < x1 && ok; base += 32) {
+      const ItemInfo nxt = load_item(p, base + 32 + lane, x1, true);
+      const int n = static_cast<int>(x1 - base < 32 ? x1 - base : 32);
+      for (int k = 0; k < n; ++k) {
+        if (!__shfl_sync(kAll, cur.valid, k)) continue;
+        const int page = __shfl_sync(kAll, cur.page, k);
+        if (lane == 0) {
+          const int g = row_pos(p, (base + k) / p.K).g;
+          const int s = static_cast<int>(i % kGqaStages);
+          if (!mbar_wait(smem_addr(&empty[s]), static_cast<uint32_t>(((i / kGqaStages) & 1) ^ 1))) {
+            set_flag(p.flags, MSA_FLAG_TIMEOUT);
+            ok = false;
+          } else {
+            const uint32_t fb = smem_addr(&full[s]);
+            const uint32_t dst = base_addr + Ly.stages + s * kStageBytes;
+            const int64_t ph = static_cast<int64_t>(page) * p.G + g;   // (page, kv head) slab
+            mbar_arrive_expect_tx(fb, kStageBytes);
+            if (!kFp4) {
+              const int y = static_cast<int>(ph * kBlock);
+              tma_load_2d(dst, &tk, 0, y, fb);
+              tma_load_2d(dst + kBoxBytes, &tk, 64, y, fb);
+              tma_load_2d(dst + 2 * kBoxBytes, &tv, 0, y, fb);
+              tma_load_2d(dst + 3 * kBoxBytes, &tv, 64, y, fb);
+            } else {
+              constexpr uint32_t cb = kBlock * kDim / 2, sb = kBlock * kDim / 16;
+              bulk_g2s(dst, p.k4 + ph * cb, cb, fb, pol);
+              bulk_g2s(dst + cb, p.ks + ph * sb, sb, fb, pol);
+              bulk_g2s(dst + cb + sb, p.v4 + ph * cb, cb, fb, pol);
+              bulk_g2s(dst + 2 * cb + sb, p.vs + ph * sb, sb, fb, pol);
+            }
+          }
+        }
+        ok = __shfl_sync(kAll, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        ++i;
       }
-      const uint32_t fb = smem_addr(&full[s]);
-      const uint32_t dst = base + Ly.stages + s * kStageBytes;
-      const int64_t ph = static_cast<int64_t>(it.page) * p.G + it.g;   // (page, kv head) slab
-      mbar_arrive_expect_tx(fb, kStageBytes);
-      if (!kFp4) {
-        const int y = static_cast<int>(ph * kBlock);
-        tma_load_2d(dst, &tk, 0, y, fb);
-        tma_load_2d(dst + kBoxBytes, &tk, 64, y, fb);
-        tma_load_2d(dst + 2 * kBoxBytes, &tv, 0, y, fb);
-        tma_load_2d(dst + 3 * kBoxBytes, &tv, 64, y, fb);
-      } else {
-        constexpr uint32_t cb = kBlock * kDim / 2, sb = kBlock * kDim / 16;
-        bulk_g2s(dst, p.k4 + ph * cb, cb, fb, pol);
-        bulk_g2s(dst + cb, p.ks + ph * sb, sb, fb, pol);
-        bulk_g2s(dst + cb + sb, p.v4 + ph * cb, cb, fb, pol);
-        bulk_g2s(dst + 2 * cb + sb, p.vs + ph * sb, sb, fb, pol);
-      }
-      ++i;
+      cur = nxt;
     }
-    const int64_t first = i > kGqaStages ? i - kGqaStages : 0;
-    for (int64_t k = first; k < i; ++k)
-      if (!mbar_wait(smem_addr(&full[k % kGqaStages]), static_cast<uint32_t>((k / kGqaStages) & 1))) break;
+    if (lane == 0) {
+      const int64_t first = i > kGqaStages ? i - kGqaStages : 0;
+      for (int64_t k = first; k < i; ++k)
+        if (!mbar_wait(smem_addr(&full[k % kGqaStages]), static_cast<uint32_t>((k / kGqaStages) & 1))) break;
+    }
     return;
   }
 
@@ -211,13 +234,14 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
   int64_t i = 0;
   bool ok = true;
 
-  auto begin_segment = [&](const Item& it) {
-    seg_row = it.row;
-    seg_b = it.b; seg_g = it.g; seg_j = it.j;
-    const int L = p.seq_lens[it.b];
-    seg_p = L - p.Q + it.j;
+  auto begin_segment = [&](int64_t r) {
+    const RowPos rp = row_pos(p, r);
+    seg_row = r;
+    seg_b = rp.b; seg_g = rp.g; seg_j = rp.j;
+    const int L = p.seq_lens[rp.b];
+    seg_p = L - p.Q + rp.j;
     seg_ell = seg_p / kBlock;
-    const uint16_t* qh = p.q + ((static_cast<int64_t>(it.b) * p.Q + it.j) * p.H + static_cast<int64_t>(it.g) * kGroup) * kDim;
+    const uint16_t* qh = p.q + ((static_cast<int64_t>(rp.b) * p.Q + rp.j) * p.H + static_cast<int64_t>(rp.g) * kGroup) * kDim;
     float qv[2][32];
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
@@ -337,19 +361,24 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     return group_sync(smem_addr(&gbar[1]), gph[1], lane);
   };
 
-  for (int64_t x = x0; x < x1 && ok; ++x) {
-    const Item it = decode_item(p, x, false);
-    if (it.row != seg_row) {
+  ItemInfo cur = load_item(p, x0 + lane, x1, false);
+  for (int64_t base = x0; base < x1 && ok; base += 32) {
+   const ItemInfo nxt = load_item(p, base + 32 + lane, x1, false);
+   const int nk = static_cast<int>(x1 - base < 32 ? x1 - base : 32);
+   for (int kx = 0; kx < nk; ++kx) {
+    const int64_t xrow = (base + kx) / p.K;
+    if (xrow != seg_row) {
       if (seg_row >= 0 && !end_segment()) { ok = false; break; }
-      begin_segment(it);
+      begin_segment(xrow);
     }
-    if (!it.valid) continue;
+    if (!__shfl_sync(kAll, cur.valid, kx)) continue;
+    const int it_blk = __shfl_sync(kAll, cur.blk, kx);
     const int s = static_cast<int>(i % kGqaStages);
     if (!mbar_wait(smem_addr(&full[s]), static_cast<uint32_t>((i / kGqaStages) & 1))) { ok = false; break; }
-    uint32_t kt = base + Ly.stages + s * kStageBytes;   // bf16 tile: K lo, K hi, V lo, V hi
+    uint32_t kt = base_addr + Ly.stages + s * kStageBytes;   // bf16 tile: K lo, K hi, V lo, V hi
     if (kFp4) {
       // Expand this page's NVFP4 K and V into the fp16 tile (one token row per thread).
-      const uint32_t tile = base + Ly.tiles + static_cast<uint32_t>(i & 1) * kTileBytes;
+      const uint32_t tile = base_addr + Ly.tiles + static_cast<uint32_t>(i & 1) * kTileBytes;
       const uint8_t* st = sm + Ly.stages + s * kStageBytes;
       const int t = ct;
 #pragma unroll
@@ -412,10 +441,10 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
       }
     }
     // ---- causal limit inside the local block
-    if (it.blk == seg_ell) {
+    if (it_blk == seg_ell) {
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
-        const int t0 = it.blk * kBlock + 32 * w + 8 * nt + 2 * c;
+        const int t0 = it_blk * kBlock + 32 * w + 8 * nt + 2 * c;
         if (t0 > seg_p) { sc[nt][0] = -INFINITY; sc[nt][2] = -INFINITY; }
         if (t0 + 1 > seg_p) { sc[nt][1] = -INFINITY; sc[nt][3] = -INFINITY; }
       }
@@ -485,6 +514,8 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
       if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
     }
     ++i;
+   }
+   cur = nxt;
   }
   if (ok && seg_row >= 0) ok = end_segment();
   if (!ok && lane == 0) set_flag(p.flags, MSA_FLAG_TIMEOUT);
