@@ -107,6 +107,8 @@ __global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_ke
   int* pref = valid + kStages;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_launch_dependents();
+  griddep_wait();
   if (warp == 0) build_prefix(p, pref, blockIdx.x == 0);
   if (threadIdx.x == 32) {
     for (int s = 0; s < kStages; ++s) {
@@ -287,6 +289,8 @@ __global__ void __launch_bounds__(128) index_score_f32_kernel(IdxParams p) {
   int* pref = reinterpret_cast<int*>(smem);
   float* qsh = reinterpret_cast<float*>(smem + ((static_cast<size_t>(p.B) + 1) * 4 + 15) / 16 * 16);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_launch_dependents();
+  griddep_wait();
   if (warp == 0) build_prefix(p, pref, blockIdx.x == 0);
   __syncthreads();
   fill_tails(p, pref);
@@ -360,7 +364,8 @@ cudaError_t launch_index_score(const IndexArgs& a, cudaStream_t stream, Dispatch
                                static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     const int grid = sms;
-    index_score_fp8_kernel<kIdxStages><<<grid, 32 * (1 + a.I), smem, stream>>>(p);
+    err = launch_pdl(index_score_fp8_kernel<kIdxStages>, dim3(grid), dim3(32 * (1 + a.I)), smem, stream, p);
+    if (err != cudaSuccess) return err;
     rec->set("index_score fp8_mma_f16 grid=%d block=%d smem=%zu stages=%d q_len=%d idx_heads=%d", grid,
              32 * (1 + a.I), smem, kIdxStages, a.Q, a.I);
   } else {
@@ -369,7 +374,8 @@ cudaError_t launch_index_score(const IndexArgs& a, cudaStream_t stream, Dispatch
                                static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     const int grid = sms * 4;
-    index_score_f32_kernel<<<grid, 128, smem, stream>>>(p);
+    err = launch_pdl(index_score_f32_kernel, dim3(grid), dim3(128), smem, stream, p);
+    if (err != cudaSuccess) return err;
     rec->set("index_score f32_fma grid=%d block=128 smem=%zu q_len=%d idx_heads=%d", grid, smem, a.Q, a.I);
   }
   return cudaGetLastError();

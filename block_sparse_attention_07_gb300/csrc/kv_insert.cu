@@ -49,6 +49,8 @@ __device__ __forceinline__ void quant_nvfp4_row(const uint16_t* src, uint8_t* co
 }
 
 __global__ void __launch_bounds__(256) kv_insert_kernel(InsertParams p) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -133,7 +135,8 @@ cudaError_t launch_kv_insert(const InsertArgs& a, cudaStream_t stream, DispatchR
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  kv_insert_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+  const cudaError_t err = launch_pdl(kv_insert_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
+  if (err != cudaSuccess) return err;
   rec->set("kv_insert %s%s grid=%lld block=256 tokens=%d", a.kv_nvfp4 ? "nvfp4" : "bf16",
            a.idx_new ? (a.idx_fp8 ? "+idx_fp8" : "+idx_f32") : "", static_cast<long long>(blocks), a.T);
   return cudaGetLastError();

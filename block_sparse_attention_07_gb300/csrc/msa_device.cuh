@@ -63,10 +63,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  for (;;) {
+#pragma unroll 1
+    for (int k = 0; k < 64; ++k)
+      if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
-  return true;
 }
 
 // ------------------------------------------------------------ bulk copies --
@@ -99,6 +101,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
 __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+
+// ------------------------------------------- programmatic dependent launch --
+// Launched with programmatic stream serialisation, a kernel may start while
+// its predecessor on the stream is still running; griddep_wait() blocks until
+// the predecessor has finished and its writes are visible (a no-op otherwise).
+// griddep_launch_dependents() lets the next kernel start its own prologue.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// GPU-scope acquire/release fence (lighter than the sequentially consistent
+// fence of __threadfence()); with a CTA barrier before it, it also publishes
+// the writes the other threads of the CTA made before that barrier.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // ------------------------------------------------------------- ldmatrix/mma --
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cuda_runtime.h>
+#include <utility>
 
 #include "msa_device.cuh"
 
@@ -22,6 +23,25 @@ struct DispatchRecord {
 };
 
 int device_sm_count();
+
+// Launches a kernel with programmatic stream serialisation: it may begin while
+// the previous kernel on the stream is still running, and waits for it with
+// griddep_wait() before touching memory that kernel may write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct InsertArgs {
   const void* k_new;
@@ -83,6 +103,7 @@ struct GqaArgs {
 };
 
 // Floats per split-K partial: o [16 heads][128 dims], then m [16], then l [16].
+// The workspace holds rows x topk partials, then one 64-bit ticket per row.
 constexpr int kPartialFloats = kGroup * kDim + 2 * kGroup;
 
 size_t gqa_workspace_bytes(int B, int Q, int G, int K);

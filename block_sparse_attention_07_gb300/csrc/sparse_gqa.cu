@@ -22,6 +22,8 @@
 // All waits are bounded; a kernel never traps.
 #include <cuda.h>
 
+#include <atomic>
+
 #include "msa_internal.h"
 
 namespace msa {
@@ -47,10 +49,13 @@ struct GqaParams {
   const uint8_t* v4;
   const uint8_t* ks;
   const uint8_t* vs;
+  unsigned long long* tickets;  // one per row, after the partials in the workspace
   float k_global, v_global;
   float scale_log2;
+  uint32_t epoch;               // differs on every call; tags the tickets
   int B, Q, H, G, NB, P, K;
-  int64_t W;  // items = B * G * Q * K
+  int row_aligned;  // 1: every CTA owns whole rows; 0: balanced item ranges, rows may be split
+  int64_t W;        // items = B * G * Q * K
 };
 
 struct SmemLayout {
@@ -67,7 +72,7 @@ __host__ __device__ constexpr SmemLayout gqa_layout() {
   s.comb_o = s.tiles + (kFp4 ? 2 * kTileBytes : 0);
   s.comb_ml = s.comb_o + kCWarps * kGroup * kDim * 4;
   s.bars = s.comb_ml + kCWarps * kGroup * 2 * 4;
-  s.total = s.bars + (2 * kGqaStages + 2) * 8;
+  s.total = s.bars + (2 * kGqaStages + 2) * 8 + 16;   // + the last-arriver flag
   return s;
 }
 
@@ -121,6 +126,23 @@ __device__ __forceinline__ ItemInfo load_item(const GqaParams& p, int64_t x, int
   return it;
 }
 
+// Counts this CTA's partial of a row: the ticket word holds (epoch << 32 | count)
+// and a count from another epoch is read as 0, so the workspace needs no
+// initialisation. Returns true for the CTA that delivers the last partial.
+__device__ bool ticket_is_last(const GqaParams& p, int64_t row, int nslots) {
+  unsigned long long* t = p.tickets + row;
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(t);
+  for (int tries = 0; tries < (1 << 20); ++tries) {
+    const uint32_t cnt = static_cast<uint32_t>(cur >> 32) == p.epoch ? static_cast<uint32_t>(cur) : 0u;
+    const unsigned long long nw = (static_cast<unsigned long long>(p.epoch) << 32) | (cnt + 1u);
+    const unsigned long long prev = atomicCAS(t, cur, nw);
+    if (prev == cur) return static_cast<int>(cnt + 1u) == nslots;
+    cur = prev;
+  }
+  set_flag(p.flags, MSA_FLAG_TIMEOUT);
+  return false;
+}
+
 // Consumer-group barrier on an mbarrier (count = 4 warps), bounded in time.
 __device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, int lane) {
   __syncwarp();
@@ -149,8 +171,10 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
   float* comb_o = reinterpret_cast<float*>(sm + Ly.comb_o);
   float* comb_m = reinterpret_cast<float*>(sm + Ly.comb_ml);
   float* comb_l = comb_m + kCWarps * kGroup;
+  int* last_flag = reinterpret_cast<int*>(sm + Ly.bars + (2 * kGqaStages + 2) * 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGqaStages; ++s) {
       mbar_init(smem_addr(&full[s]), 1);
@@ -159,11 +183,24 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     mbar_init(smem_addr(&gbar[0]), kCWarps);
     mbar_init(smem_addr(&gbar[1]), kCWarps);
     fence_mbar_init();
+    if (!kFp4) {
+      prefetch_tensormap(&tk);
+      prefetch_tensormap(&tv);
+    }
   }
   __syncthreads();
+  griddep_wait();
 
   const int C = gridDim.x;
-  const int64_t x0 = p.W * blockIdx.x / C, x1 = p.W * (blockIdx.x + 1) / C;
+  int64_t x0, x1;
+  if (p.row_aligned) {
+    const int64_t rows = p.W / p.K;
+    x0 = rows * blockIdx.x / C * p.K;
+    x1 = rows * (blockIdx.x + 1) / C * p.K;
+  } else {
+    x0 = p.W * blockIdx.x / C;
+    x1 = p.W * (blockIdx.x + 1) / C;
+  }
   if (x0 >= x1) return;
 
   if (warp == 0) {
@@ -338,27 +375,66 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     const int64_t r = seg_row;
     const bool whole = x0 <= r * p.K && (r + 1) * p.K <= x1;
     const int64_t head = (static_cast<int64_t>(seg_b) * p.Q + seg_j) * p.H + static_cast<int64_t>(seg_g) * kGroup + hh;
-    if (whole) {
-      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    auto write_out = [&](const float (&v)[16], float mm, float ll) {
+      const float inv = ll > 0.f ? 1.f / ll : 0.f;
       uint32_t packed[8];
 #pragma unroll
-      for (int d = 0; d < 8; ++d) packed[d] = pack_bf16x2(acc[2 * d] * inv, acc[2 * d + 1] * inv);
+      for (int d = 0; d < 8; ++d) packed[d] = pack_bf16x2(v[2 * d] * inv, v[2 * d + 1] * inv);
       uint4* dst = reinterpret_cast<uint4*>(p.out + head * kDim + d0);
       dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
       dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-      if (p.lse != nullptr && (ct & 7) == 0) p.lse[head] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
-    } else {
-      const int slot = static_cast<int>(blockIdx.x) - cta_of(r * p.K, p.W, C);
-      float* part = p.ws + (r * p.K + slot) * static_cast<int64_t>(kPartialFloats);
-      float4* dst = reinterpret_cast<float4*>(part + hh * kDim + d0);
-#pragma unroll
-      for (int d = 0; d < 4; ++d) dst[d] = make_float4(acc[4 * d], acc[4 * d + 1], acc[4 * d + 2], acc[4 * d + 3]);
-      if ((ct & 7) == 0) {
-        part[kGroup * kDim + hh] = M;
-        part[kGroup * kDim + kGroup + hh] = Ls;
-      }
+      if (p.lse != nullptr && (ct & 7) == 0) p.lse[head] = ll > 0.f ? (mm + log2f(ll)) * kLn2 : -INFINITY;
+    };
+    if (whole) {
+      write_out(acc, M, Ls);
+      return group_sync(smem_addr(&gbar[1]), gph[1], lane);
     }
-    return group_sync(smem_addr(&gbar[1]), gph[1], lane);
+    // Split row: publish this CTA's partial; the CTA that delivers the last
+    // one merges them all.
+    const int first = cta_of(r * p.K, p.W, C);
+    const int nslots = cta_of(r * p.K + p.K - 1, p.W, C) - first + 1;
+    float* rowp = p.ws + r * p.K * static_cast<int64_t>(kPartialFloats);
+    float* part = rowp + (static_cast<int>(blockIdx.x) - first) * static_cast<int64_t>(kPartialFloats);
+    float4* dst = reinterpret_cast<float4*>(part + hh * kDim + d0);
+#pragma unroll
+    for (int d = 0; d < 4; ++d) dst[d] = make_float4(acc[4 * d], acc[4 * d + 1], acc[4 * d + 2], acc[4 * d + 3]);
+    if ((ct & 7) == 0) {
+      part[kGroup * kDim + hh] = M;
+      part[kGroup * kDim + kGroup + hh] = Ls;
+    }
+    if (!group_sync(smem_addr(&gbar[1]), gph[1], lane)) return false;
+    if (ct == 0) {
+      fence_acq_rel_gpu();                       // publish the CTA's partial (after the barrier above)
+      const bool last = ticket_is_last(p, r, nslots);
+      if (last) fence_acq_rel_gpu();             // see the other CTAs' partials
+      *last_flag = last ? 1 : 0;
+    }
+    if (!group_sync(smem_addr(&gbar[0]), gph[0], lane)) return false;
+    if (*last_flag) {
+      float M2 = -INFINITY;
+      for (int q = 0; q < nslots; ++q) M2 = fmaxf(M2, __ldcg(rowp + q * kPartialFloats + kGroup * kDim + hh));
+      float L2 = 0.f;
+      float v[16];
+#pragma unroll
+      for (int d = 0; d < 16; ++d) v[d] = 0.f;
+      if (M2 != -INFINITY) {
+        for (int q = 0; q < nslots; ++q) {
+          const float* pq = rowp + q * kPartialFloats;
+          const float f = exp2f(__ldcg(pq + kGroup * kDim + hh) - M2);
+          L2 += f * __ldcg(pq + kGroup * kDim + kGroup + hh);
+#pragma unroll
+          for (int d4 = 0; d4 < 4; ++d4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(pq + hh * kDim + d0) + d4);
+            v[4 * d4] += f * x.x;
+            v[4 * d4 + 1] += f * x.y;
+            v[4 * d4 + 2] += f * x.z;
+            v[4 * d4 + 3] += f * x.w;
+          }
+        }
+      }
+      write_out(v, M2, L2);
+    }
+    return true;
   };
 
   ItemInfo cur = load_item(p, x0 + lane, x1, false);
@@ -521,43 +597,9 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
   if (!ok && lane == 0) set_flag(p.flags, MSA_FLAG_TIMEOUT);
 }
 
-// Merges the split-K partials of every (row, head) whose row spans several CTAs.
-__global__ void __launch_bounds__(256) gqa_combine_kernel(GqaParams p, int C) {
-  const int lane = threadIdx.x & 31;
-  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t rows = p.W / p.K;
-  if (wid >= rows * kGroup) return;
-  const int64_t r = wid / kGroup;
-  const int hh = static_cast<int>(wid % kGroup);
-  const int first = cta_of(r * p.K, p.W, C), last = cta_of(r * p.K + p.K - 1, p.W, C);
-  if (first == last) return;   // written directly by the attention kernel
-  const int j = static_cast<int>(r % p.Q);
-  const int g = static_cast<int>((r / p.Q) % p.G);
-  const int b = static_cast<int>(r / (static_cast<int64_t>(p.Q) * p.G));
-  const float* base = p.ws + r * p.K * static_cast<int64_t>(kPartialFloats);
-  const int n = last - first + 1;
-  float M = -INFINITY;
-  for (int s = 0; s < n; ++s) M = fmaxf(M, base[s * kPartialFloats + kGroup * kDim + hh]);
-  float Ls = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
-    for (int s = 0; s < n; ++s) {
-      const float* part = base + s * kPartialFloats;
-      const float f = exp2f(part[kGroup * kDim + hh] - M);
-      Ls += f * part[kGroup * kDim + kGroup + hh];
-      const float4 v = *reinterpret_cast<const float4*>(part + hh * kDim + 4 * lane);
-      acc.x += f * v.x; acc.y += f * v.y; acc.z += f * v.z; acc.w += f * v.w;
-    }
-  }
-  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-  const int64_t head = (static_cast<int64_t>(b) * p.Q + j) * p.H + static_cast<int64_t>(g) * kGroup + hh;
-  uint2 packed = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-  *reinterpret_cast<uint2*>(p.out + head * kDim + 4 * lane) = packed;
-  if (p.lse != nullptr && lane == 0) p.lse[head] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
-}
-
 size_t gqa_workspace_bytes(int B, int Q, int G, int K) {
-  return static_cast<size_t>(B) * Q * G * K * kPartialFloats * sizeof(float);
+  const size_t rows = static_cast<size_t>(B) * Q * G;
+  return rows * K * kPartialFloats * sizeof(float) + rows * sizeof(unsigned long long);
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up through the runtime so the
@@ -621,34 +663,39 @@ cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRec
   CUtensorMap tk, tv;
   memset(&tk, 0, sizeof(tk));
   memset(&tv, 0, sizeof(tv));
-  const int64_t rows = static_cast<int64_t>(a.P) * a.G * kBlock;
+  const int64_t cache_rows = static_cast<int64_t>(a.P) * a.G * kBlock;
   cudaError_t err;
   if (!a.nvfp4) {
-    if ((err = make_kv_map(&tk, a.k, rows)) != cudaSuccess) return err;
-    if ((err = make_kv_map(&tv, a.v, rows)) != cudaSuccess) return err;
+    if ((err = make_kv_map(&tk, a.k, cache_rows)) != cudaSuccess) return err;
+    if ((err = make_kv_map(&tv, a.v, cache_rows)) != cudaSuccess) return err;
   }
+  // Work split. bf16 pages (64 KB per block) stream best when every CTA owns
+  // whole rows: no split-K partials, no merge. NVFP4 pages (18 KB) are latency
+  // bound per block, so their item ranges are balanced exactly over all SMs
+  // and the CTAs that share a row merge through the workspace.
   const int sms = device_sm_count();
-  const int C = static_cast<int>(p.W < sms ? p.W : sms);
-  const size_t smem = (a.nvfp4 ? gqa_layout<true>().total : gqa_layout<false>().total) + 1024;
-  if (a.nvfp4) {
-    err = cudaFuncSetAttribute(sparse_gqa_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    sparse_gqa_kernel<true><<<C, 32 * (1 + kCWarps), smem, stream>>>(tk, tv, p);
+  const int64_t rows = p.W / p.K;
+  int C;
+  if (!a.nvfp4) {
+    p.row_aligned = 1;
+    C = static_cast<int>(rows < sms ? rows : sms);
   } else {
-    err = cudaFuncSetAttribute(sparse_gqa_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    sparse_gqa_kernel<false><<<C, 32 * (1 + kCWarps), smem, stream>>>(tk, tv, p);
+    p.row_aligned = 0;
+    C = static_cast<int>(p.W < sms ? p.W : sms);
   }
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  const int64_t warps = (p.W / p.K) * kGroup;
-  const int64_t cgrid = (warps + 7) / 8;
-  gqa_combine_kernel<<<static_cast<unsigned>(cgrid), 256, 0, stream>>>(p, C);
-  rec->set("sparse_gqa %s split_k persistent grid=%d block=%d smem=%zu stages=%d items=%lld + combine grid=%lld",
-           a.nvfp4 ? "nvfp4_dequant_f16_mma" : "bf16_tma_mma", C, 32 * (1 + kCWarps), smem, kGqaStages,
-           static_cast<long long>(p.W), static_cast<long long>(cgrid));
-  return cudaGetLastError();
+  const size_t smem = (a.nvfp4 ? gqa_layout<true>().total : gqa_layout<false>().total) + 1024;
+  static std::atomic<uint32_t> epoch{1};
+  p.epoch = epoch.fetch_add(1);
+  if (p.epoch == 0) p.epoch = epoch.fetch_add(1);    // 0 never tags a ticket
+  p.tickets = reinterpret_cast<unsigned long long*>(a.workspace + (p.W / p.K) * p.K * kPartialFloats);
+  auto kern = a.nvfp4 ? sparse_gqa_kernel<true> : sparse_gqa_kernel<false>;
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  err = launch_pdl(kern, dim3(C), dim3(32 * (1 + kCWarps)), smem, stream, tk, tv, p);
+  rec->set("sparse_gqa %s persistent %s grid=%d block=%d smem=%zu stages=%d items=%lld",
+           a.nvfp4 ? "nvfp4_dequant_f16_mma" : "bf16_tma_mma", p.row_aligned ? "whole_rows" : "split_k_fused_combine",
+           C, 32 * (1 + kCWarps), smem, kGqaStages, static_cast<long long>(p.W));
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace msa

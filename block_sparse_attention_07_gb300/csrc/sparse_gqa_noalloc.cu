@@ -19,8 +19,9 @@
 //     initial value (each is written before it is read) and the array keeps the
 //     last call's contents, but two calls whose kernels overlap on the GPU (on
 //     different streams, or from different threads) race on it: serialise them.
-//   - A shape whose partials do not fit (B * Q * G * topk * 8,320 bytes >
-//     64 MiB) is rejected with MSA_ERR_WORKSPACE before anything is launched.
+//   - A shape whose workspace does not fit (B * Q * G * (topk * 8,320 + 8)
+//     bytes > 64 MiB) is rejected with MSA_ERR_WORKSPACE before anything is
+//     launched.
 // Nothing here calls cudaMalloc, cudaFree or any allocating routine.
 #include <mutex>
 

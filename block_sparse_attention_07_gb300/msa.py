@@ -144,28 +144,50 @@ class IndexCache:
         return _IndexCache(self.dtype, _ptr(self.keys), _ptr(self.scale))
 
 
+class Prepared:
+    """A library call whose arguments were marshalled once; calling it launches again.
+
+    Holds the ctypes structures the arguments point to. Used on launch-bound
+    paths (the same call issued every decode step)."""
+    __slots__ = ("fn", "args", "keep", "what")
+
+    def __init__(self, fn, args, keep, what):
+        self.fn, self.args, self.keep, self.what = fn, args, keep, what
+
+    def __call__(self):
+        st = self.fn(*self.args)
+        if st != OK:
+            raise MSAError(st, self.what)
+
+
+def _call(fn, args, keep, what, prepare):
+    if prepare:
+        return Prepared(fn, args, keep, what)
+    _check(fn(*args), what)
+    return None
+
+
 def kv_insert_quant(dims: Dims, k_new, v_new, idx_k_new, idx_new_dtype: int, slot_mapping, cache: KVCache,
-                    idx_cache: IndexCache | None, flags, stream=None):
+                    idx_cache: IndexCache | None, flags, stream=None, prepare=False):
     kc = cache.c()
     ic = idx_cache.c() if idx_cache is not None else None
-    st = lib.msa_kv_insert_quant(ctypes.byref(dims), _ptr(k_new), _ptr(v_new), _ptr(idx_k_new), idx_new_dtype,
-                                 _ptr(slot_mapping), int(k_new.shape[0]), ctypes.byref(kc),
-                                 ctypes.byref(ic) if ic is not None else None, _ptr(flags), _stream(stream))
-    _check(st, "msa_kv_insert_quant")
+    args = (ctypes.byref(dims), _ptr(k_new), _ptr(v_new), _ptr(idx_k_new), idx_new_dtype, _ptr(slot_mapping),
+            int(k_new.shape[0]), ctypes.byref(kc), ctypes.byref(ic) if ic is not None else None, _ptr(flags),
+            _stream(stream))
+    return _call(lib.msa_kv_insert_quant, args, (dims, kc, ic), "msa_kv_insert_quant", prepare)
 
 
 def index_score(dims: Dims, idx_q, q_dtype: int, idx_cache: IndexCache, block_table, seq_lens, scores, flags,
-                stream=None):
+                stream=None, prepare=False):
     ic = idx_cache.c()
-    st = lib.msa_index_score(ctypes.byref(dims), _ptr(idx_q), q_dtype, ctypes.byref(ic), _ptr(block_table),
-                             _ptr(seq_lens), _ptr(scores), _ptr(flags), _stream(stream))
-    _check(st, "msa_index_score")
+    args = (ctypes.byref(dims), _ptr(idx_q), q_dtype, ctypes.byref(ic), _ptr(block_table), _ptr(seq_lens),
+            _ptr(scores), _ptr(flags), _stream(stream))
+    return _call(lib.msa_index_score, args, (dims, ic), "msa_index_score", prepare)
 
 
-def select_blocks(dims: Dims, scores, seq_lens, selected, flags, stream=None):
-    st = lib.msa_select_blocks(ctypes.byref(dims), _ptr(scores), _ptr(seq_lens), _ptr(selected), _ptr(flags),
-                               _stream(stream))
-    _check(st, "msa_select_blocks")
+def select_blocks(dims: Dims, scores, seq_lens, selected, flags, stream=None, prepare=False):
+    args = (ctypes.byref(dims), _ptr(scores), _ptr(seq_lens), _ptr(selected), _ptr(flags), _stream(stream))
+    return _call(lib.msa_select_blocks, args, (dims,), "msa_select_blocks", prepare)
 
 
 def sparse_gqa_workspace_size(dims: Dims, kv_dtype: int) -> int:
@@ -173,13 +195,12 @@ def sparse_gqa_workspace_size(dims: Dims, kv_dtype: int) -> int:
 
 
 def sparse_gqa_decode(dims: Dims, q, cache: KVCache, block_table, seq_lens, selected, out, lse, workspace, flags,
-                      stream=None):
+                      stream=None, prepare=False):
     kc = cache.c()
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.msa_sparse_gqa_decode(ctypes.byref(dims), _ptr(q), ctypes.byref(kc), _ptr(block_table),
-                                   _ptr(seq_lens), _ptr(selected), _ptr(out), _ptr(lse), _ptr(workspace), nbytes,
-                                   _ptr(flags), _stream(stream))
-    _check(st, "msa_sparse_gqa_decode")
+    args = (ctypes.byref(dims), _ptr(q), ctypes.byref(kc), _ptr(block_table), _ptr(seq_lens), _ptr(selected),
+            _ptr(out), _ptr(lse), _ptr(workspace), nbytes, _ptr(flags), _stream(stream))
+    return _call(lib.msa_sparse_gqa_decode, args, (dims, kc), "msa_sparse_gqa_decode", prepare)
 
 
 def sparse_gqa_decode_noalloc(dims: Dims, q, cache: KVCache, block_table, seq_lens, selected, out, lse, flags,

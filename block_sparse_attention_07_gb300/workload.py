@@ -85,6 +85,7 @@ class DeviceWorkload:
         self.selected = torch.empty((B, Q, I, w.topk), dtype=torch.int32, device=dev)
         self.out = torch.empty((B, Q, H, D), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((B, Q, H), dtype=torch.float32, device=dev)
+        self._prep = None
         ws = msa.sparse_gqa_workspace_size(self.dims, self.cache.dtype)
         self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
         torch.cuda.synchronize(dev)
@@ -98,18 +99,41 @@ class DeviceWorkload:
         msa.kv_insert_quant(self.dims, kd, vd, idd, self.idx_new_dtype, sd, self.cache, self.idx_cache, self.flags)
 
     # ------------------------------------------------------------ stages --
+    def prepared(self):
+        """The four stage calls with their arguments marshalled once (current stream)."""
+        if self._prep is None:
+            self._prep = dict(
+                insert=msa.kv_insert_quant(self.dims, self.new_k, self.new_v, self.new_idx, self.idx_new_dtype,
+                                           self.new_slots, self.cache, self.idx_cache, self.flags, prepare=True),
+                index=msa.index_score(self.dims, self.q_idx, self.q_idx_dtype, self.idx_cache, self.block_table_d,
+                                      self.seq_lens_d, self.scores, self.flags, prepare=True),
+                select=msa.select_blocks(self.dims, self.scores, self.seq_lens_d, self.selected, self.flags,
+                                         prepare=True),
+                attend=msa.sparse_gqa_decode(self.dims, self.q, self.cache, self.block_table_d, self.seq_lens_d,
+                                             self.selected, self.out, self.lse, self.workspace, self.flags,
+                                             prepare=True))
+        return self._prep
+
     def insert_step_tokens(self, stream=None):
+        if stream is None:
+            return self.prepared()["insert"]()
         msa.kv_insert_quant(self.dims, self.new_k, self.new_v, self.new_idx, self.idx_new_dtype, self.new_slots,
                             self.cache, self.idx_cache, self.flags, stream)
 
     def index_score(self, stream=None):
+        if stream is None:
+            return self.prepared()["index"]()
         msa.index_score(self.dims, self.q_idx, self.q_idx_dtype, self.idx_cache, self.block_table_d,
                         self.seq_lens_d, self.scores, self.flags, stream)
 
     def select(self, stream=None):
+        if stream is None:
+            return self.prepared()["select"]()
         msa.select_blocks(self.dims, self.scores, self.seq_lens_d, self.selected, self.flags, stream)
 
     def attend(self, stream=None, selected=None):
+        if stream is None and selected is None:
+            return self.prepared()["attend"]()
         msa.sparse_gqa_decode(self.dims, self.q, self.cache, self.block_table_d, self.seq_lens_d,
                               self.selected if selected is None else selected, self.out, self.lse, self.workspace,
                               self.flags, stream)

@@ -197,9 +197,10 @@ size_t msa_sparse_gqa_workspace_size(const msa_dims_t* dims, msa_dtype_t kv_dtyp
  * with a log-sum-exp combine. K/V are read from bf16 or NVFP4 pages and
  * dequantised in the kernel.
  * q: bf16 [B, Q, H, D]. out: bf16 [B, Q, H, D]. lse: fp32 [B, Q, H] or NULL.
- * workspace: device scratch of at least msa_sparse_gqa_workspace_size bytes,
- * 256-byte aligned; its contents need no initialisation and are not
- * meaningful after the call.
+ * workspace: device scratch of at least msa_sparse_gqa_workspace_size bytes
+ * (B * Q * G * (topk * 8,320 + 8)), 256-byte aligned: split-K partials and one
+ * tagged ticket per row. Its contents need no initialisation and are not
+ * meaningful after the call; calls that overlap on the GPU must not share it.
  */
 msa_status_t msa_sparse_gqa_decode(const msa_dims_t* dims, const void* q, const msa_kv_cache_t* cache,
                                    const int32_t* block_table, const int32_t* seq_lens,
@@ -217,8 +218,9 @@ msa_status_t msa_sparse_gqa_decode(const msa_dims_t* dims, const void* q, const 
  * exits. The first call on a device looks up that array's address (make it
  * before any stream capture on that device). All calls on a device share the
  * array, so calls whose kernels overlap on the GPU race; nothing in it needs
- * to start at zero. Shapes that need more than 64 MiB
- * (B * Q * G * topk * 8,320 bytes) return MSA_ERR_WORKSPACE without launching.
+ * to start at zero. Shapes whose workspace (msa_sparse_gqa_workspace_size:
+ * B * Q * G * (topk * 8,320 + 8) bytes) exceeds 64 MiB return
+ * MSA_ERR_WORKSPACE without launching.
  * Calls no allocating routine.
  */
 msa_status_t msa_sparse_gqa_decode_noalloc(const msa_dims_t* dims, const void* q, const msa_kv_cache_t* cache,

@@ -57,7 +57,8 @@ def test_dims_validation(m):
 def test_workspace_size_and_rejection(m):
     d = m.make_dims(3, 2, max_blocks_per_seq=4, num_pages=8)
     need = m.sparse_gqa_workspace_size(d, m.BF16)
-    assert need == 3 * 2 * 4 * 16 * (16 * 128 + 32) * 4
+    rows = 3 * 2 * 4
+    assert need == rows * 16 * (16 * 128 + 32) * 4 + rows * 8      # partials, then one ticket per row
     fake = ctypes.c_void_p(0x10000)
     kv = m._KVCache(m.BF16, fake, fake, None, None, 1.0, 1.0)
     st = m.lib.msa_sparse_gqa_decode(ctypes.byref(d), fake, ctypes.byref(kv), fake, fake, fake, fake, None, fake,

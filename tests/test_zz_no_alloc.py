@@ -45,7 +45,7 @@ def test_noalloc_matches_workspace_entry_point(name, changes):
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
-    # 64 MiB holds B * Q * G * topk <= 8065 split-K partials of 8,320 bytes
+    # 64 MiB holds about 8,000 split-K partials of 8,320 bytes
     dims = msa.make_dims(64, 8, max_blocks_per_seq=4, num_pages=8)      # 64 * 8 * 4 * 16 = 32768 partials
     x = torch.zeros(16, dtype=torch.uint8, device="cuda")
     kv = msa.KVCache(msa.BF16, x, x)
