@@ -42,10 +42,13 @@ sys.path.insert(0, ROOT)
 METRIC = "MSA decode query-tokens/s at 1 GB300; achieved HBM GB/s vs peak per kernel"
 FALLBACK_HBM_GBS = 6800.0
 
-# ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the index-score
-# kernel, keyed by the hash of the sources it was measured on (a changed kernel
-# reports null until it is measured again).
-NCU_TRAFFIC = {}
+# ncu dram__bytes_read.sum + dram__bytes_write.sum per launch on the default
+# workload, keyed by the hash of the kernel's sources when it was measured (a
+# changed kernel reports null until it is measured again). Summaries: profiles/.
+NCU_TRAFFIC = {
+    ("index_score", "1097b3c4487c882a"): 551638272 + 3004672,
+    ("sparse_gqa", "8987f8d2488a11f7"): 134868224 + 324096,
+}
 
 
 def _src_hash(*names):
@@ -290,7 +293,10 @@ def run_ours(args, world, rank, local):
     sel = dw.selected.cpu().numpy()
     ab = attention_bytes(dw, sel)
     att_ms = statistics.mean(per["sparse_gqa"])
-    traffic = NCU_TRAFFIC.get(_src_hash("index_score.cu", "msa_device.cuh"))
+    traffic = NCU_TRAFFIC.get(("index_score", _src_hash("index_score.cu", "msa_device.cuh")))
+    att_traffic = NCU_TRAFFIC.get(("sparse_gqa", _src_hash("sparse_gqa.cu", "msa_device.cuh")))
+    if args.workload != "b32_32k" or args.batch:
+        traffic = att_traffic = None          # the counters were taken on the default workload
     line = {
         "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": statistics.mean(step_ms), "higher_is_better": True,
@@ -302,7 +308,8 @@ def run_ours(args, world, rank, local):
                      "algorithmic_bytes_per_launch": ib, "avg_launch_ms": idx_ms},
         "kernels_ms": {n: statistics.mean(v) for n, v in per.items()},
         "sparse_gqa_roofline": {"achieved": ab / (att_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
-                                "frac": ab / (att_ms / 1e3) / 1e9 / peak, "algorithmic_bytes_per_launch": ab},
+                                "frac": ab / (att_ms / 1e3) / 1e9 / peak, "algorithmic_bytes_per_launch": ab,
+                                "traffic": att_traffic},
         "e2e": {"value": B * Q * args.steps * world / e2e_tot, "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
