@@ -28,7 +28,8 @@
 
 namespace msa {
 
-constexpr int kGqaStages = 3;
+template <bool kFp4>
+constexpr int stages_for() { return kFp4 ? 6 : 3; }   // 64 KB bf16 pages / 18 KB NVFP4 pages
 constexpr int kCWarps = 4;
 constexpr int kBoxBytes = kBlock * 64 * 2;       // 128 rows x 128 B (64 fp16/bf16)
 constexpr int kTileBytes = 4 * kBoxBytes;        // K lo/hi + V lo/hi = 64 KB
@@ -68,11 +69,11 @@ __host__ __device__ constexpr SmemLayout gqa_layout() {
   SmemLayout s{};
   s.stages = 0;
   const uint32_t stage_bytes = kFp4 ? kFp4StageBytes : kTileBytes;
-  s.tiles = s.stages + kGqaStages * stage_bytes;
-  s.comb_o = s.tiles + (kFp4 ? 2 * kTileBytes : 0);
+  s.tiles = s.stages + stages_for<kFp4>() * stage_bytes;
+  s.comb_o = s.tiles + (kFp4 ? kTileBytes : 0);
   s.comb_ml = s.comb_o + kCWarps * kGroup * kDim * 4;
   s.bars = s.comb_ml + kCWarps * kGroup * 2 * 4;
-  s.total = s.bars + (2 * kGqaStages + 2) * 8 + 16;   // + the last-arriver flag
+  s.total = s.bars + (2 * stages_for<kFp4>() + 2) * 8 + 16;   // + the last-arriver flag
   return s;
 }
 
@@ -162,12 +163,13 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
   extern __shared__ uint8_t smem_raw[];
   constexpr SmemLayout Ly = gqa_layout<kFp4>();
   constexpr uint32_t kStageBytes = kFp4 ? kFp4StageBytes : kTileBytes;
+  constexpr int kGqaStages = stages_for<kFp4>();
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base_addr = (raw + 1023u) & ~1023u;
   uint8_t* sm = smem_raw + (base_addr - raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + Ly.bars);
   uint64_t* empty = full + kGqaStages;
-  uint64_t* gbar = empty + kGqaStages;   // [0]: partials written, [1]: partials read / tile ready
+  uint64_t* gbar = empty + kGqaStages;   // [0]: partials written, [1]: partials read
   float* comb_o = reinterpret_cast<float*>(sm + Ly.comb_o);
   float* comb_m = reinterpret_cast<float*>(sm + Ly.comb_ml);
   float* comb_l = comb_m + kCWarps * kGroup;
@@ -453,8 +455,10 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     if (!mbar_wait(smem_addr(&full[s]), static_cast<uint32_t>((i / kGqaStages) & 1))) { ok = false; break; }
     uint32_t kt = base_addr + Ly.stages + s * kStageBytes;   // bf16 tile: K lo, K hi, V lo, V hi
     if (kFp4) {
-      // Expand this page's NVFP4 K and V into the fp16 tile (one token row per thread).
-      const uint32_t tile = base_addr + Ly.tiles + static_cast<uint32_t>(i & 1) * kTileBytes;
+      // Expand this page's NVFP4 K and V into the fp16 tile. Thread ct expands
+      // token row ct = 32 w + lane, which only its own warp reads afterwards, so
+      // a warp-level barrier suffices and the tile can be reused at once.
+      const uint32_t tile = base_addr + Ly.tiles;
       const uint8_t* st = sm + Ly.stages + s * kStageBytes;
       const int t = ct;
 #pragma unroll
@@ -492,28 +496,33 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
-      if (!group_sync(smem_addr(&gbar[1]), gph[1], lane)) { ok = false; break; }
       kt = tile;
     }
 
     // ---- S = Q K^T for this warp's 32 tokens (4 n-tiles of 8 tokens).
+    // The four n-tiles are independent accumulation chains, interleaved per
+    // pair of k-steps so that the mma latencies overlap.
     float sc[4][4];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-      const int tok = 32 * w + 8 * nt + (lane & 7);
+    for (int nt = 0; nt < 4; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
-      for (int sp = 0; sp < 4; ++sp) {
-        const int chunk = 4 * sp + (lane >> 3);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(swz(kt + (chunk >> 3) * kBoxBytes, tok, chunk & 7), b0, b1, b2, b3);
-        if (kFp4) {
-          mma_f16(sc[nt], qf[2 * sp], b0, b1);
-          mma_f16(sc[nt], qf[2 * sp + 1], b2, b3);
-        } else {
-          mma_bf16(sc[nt], qf[2 * sp], b0, b1);
-          mma_bf16(sc[nt], qf[2 * sp + 1], b2, b3);
-        }
+    for (int sp = 0; sp < 4; ++sp) {
+      const int chunk = 4 * sp + (lane >> 3);
+      uint32_t b[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int tok = 32 * w + 8 * nt + (lane & 7);
+        ldsm_x4(swz(kt + (chunk >> 3) * kBoxBytes, tok, chunk & 7), b[nt][0], b[nt][1], b[nt][2], b[nt][3]);
+      }
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        if (kFp4) mma_f16(sc[nt], qf[2 * sp], b[nt][0], b[nt][1]);
+        else mma_bf16(sc[nt], qf[2 * sp], b[nt][0], b[nt][1]);
+      }
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        if (kFp4) mma_f16(sc[nt], qf[2 * sp + 1], b[nt][2], b[nt][3]);
+        else mma_bf16(sc[nt], qf[2 * sp + 1], b[nt][2], b[nt][3]);
       }
     }
     // ---- causal limit inside the local block
@@ -694,7 +703,7 @@ cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRec
   err = launch_pdl(kern, dim3(C), dim3(32 * (1 + kCWarps)), smem, stream, tk, tv, p);
   rec->set("sparse_gqa %s persistent %s grid=%d block=%d smem=%zu stages=%d items=%lld",
            a.nvfp4 ? "nvfp4_dequant_f16_mma" : "bf16_tma_mma", p.row_aligned ? "whole_rows" : "split_k_fused_combine",
-           C, 32 * (1 + kCWarps), smem, kGqaStages, static_cast<long long>(p.W));
+           C, 32 * (1 + kCWarps), smem, a.nvfp4 ? stages_for<true>() : stages_for<false>(), static_cast<long long>(p.W));
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
