@@ -63,7 +63,7 @@ def workload_desc(w):
     ctx = f"context {w.ctx}" if w.ctx else f"context U[{w.ctx_range[0]},{w.ctx_range[1]}]"
     return (f"msa_decode_{w.name}: batch {w.batch}, {ctx}, q_len {w.q_len}, {w.n_heads} q / {w.n_kv_heads} kv / "
             f"{w.n_idx_heads} index heads, head_dim {w.head_dim}, block {w.block_size}, top-{w.topk} incl. local, "
-            f"{'FP8 E4M3' if w.idx_dtype == 'fp8' else 'fp32'} index keys, {w.kv_dtype} KV")
+            f"{ {'fp8': 'FP8 E4M3', 'nvfp4': 'NVFP4', 'f32': 'fp32'}[w.idx_dtype]} index keys, {w.kv_dtype} KV")
 
 
 def measured_peaks():
@@ -156,8 +156,9 @@ def index_bytes(dw):
     per-token scales for all index heads, the index queries, the score rows."""
     w = dw.w
     units = sum(max(0, (int(L) - 1) // w.block_size) for L in dw.lens)
-    per_unit = w.n_idx_heads * w.block_size * (w.head_dim * (1 if w.idx_dtype == "fp8" else 4)
-                                               + (4 if w.idx_dtype == "fp8" else 0))
+    per_token_head = {"fp8": w.head_dim + 4, "nvfp4": w.head_dim // 2 + w.head_dim // 16,
+                      "f32": 4 * w.head_dim}[w.idx_dtype]
+    per_unit = w.n_idx_heads * w.block_size * per_token_head
     q = dw.q_idx.numel() * dw.q_idx.element_size()
     scores = dw.scores.numel() * 4
     return units * per_unit + q + scores
@@ -328,11 +329,13 @@ def cpu_baseline(w, n_requests, budget_s=20.0):
     from oracle import run as orun
     lens = synth.seq_lens(w)
     kg = kv = float(np.float32(synth.NVFP4_SYNTH_GLOBAL)) if w.kv_dtype == "nvfp4" else 1.0
+    idx_g = float(np.float32(synth.NVFP4_IDX_SYNTH_GLOBAL)) if w.idx_dtype == "nvfp4" else 1.0
     spent, done = 0.0, 0
     for b in range(min(n_requests, w.batch)):
         req = synth.request(w, b, int(lens[b]))
         t0 = time.perf_counter()
-        orun.run_request(req, int(lens[b]), w.topk, w.softmax_scale, w.block_size, w.idx_dtype, w.kv_dtype, kg, kv)
+        orun.run_request(req, int(lens[b]), w.topk, w.softmax_scale, w.block_size, w.idx_dtype, w.kv_dtype, kg, kv,
+                         idx_global=idx_g)
         spent += time.perf_counter() - t0
         done += 1
         if spent > budget_s:
@@ -350,6 +353,7 @@ def run_reference(args, world, rank):
     w = synth.WORKLOADS[args.workload]
     lens = synth.seq_lens(w)
     kg = kv = float(np.float32(synth.NVFP4_SYNTH_GLOBAL)) if w.kv_dtype == "nvfp4" else 1.0
+    idx_g = float(np.float32(synth.NVFP4_IDX_SYNTH_GLOBAL)) if w.idx_dtype == "nvfp4" else 1.0
     reqs = {}
 
     def one(s):
@@ -358,7 +362,7 @@ def run_reference(args, world, rank):
             reqs[b] = synth.request(w, b, int(lens[b]))
         t0 = time.perf_counter()
         orun.run_request(reqs[b], int(lens[b]), w.topk, w.softmax_scale, w.block_size, w.idx_dtype, w.kv_dtype,
-                         kg, kv)
+                         kg, kv, idx_global=idx_g)
         return time.perf_counter() - t0
 
     for s in range(args.warmup):

@@ -23,18 +23,20 @@
 
 namespace msa {
 
-constexpr int kIdxStages = 3;
+constexpr int kIdxStages = 3;       // 66.5 KB pages (FP8 keys, 4 heads)
+constexpr int kIdxStagesFp4 = 5;    // 36 KB pages (NVFP4 keys, 4 heads)
 constexpr int kMaxIdxHeads = 4;
 constexpr uint32_t kFull = 0xffffffffu;
 
 struct IdxParams {
   const void* q;
   const void* keys;
-  const float* scale;
+  const void* scale;        // fp32 per token (FP8 keys) or E4M3 per 16 values (NVFP4 keys)
   const int32_t* block_table;
   const int32_t* seq_lens;
   float* scores;
   uint32_t* flags;
+  float global_scale;       // NVFP4 keys: fp32 per-tensor scale
   int B, Q, I, NB, P;
 };
 
@@ -93,13 +95,21 @@ __device__ void fill_tails(const IdxParams& p, const int* pref) {
   }
 }
 
-template <int kStages>
+// Bytes of one page of index keys / key scales, per index head.
+template <bool kFp4Keys>
+__host__ __device__ constexpr uint32_t key_bytes_per_head() { return kFp4Keys ? kBlock * kDim / 2 : kBlock * kDim; }
+template <bool kFp4Keys>
+__host__ __device__ constexpr uint32_t scale_bytes_per_head() { return kFp4Keys ? kBlock * kDim / 16 : kBlock * 4; }
+
+// kFp4Keys = false: E4M3 keys + fp32 per-token scale. true: NVFP4 keys (E2M1
+// pairs, E4M3 scale per 16 values, fp32 global scale).
+template <int kStages, bool kFp4Keys>
 __global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_kernel(IdxParams p) {
   extern __shared__ __align__(1024) uint8_t smem_fp8[];
   uint8_t* smem = smem_fp8;
   const int I = p.I;
-  const uint32_t key_bytes = static_cast<uint32_t>(I) * kBlock * kDim;   // I x 16 KB
-  const uint32_t scale_bytes = static_cast<uint32_t>(I) * kBlock * 4;    // I x 512 B
+  const uint32_t key_bytes = static_cast<uint32_t>(I) * key_bytes_per_head<kFp4Keys>();
+  const uint32_t scale_bytes = static_cast<uint32_t>(I) * scale_bytes_per_head<kFp4Keys>();
   const uint32_t stage_bytes = key_bytes + scale_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * stage_bytes);
   uint64_t* empty = full + kStages;
@@ -160,7 +170,8 @@ __global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_ke
               const uint32_t dst = smem_addr(smem + s * stage_bytes);
               mbar_arrive_expect_tx(fb, stage_bytes);
               bulk_g2s(dst, keys + static_cast<int64_t>(page) * key_bytes, key_bytes, fb, pol);
-              bulk_g2s(dst + key_bytes, p.scale + static_cast<int64_t>(page) * I * kBlock, scale_bytes, fb, pol);
+              bulk_g2s(dst + key_bytes, static_cast<const uint8_t*>(p.scale) + static_cast<int64_t>(page) * scale_bytes,
+                       scale_bytes, fb, pol);
             }
           }
         }
@@ -197,11 +208,14 @@ __global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_ke
       // Index-query fragment of position gr for this request and head.
       float qv[32];
       if (gr < p.Q) {
+        // dims this thread feeds to the mma: FP8 keys 16c..16c+15 and 64+16c..64+16c+15
+        // (two 16-byte runs of a key row), NVFP4 keys 32c..32c+31 (one 16-byte run)
         const uint16_t* qp = qbase + ((static_cast<int64_t>(b) * p.Q + gr) * I + g) * kDim;
-        const uint4 a0 = *reinterpret_cast<const uint4*>(qp + 16 * c);
-        const uint4 a1 = *reinterpret_cast<const uint4*>(qp + 16 * c + 8);
-        const uint4 a2 = *reinterpret_cast<const uint4*>(qp + 64 + 16 * c);
-        const uint4 a3 = *reinterpret_cast<const uint4*>(qp + 64 + 16 * c + 8);
+        const int o0 = kFp4Keys ? 32 * c : 16 * c, o1 = kFp4Keys ? 32 * c + 16 : 64 + 16 * c;
+        const uint4 a0 = *reinterpret_cast<const uint4*>(qp + o0);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(qp + o0 + 8);
+        const uint4 a2 = *reinterpret_cast<const uint4*>(qp + o1);
+        const uint4 a3 = *reinterpret_cast<const uint4*>(qp + o1 + 8);
         const uint32_t w[16] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w,
                                 a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
 #pragma unroll
@@ -220,7 +234,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_ke
       amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
       const int sh = fp16_shift_for(amax);
       const float f = exp2_int(sh);
-      const float inv = gr < p.Q ? exp2_int(-sh) : 0.f;
+      const float inv = gr < p.Q ? exp2_int(-sh) * (kFp4Keys ? p.global_scale : 1.f) : 0.f;
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         qb[s][0] = pack_f16x2(qv[4 * s] * f, qv[4 * s + 1] * f);
@@ -239,7 +253,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_ke
       break;
     }
     float m0 = -INFINITY, m1 = -INFINITY;
-    if (valid[s]) {
+    if (valid[s] && !kFp4Keys) {
       const uint8_t* kb = smem + s * stage_bytes + g * (kBlock * kDim);
       const float* sc = reinterpret_cast<const float*>(smem + s * stage_bytes + key_bytes) + g * kBlock;
 #pragma unroll 2
@@ -263,6 +277,42 @@ __global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_ke
         const float s0 = sc[16 * t + gr], s1 = sc[16 * t + gr + 8];
         m0 = fmaxf(m0, fmaxf(acc[0] * s0, acc[2] * s1));
         m1 = fmaxf(m1, fmaxf(acc[1] * s0, acc[3] * s1));
+      }
+    } else if (valid[s]) {
+      // NVFP4 keys: 64 B of E2M1 pairs per token row, 8 E4M3 scales; e2m1 x e4m3
+      // is exact in fp16, so the fragment is the decoded key up to the global scale.
+      const uint8_t* kb = smem + s * stage_bytes + g * (kBlock * kDim / 2);
+      const uint8_t* sb = smem + s * stage_bytes + key_bytes + g * (kBlock * kDim / 16);
+#pragma unroll 2
+      for (int t = 0; t < 8; ++t) {
+        const int r0 = 16 * t + gr, r1 = r0 + 8;
+        const uint4 x = *reinterpret_cast<const uint4*>(kb + r0 * (kDim / 2) + 16 * c);
+        const uint4 y = *reinterpret_cast<const uint4*>(kb + r1 * (kDim / 2) + 16 * c);
+        const uint32_t sx = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sb + r0 * (kDim / 16) + 2 * c));
+        const uint32_t sy = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sb + r1 * (kDim / 16) + 2 * c));
+        const __half2 sx0 = __half2half2(__ushort_as_half(static_cast<unsigned short>(sx & 0xFFFF)));
+        const __half2 sx1 = __half2half2(__ushort_as_half(static_cast<unsigned short>(sx >> 16)));
+        const __half2 sy0 = __half2half2(__ushort_as_half(static_cast<unsigned short>(sy & 0xFFFF)));
+        const __half2 sy1 = __half2half2(__ushort_as_half(static_cast<unsigned short>(sy >> 16)));
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+        const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          uint32_t xl, xh, yl, yh;
+          e2m1x4_to_f16x2x2(static_cast<uint16_t>(xw[k >> 1] >> (16 * (k & 1))), xl, xh);
+          e2m1x4_to_f16x2x2(static_cast<uint16_t>(yw[k >> 1] >> (16 * (k & 1))), yl, yh);
+          const __half2 scx = k < 4 ? sx0 : sx1, scy = k < 4 ? sy0 : sy1;
+          __half2 h0 = __hmul2(*reinterpret_cast<__half2*>(&xl), scx);
+          __half2 h1 = __hmul2(*reinterpret_cast<__half2*>(&yl), scy);
+          __half2 h2 = __hmul2(*reinterpret_cast<__half2*>(&xh), scx);
+          __half2 h3 = __hmul2(*reinterpret_cast<__half2*>(&yh), scy);
+          const uint32_t a[4] = {*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1),
+                                 *reinterpret_cast<uint32_t*>(&h2), *reinterpret_cast<uint32_t*>(&h3)};
+          mma_f16(acc, a, qb[k][0], qb[k][1]);
+        }
+        m0 = fmaxf(m0, fmaxf(acc[0], acc[2]));
+        m1 = fmaxf(m1, fmaxf(acc[1], acc[3]));
       }
     }
     __syncwarp();
@@ -354,20 +404,23 @@ __global__ void __launch_bounds__(128) index_score_f32_kernel(IdxParams p) {
 }
 
 cudaError_t launch_index_score(const IndexArgs& a, cudaStream_t stream, DispatchRecord* rec) {
-  IdxParams p{a.q, a.keys, a.scale, a.block_table, a.seq_lens, a.scores, a.flags, a.B, a.Q, a.I, a.NB, a.P};
+  IdxParams p{a.q, a.keys, a.scale, a.block_table, a.seq_lens, a.scores, a.flags, a.global_scale,
+              a.B, a.Q, a.I, a.NB, a.P};
   const int sms = device_sm_count();
   cudaError_t err;
-  if (a.fp8) {
-    const size_t stage = static_cast<size_t>(a.I) * kBlock * kDim + static_cast<size_t>(a.I) * kBlock * 4;
-    const size_t smem = kIdxStages * stage + 2 * kIdxStages * 8 + kIdxStages * 4 + (a.B + 1) * 4;
-    err = cudaFuncSetAttribute(index_score_fp8_kernel<kIdxStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem));
+  if (a.fp8 || a.fp4) {
+    const int stages = a.fp4 ? kIdxStagesFp4 : kIdxStages;
+    const size_t stage = a.fp4 ? static_cast<size_t>(a.I) * (key_bytes_per_head<true>() + scale_bytes_per_head<true>())
+                               : static_cast<size_t>(a.I) * (key_bytes_per_head<false>() + scale_bytes_per_head<false>());
+    const size_t smem = stages * stage + 2 * stages * 8 + stages * 4 + (a.B + 1) * 4;
+    auto kern = a.fp4 ? index_score_fp8_kernel<kIdxStagesFp4, true> : index_score_fp8_kernel<kIdxStages, false>;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     const int grid = sms;
-    err = launch_pdl(index_score_fp8_kernel<kIdxStages>, dim3(grid), dim3(32 * (1 + a.I)), smem, stream, p);
+    err = launch_pdl(kern, dim3(grid), dim3(32 * (1 + a.I)), smem, stream, p);
     if (err != cudaSuccess) return err;
-    rec->set("index_score fp8_mma_f16 grid=%d block=%d smem=%zu stages=%d q_len=%d idx_heads=%d", grid,
-             32 * (1 + a.I), smem, kIdxStages, a.Q, a.I);
+    rec->set("index_score %s grid=%d block=%d smem=%zu stages=%d q_len=%d idx_heads=%d",
+             a.fp4 ? "nvfp4_mma_f16" : "fp8_mma_f16", grid, 32 * (1 + a.I), smem, stages, a.Q, a.I);
   } else {
     const size_t smem = ((static_cast<size_t>(a.B) + 1) * 4 + 15) / 16 * 16 + 4 * 8 * kDim * 4;
     err = cudaFuncSetAttribute(index_score_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

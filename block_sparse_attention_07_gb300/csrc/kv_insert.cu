@@ -19,17 +19,17 @@ struct InsertParams {
   uint8_t* k_scale; uint8_t* v_scale;
   float k_global, v_global;
   int idx_fp8;
-  void* idx_keys;             // f32 or u8 [P, G, BS, D]
-  float* idx_scale;           // [P, G, BS]
+  int idx_fp4;
+  void* idx_keys;             // f32 / u8 [P, G, BS, D], or u8 [P, G, BS, D/2] NVFP4
+  float* idx_scale;           // fp8: [P, G, BS]
+  uint8_t* idx_block_scale;   // nvfp4: [P, G, BS, D/16]
+  float idx_global;
   uint32_t* flags;
 };
 
 // NVFP4: lane owns 4 consecutive values; 4 lanes form one 16-value group.
-__device__ __forceinline__ void quant_nvfp4_row(const uint16_t* src, uint8_t* codes, uint8_t* scales, float g,
-                                                int lane) {
-  const uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
-  float x[4] = {bf16_bits_to_f32(raw.x & 0xFFFF), bf16_bits_to_f32(raw.x >> 16), bf16_bits_to_f32(raw.y & 0xFFFF),
-                bf16_bits_to_f32(raw.y >> 16)};
+__device__ __forceinline__ void quant_nvfp4_vals(const float (&x)[4], uint8_t* codes, uint8_t* scales, float g,
+                                                 int lane) {
   float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
   a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
   a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
@@ -46,6 +46,14 @@ __device__ __forceinline__ void quant_nvfp4_row(const uint16_t* src, uint8_t* co
   }
   *reinterpret_cast<uint16_t*>(codes + 2 * lane) = packed;
   if ((lane & 3) == 0) scales[lane >> 2] = sb_code;
+}
+
+__device__ __forceinline__ void quant_nvfp4_row(const uint16_t* src, uint8_t* codes, uint8_t* scales, float g,
+                                                int lane) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
+  const float x[4] = {bf16_bits_to_f32(raw.x & 0xFFFF), bf16_bits_to_f32(raw.x >> 16),
+                      bf16_bits_to_f32(raw.y & 0xFFFF), bf16_bits_to_f32(raw.y >> 16)};
+  quant_nvfp4_vals(x, codes, scales, g, lane);
 }
 
 __global__ void __launch_bounds__(256) kv_insert_kernel(InsertParams p) {
@@ -90,7 +98,10 @@ __global__ void __launch_bounds__(256) kv_insert_kernel(InsertParams p) {
         const float4 raw = *reinterpret_cast<const float4*>(static_cast<const float*>(p.idx_new) + src + 4 * lane);
         x[0] = raw.x; x[1] = raw.y; x[2] = raw.z; x[3] = raw.w;
       }
-      if (!p.idx_fp8) {
+      if (p.idx_fp4) {
+        quant_nvfp4_vals(x, static_cast<uint8_t*>(p.idx_keys) + row * (kDim / 2),
+                         p.idx_block_scale + row * (kDim / 16), p.idx_global, lane);
+      } else if (!p.idx_fp8) {
         *reinterpret_cast<float4*>(static_cast<float*>(p.idx_keys) + row * kDim + 4 * lane) =
             make_float4(x[0], x[1], x[2], x[3]);
       } else {
@@ -127,8 +138,11 @@ cudaError_t launch_kv_insert(const InsertArgs& a, cudaStream_t stream, DispatchR
   p.v_scale = static_cast<uint8_t*>(a.v_scale);
   p.k_global = a.k_global; p.v_global = a.v_global;
   p.idx_fp8 = a.idx_fp8;
+  p.idx_fp4 = a.idx_fp4;
   p.idx_keys = a.idx_keys;
   p.idx_scale = a.idx_scale;
+  p.idx_block_scale = static_cast<uint8_t*>(a.idx_block_scale);
+  p.idx_global = a.idx_global;
   p.flags = a.flags;
   const int64_t warps = static_cast<int64_t>(a.T) * a.G;
   int64_t blocks = (warps + 7) / 8;
@@ -138,7 +152,8 @@ cudaError_t launch_kv_insert(const InsertArgs& a, cudaStream_t stream, DispatchR
   const cudaError_t err = launch_pdl(kv_insert_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
   if (err != cudaSuccess) return err;
   rec->set("kv_insert %s%s grid=%lld block=256 tokens=%d", a.kv_nvfp4 ? "nvfp4" : "bf16",
-           a.idx_new ? (a.idx_fp8 ? "+idx_fp8" : "+idx_f32") : "", static_cast<long long>(blocks), a.T);
+           a.idx_new ? (a.idx_fp4 ? "+idx_nvfp4" : a.idx_fp8 ? "+idx_fp8" : "+idx_f32") : "",
+           static_cast<long long>(blocks), a.T);
   return cudaGetLastError();
 }
 

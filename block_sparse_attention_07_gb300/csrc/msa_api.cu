@@ -101,6 +101,13 @@ msa_status_t msa_kv_insert_quant(const msa_dims_t* dims, const void* k_new, cons
       if (idx_cache->scale == nullptr) return MSA_ERR_INVALID_ARG;
       if (idx_new_dtype != MSA_F32 && idx_new_dtype != MSA_BF16) return MSA_ERR_UNSUPPORTED;
       a.idx_fp8 = 1;
+    } else if (idx_cache->dtype == MSA_NVFP4) {
+      if (idx_cache->block_scale == nullptr) return MSA_ERR_INVALID_ARG;
+      if (!(idx_cache->global_scale > 0.f) || idx_cache->global_scale > 3.0e38f) return MSA_ERR_INVALID_ARG;
+      if (idx_new_dtype != MSA_F32 && idx_new_dtype != MSA_BF16) return MSA_ERR_UNSUPPORTED;
+      a.idx_fp4 = 1;
+      a.idx_block_scale = idx_cache->block_scale;
+      a.idx_global = idx_cache->global_scale;
     } else if (idx_cache->dtype == MSA_F32) {
       if (idx_new_dtype != MSA_F32) return MSA_ERR_UNSUPPORTED;
     } else {
@@ -138,10 +145,21 @@ msa_status_t msa_index_score(const msa_dims_t* dims, const void* idx_q, msa_dtyp
   if (!aligned16(idx_q) || !aligned16(idx_cache->keys)) return MSA_ERR_INVALID_ARG;
   IndexArgs a;
   a.fp8 = 0;
+  a.fp4 = 0;
+  a.scale = nullptr;
+  a.global_scale = 1.f;
   if (idx_cache->dtype == MSA_FP8_E4M3) {
     if (q_dtype != MSA_BF16) return MSA_ERR_UNSUPPORTED;
     if (idx_cache->scale == nullptr || !aligned16(idx_cache->scale)) return MSA_ERR_INVALID_ARG;
     a.fp8 = 1;
+    a.scale = idx_cache->scale;
+  } else if (idx_cache->dtype == MSA_NVFP4) {
+    if (q_dtype != MSA_BF16) return MSA_ERR_UNSUPPORTED;
+    if (idx_cache->block_scale == nullptr || !aligned16(idx_cache->block_scale)) return MSA_ERR_INVALID_ARG;
+    if (!(idx_cache->global_scale > 0.f) || idx_cache->global_scale > 3.0e38f) return MSA_ERR_INVALID_ARG;
+    a.fp4 = 1;
+    a.scale = idx_cache->block_scale;
+    a.global_scale = idx_cache->global_scale;
   } else if (idx_cache->dtype == MSA_F32) {
     if (q_dtype != MSA_F32) return MSA_ERR_UNSUPPORTED;
   } else {
@@ -149,7 +167,6 @@ msa_status_t msa_index_score(const msa_dims_t* dims, const void* idx_q, msa_dtyp
   }
   a.q = idx_q;
   a.keys = idx_cache->keys;
-  a.scale = idx_cache->scale;
   a.block_table = block_table;
   a.seq_lens = seq_lens;
   a.scores = scores;

@@ -58,21 +58,25 @@ struct InsertArgs {
   void* v_scale;
   float k_global, v_global;
   int idx_fp8;
+  int idx_fp4;
   void* idx_keys;
   float* idx_scale;
+  void* idx_block_scale;
+  float idx_global;
   uint32_t* flags;
 };
 
 struct IndexArgs {
   const void* q;          // [B, Q, I, D] f32 or bf16
-  const void* keys;       // [P, I, BS, D] f32 or u8
-  const float* scale;     // [P, I, BS] (fp8 only)
+  const void* keys;       // [P, I, BS, D] f32 / u8 E4M3, or [P, I, BS, D/2] NVFP4
+  const void* scale;      // fp8: fp32 [P, I, BS]; nvfp4: E4M3 [P, I, BS, D/16]
+  float global_scale;     // nvfp4 only
   const int32_t* block_table;
   const int32_t* seq_lens;
   float* scores;          // [B, Q, I, NB]
   uint32_t* flags;
   int B, Q, I, NB, P;
-  int fp8;
+  int fp8, fp4;
 };
 
 struct SelectArgs {

@@ -43,7 +43,8 @@ class _KVCache(ctypes.Structure):
 
 
 class _IndexCache(ctypes.Structure):
-    _fields_ = [("dtype", ctypes.c_int), ("keys", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
+    _fields_ = [("dtype", ctypes.c_int), ("keys", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("block_scale", ctypes.c_void_p), ("global_scale", ctypes.c_float)]
 
 
 class MSAError(RuntimeError):
@@ -135,13 +136,16 @@ class KVCache:
 
 @dataclasses.dataclass
 class IndexCache:
-    """F32: keys f32 [P, I, BS, D]. FP8_E4M3: keys uint8 [P, I, BS, D], scale f32 [P, I, BS]."""
+    """F32: keys f32 [P, I, BS, D]. FP8_E4M3: keys uint8 [P, I, BS, D], scale f32 [P, I, BS].
+    NVFP4: keys uint8 [P, I, BS, D/2], block_scale uint8 [P, I, BS, D/16], global_scale (host float)."""
     dtype: int
     keys: object
     scale: object = None
+    block_scale: object = None
+    global_scale: float = 1.0
 
     def c(self):
-        return _IndexCache(self.dtype, _ptr(self.keys), _ptr(self.scale))
+        return _IndexCache(self.dtype, _ptr(self.keys), _ptr(self.scale), _ptr(self.block_scale), self.global_scale)
 
 
 class Prepared:

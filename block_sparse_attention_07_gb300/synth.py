@@ -19,6 +19,8 @@ blocks including the local one, at most 2,048 keys per query):
                 of 128), 10 % of blocks planted +2 sigma.
 * ``spec8``     batch 32, 65,536 tokens, 8 query positions per request.
 * ``nvfp4_256k`` batch 16, 262,144 tokens, NVFP4 KV.
+* ``b32_32k_fp4idx`` and ``fp4_256k``: as ``b32_32k`` and ``nvfp4_256k`` with
+  NVFP4 index keys.
 """
 from __future__ import annotations
 
@@ -39,7 +41,7 @@ class Workload:
     q_len: int
     ctx: int | None            # fixed context length, or None for ragged
     ctx_range: tuple | None    # (lo, hi) for ragged lengths
-    idx_dtype: str             # "f32" (fp32 index keys/query) or "fp8" (bf16 source, FP8 cache)
+    idx_dtype: str             # "f32" (fp32 index keys/query), "fp8" or "nvfp4" (bf16 source, quantised cache)
     kv_dtype: str              # "bf16" or "nvfp4"
     planted: bool              # ragged recipe: 10 % of blocks offset by +2 sigma
     n_heads: int = 64
@@ -61,6 +63,9 @@ WORKLOADS = {
     "ragged": Workload("ragged", 64, 1, None, (8192, 131072), "fp8", "bf16", True, seed=20261204),
     "spec8": Workload("spec8", 32, 8, 65536, None, "fp8", "bf16", False, seed=20261205),
     "nvfp4_256k": Workload("nvfp4_256k", 16, 1, 262144, None, "fp8", "nvfp4", False, seed=20261206),
+    # NVFP4 index keys (the indexer format of the NVFP4 checkpoint's serving recipe)
+    "b32_32k_fp4idx": Workload("b32_32k_fp4idx", 32, 1, 32768, None, "nvfp4", "bf16", False, seed=20261207),
+    "fp4_256k": Workload("fp4_256k", 16, 1, 262144, None, "nvfp4", "nvfp4", False, seed=20261208),
 }
 
 # Field ids of the per-request random streams.
@@ -70,6 +75,8 @@ _F_LEN, _F_PERM, _F_Q, _F_QIDX, _F_IDXK, _F_OFF, _F_K, _F_V, _F_PLANT = range(9)
 # constant (amax 6, i.e. six standard deviations of N(0,1) data, over the
 # largest E2M1 magnitude times the largest E4M3 magnitude).
 NVFP4_SYNTH_GLOBAL = 6.0 / (6.0 * 448.0)
+# Index keys carry block offsets on top of N(0,1); their calibration amax is 8.
+NVFP4_IDX_SYNTH_GLOBAL = 8.0 / (6.0 * 448.0)
 
 
 def scaled(w: Workload, **changes) -> Workload:

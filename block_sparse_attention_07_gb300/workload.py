@@ -51,6 +51,12 @@ class DeviceWorkload:
             self.idx_cache = msa.IndexCache(msa.F32, torch.zeros((P, I, BS, D), dtype=torch.float32, device=dev))
             self.q_idx_dtype = msa.F32
             self.idx_new_dtype = msa.F32
+        elif w.idx_dtype == "nvfp4":
+            self.idx_cache = msa.IndexCache(msa.NVFP4, torch.zeros((P, I, BS, D // 2), dtype=torch.uint8, device=dev),
+                                            None, torch.zeros((P, I, BS, D // 16), dtype=torch.uint8, device=dev),
+                                            float(np.float32(synth.NVFP4_IDX_SYNTH_GLOBAL)))
+            self.q_idx_dtype = msa.BF16
+            self.idx_new_dtype = msa.BF16
         else:
             self.idx_cache = msa.IndexCache(msa.FP8_E4M3, torch.zeros((P, I, BS, D), dtype=torch.uint8, device=dev),
                                             torch.zeros((P, I, BS), dtype=torch.float32, device=dev))

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define MSA_ABI_VERSION 1
+#define MSA_ABI_VERSION 2
 
 typedef enum {
   MSA_OK = 0,
@@ -117,11 +117,18 @@ typedef struct {
  *   MSA_F32:      keys = fp32 [P, I, BS, D]; scale = NULL.
  *   MSA_FP8_E4M3: keys = uint8 E4M3 [P, I, BS, D]; scale = fp32 [P, I, BS],
  *                 one per (token, index head); key value = e4m3 * scale.
+ *   MSA_NVFP4:    keys = uint8 [P, I, BS, D/2] E2M1 pairs (low nibble = even
+ *                 element); block_scale = uint8 E4M3 [P, I, BS, D/16];
+ *                 global_scale = fp32 per-tensor scale (host value, > 0);
+ *                 key value = e2m1 * e4m3 * global ("MiniMax-M3.1-Flash
+ *                 Day-0 対応", section "試し方": indexer_kv_dtype nvfp4).
  *   16-byte aligned pointers. */
 typedef struct {
   msa_dtype_t dtype;
   void* keys;
   float* scale;
+  void* block_scale;
+  float global_scale;
 } msa_index_cache_t;
 
 /* ABI version of the loaded library (MSA_ABI_VERSION at build time). */
@@ -141,11 +148,11 @@ msa_status_t msa_get_last_dispatch(char* buf, size_t len);
  * implemented is:
  *   FP8 index keys: s = amax / 448 over the token's D values of that head (fp32,
  *     IEEE division), code = E4M3_RNE_satfinite(x / s); s = 0 -> codes 0.
- *   NVFP4 K/V: per 16 values sb = E4M3_RNE((amax16 / 6) / global),
- *     code = E2M1_RNE_satfinite(x / (sb * global)); sb == 0 -> codes 0.
+ *   NVFP4 K/V and NVFP4 index keys: per 16 values sb = E4M3_RNE((amax16 / 6) /
+ *     global), code = E2M1_RNE_satfinite(x / (sb * global)); sb == 0 -> codes 0.
  *   bf16 K/V and fp32 index keys are copied.
  * k_new, v_new: bf16 [T, G, D]. idx_k_new: [T, I, D] of idx_new_dtype
- * (MSA_F32 or MSA_BF16; MSA_BF16 requires an FP8 index cache), or NULL to
+ * (MSA_F32 or MSA_BF16; MSA_BF16 requires an FP8 or NVFP4 index cache), or NULL to
  * leave the index cache untouched (idx_cache may then be NULL).
  * slot_mapping: int64 [T], slot = page * BS + offset; a negative slot skips
  * the token; slot >= P * BS skips it and sets MSA_FLAG_BAD_SLOT.
@@ -160,12 +167,13 @@ msa_status_t msa_kv_insert_quant(const msa_dims_t* dims, const void* k_new, cons
  * Stage 1, block scoring ("MSA 実行プロセス" step 1). For every request b,
  * position j, index head g and block n < l_j (the query's local block):
  *   scores[b, j, g, n] = max over the block's 128 tokens t of s_t * (q_idx[b, j, g] . k_t)
- * with s_t the key's per-token scale (1 for fp32 keys); no other scale is
- * applied (a positive constant cannot change the selection). All other
+ * with s_t the key's per-token scale (1 for fp32 and NVFP4 keys; NVFP4 keys
+ * carry their block and global scales in k_t); no other scale is applied (a
+ * positive constant cannot change the selection). All other
  * entries up to max_blocks_per_seq are set to -inf. All Q positions of a
  * request are computed from one load of each index key.
  * idx_q: [B, Q, I, D] in q_dtype (MSA_F32 with an MSA_F32 index cache,
- * MSA_BF16 with an MSA_FP8_E4M3 one). block_table: int32 [B, NB].
+ * MSA_BF16 with an MSA_FP8_E4M3 or MSA_NVFP4 one). block_table: int32 [B, NB].
  * seq_lens: int32 [B]. scores: fp32 [B, Q, I, NB].
  */
 msa_status_t msa_index_score(const msa_dims_t* dims, const void* idx_q, msa_dtype_t q_dtype,

@@ -27,15 +27,22 @@ def to_f32(a: np.ndarray) -> np.ndarray:
     return np.asarray(a, dtype=np.float32)
 
 
-def cached_index_keys(idx_k: np.ndarray, idx_dtype: str):
-    """The index cache's content for these tokens, decoded: (keys fp64 [L, I, D], scale fp64 [L, I] or None)."""
+def cached_index_keys(idx_k: np.ndarray, idx_dtype: str, idx_global: float = 1.0):
+    """The index cache's content for these tokens, decoded: (keys fp64 [L, I, D], scale fp64 [L, I] or None).
+
+    FP8 keys carry a per-token scale; NVFP4 keys (E2M1 x E4M3 block scale x
+    global scale) decode to their value and have no per-token scale.
+    """
     L = idx_k.shape[0]
     keys = np.empty(idx_k.shape, dtype=np.float64)
-    scale = None if idx_dtype == "f32" else np.empty(idx_k.shape[:2], dtype=np.float64)
+    scale = np.empty(idx_k.shape[:2], dtype=np.float64) if idx_dtype == "fp8" else None
     for t0 in range(0, L, _CHUNK):
         x = to_f32(idx_k[t0:t0 + _CHUNK])
         if idx_dtype == "f32":
             keys[t0:t0 + _CHUNK] = x
+        elif idx_dtype == "nvfp4":
+            codes, sc = quant.quant_nvfp4(x, idx_global)
+            keys[t0:t0 + _CHUNK] = formats.nvfp4_decode(codes, sc, idx_global)
         else:
             codes, s = quant.quant_index_keys_fp8(x)
             keys[t0:t0 + _CHUNK] = formats.e4m3_decode(codes)
@@ -69,7 +76,8 @@ class _Rows:
 
 
 def run_request(req: dict, seq_len: int, topk: int, softmax_scale: float, block_size: int, idx_dtype: str,
-                kv_dtype: str, k_global: float = 1.0, v_global: float = 1.0, sel=None, heads=None):
+                kv_dtype: str, k_global: float = 1.0, v_global: float = 1.0, sel=None, heads=None,
+                idx_global: float = 1.0):
     """All three stages for one request.
 
     ``sel`` ([Q, G, topk]) replaces the oracle's own selection in the attention
@@ -77,7 +85,7 @@ def run_request(req: dict, seq_len: int, topk: int, softmax_scale: float, block_
     restricts the attention stage to some query heads (others are NaN).
     Returns dict(S, sel, margin, out, lse, sel_used).
     """
-    keys, kscale = cached_index_keys(req["idx_k"], idx_dtype)
+    keys, kscale = cached_index_keys(req["idx_k"], idx_dtype, idx_global)
     qi = to_f32(req["q_idx"]).astype(np.float64)
     S = msa.index_scores(qi, keys, kscale, seq_len, block_size)
     del keys

@@ -3,8 +3,9 @@
 Tolerances (written here once, used by every GPU test):
   * Block scores: |gpu - oracle| <= SCORE_REL * A, with A = max over the block's
     tokens of s_t * sum_d |q_d k_td|. Each product of a bf16 query and an E4M3
-    key is exact in fp32 and the kernel sums 128 of them in fp32 before one
-    multiply by s_t, so the error is below (128 + 2) * 2^-24 * A ~ 7.8e-6 * A.
+    (or E2M1 x E4M3) key is exact in fp32 and the kernel sums 128 of them in
+    fp32 before one multiply by s_t (or the global scale), so the error is
+    below (128 + 2) * 2^-24 * A ~ 7.8e-6 * A.
   * Selections: bit-exact, except that where the oracle's last chosen and first
     unchosen competing scores differ by less than NEAR_TIE relative, the GPU may
     swap blocks that lie inside that band.
@@ -32,9 +33,13 @@ def build(w, which=None, lens=None):
     return DeviceWorkload(w, "cuda", which=which, lens=lens)
 
 
+def idx_global(w):
+    return float(np.float32(synth.NVFP4_IDX_SYNTH_GLOBAL)) if w.idx_dtype == "nvfp4" else 1.0
+
+
 def score_bound(req, w, L):
     """A[j, g, n] = max_t s_t * sum_d |q_jgd k_tgd| over the block's tokens."""
-    keys, scale = orun.cached_index_keys(req["idx_k"], w.idx_dtype)
+    keys, scale = orun.cached_index_keys(req["idx_k"], w.idx_dtype, idx_global(w))
     qi = np.abs(orun.to_f32(req["q_idx"]).astype(np.float64))
     BS = w.block_size
     nb = (L + BS - 1) // BS
@@ -123,7 +128,7 @@ def verify_workload(dw, w, full_lens, sample=None, heads=None, run_step=True):
         L = int(full_lens[b])
         req = synth.request(w, b, L)
         ora = orun.run_request(req, L, w.topk, w.softmax_scale, w.block_size, w.idx_dtype, w.kv_dtype, kg, vg,
-                               sel=sel[bi], heads=heads)
+                               sel=sel[bi], heads=heads, idx_global=idx_global(w))
         nb = ora["S"].shape[2]
         where = f"{w.name} b={b} L={L}"
         check_scores(S[bi, :, :, :nb], ora["S"], score_bound(req, w, L), where)

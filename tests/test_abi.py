@@ -29,7 +29,7 @@ def test_every_declared_function_is_exported(m):
 
 
 def test_version_and_status_strings(m):
-    assert m.lib.msa_abi_version() == 1
+    assert m.lib.msa_abi_version() == 2
     assert m.status_string(m.OK) == "MSA_OK"
     assert m.status_string(m.ERR_WORKSPACE) == "MSA_ERR_WORKSPACE"
     assert m.status_string(99) == "MSA_ERR_UNKNOWN"
@@ -76,9 +76,15 @@ def test_dtype_combinations_rejected(m):
     ic = m._IndexCache(m.FP8_E4M3, fake, fake)
     st = m.lib.msa_index_score(ctypes.byref(d), fake, m.F32, ctypes.byref(ic), fake, fake, fake, fake, None)
     assert st == m.ERR_UNSUPPORTED
-    ic = m._IndexCache(m.NVFP4, fake, None)
+    ic = m._IndexCache(m.BF16, fake, None, None, 1.0)                # no bf16 index cache
     st = m.lib.msa_index_score(ctypes.byref(d), fake, m.BF16, ctypes.byref(ic), fake, fake, fake, fake, None)
     assert st == m.ERR_UNSUPPORTED
+    ic = m._IndexCache(m.NVFP4, fake, None, None, 1.0)               # NVFP4 keys need their block scales
+    st = m.lib.msa_index_score(ctypes.byref(d), fake, m.BF16, ctypes.byref(ic), fake, fake, fake, fake, None)
+    assert st == m.ERR_INVALID_ARG
+    ic = m._IndexCache(m.NVFP4, fake, None, fake, 0.0)               # and a positive global scale
+    st = m.lib.msa_index_score(ctypes.byref(d), fake, m.BF16, ctypes.byref(ic), fake, fake, fake, fake, None)
+    assert st == m.ERR_INVALID_ARG
     kv = m._KVCache(m.NVFP4, fake, fake, fake, fake, 0.0, 1.0)      # global scale must be > 0
     st = m.lib.msa_kv_insert_quant(ctypes.byref(d), fake, fake, None, m.F32, fake, 4, ctypes.byref(kv), None,
                                    fake, None)

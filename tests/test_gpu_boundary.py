@@ -82,6 +82,10 @@ def test_dispatch_record_names_the_variant():
     dw4 = parity.build(w4)
     dw4.step()
     assert "sparse_gqa nvfp4_dequant_f16_mma" in msa.last_dispatch()
+    w5 = synth.scaled(synth.WORKLOADS["b32_32k_fp4idx"], batch=1, ctx=700)
+    dw5 = parity.build(w5)
+    dw5.index_score()
+    assert "index_score nvfp4_mma_f16" in msa.last_dispatch()
     wt = synth.scaled(synth.WORKLOADS["tiny"], batch=1, ctx=700)
     dwt = parity.build(wt)
     dwt.index_score()

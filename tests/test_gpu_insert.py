@@ -28,6 +28,9 @@ def _insert(k, v, idx, idx_dtype, kv_dtype, g=1.0, P=4, G=4):
     if idx_dtype == "fp8":
         ic = msa.IndexCache(msa.FP8_E4M3, torch.zeros((P, G, 128, 128), dtype=torch.uint8, device="cuda"),
                             torch.zeros((P, G, 128), dtype=torch.float32, device="cuda"))
+    elif idx_dtype == "nvfp4":
+        ic = msa.IndexCache(msa.NVFP4, torch.zeros((P, G, 128, 64), dtype=torch.uint8, device="cuda"), None,
+                            torch.zeros((P, G, 128, 8), dtype=torch.uint8, device="cuda"), g)
     else:
         ic = msa.IndexCache(msa.F32, torch.zeros((P, G, 128, 128), dtype=torch.float32, device="cuda"))
     slots = torch.arange(T, dtype=torch.int64, device="cuda")
@@ -40,6 +43,8 @@ def _insert(k, v, idx, idx_dtype, kv_dtype, g=1.0, P=4, G=4):
     # token t lives at page t // 128, offset t % 128: [P, G, BS, ...] -> [T, G, ...]
     tok = lambda a: a.cpu().numpy().transpose(0, 2, 1, *range(3, a.dim())).reshape(P * 128, G, *a.shape[3:])[:T]
     out = {"idx_keys": tok(ic.keys)}
+    if ic.block_scale is not None:
+        out["idx_block_scale"] = tok(ic.block_scale)
     if ic.scale is not None:
         out["idx_scale"] = ic.scale.cpu().numpy().transpose(0, 2, 1).reshape(P * 128, G)[:T]
     if kv_dtype == "bf16":
@@ -132,3 +137,20 @@ def test_negative_slots_skip_and_bad_slots_flag():
     assert msa.read_device_flags(flags) == msa.FLAG_BAD_SLOT
     c = cache.k.float().cpu()
     assert c[0, :, 5].eq(1).all() and c.sum().item() == 4 * 128
+
+
+@pytest.mark.parametrize("src", ["f32", "bf16"])
+def test_nvfp4_index_keys_bit_exact(src):
+    rng = np.random.default_rng(6)
+    T, G = 280, 4
+    x = (rng.standard_normal((T, G, 128)) * rng.uniform(0.1, 3, (T, G, 1))).astype(np.float32)
+    x[0, 0, :16] = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0, -0.25, -0.75, -1.25, -1.75, -2.5, -3.5, -5.0, -6.0]
+    x[1, 1, :] = 0.0
+    g = float(np.float32(8.0 / (6 * 448)))
+    k = rng.standard_normal((T, G, 128)).astype(np.float32)
+    idx = x if src == "f32" else synth.f32_to_bf16_bits(x)
+    xv = x if src == "f32" else synth.bf16_bits_to_f32(idx)
+    got = _insert(k, k, idx, "nvfp4", "bf16", g=g)
+    codes, scales = Qz.quant_nvfp4(xv, g)
+    assert np.array_equal(got["idx_block_scale"], scales)
+    assert np.array_equal(got["idx_keys"], codes)

@@ -21,6 +21,8 @@ REDUCED = {
     "ragged": synth.scaled(W["ragged"], batch=5, ctx_range=(300, 5000)),
     "spec8": synth.scaled(W["spec8"], batch=3, ctx=3000),
     "nvfp4_256k": synth.scaled(W["nvfp4_256k"], batch=2, ctx=3000),
+    "b32_32k_fp4idx": synth.scaled(W["b32_32k_fp4idx"], batch=3, ctx=2300),
+    "fp4_256k": synth.scaled(W["fp4_256k"], batch=2, ctx=2900),
 }
 
 
@@ -38,6 +40,7 @@ EDGE_LENS = {
     "spec_straddle": ("spec8", [8, 9, 130, 135, 136, 1028, 2948, 2951, 2952]),
     "nvfp4_edges": ("nvfp4_256k", [1, 128, 129, 1500, 2049]),
     "tiny_f32_edges": ("tiny", [1, 200, 4095]),
+    "fp4idx_edges": ("b32_32k_fp4idx", [1, 129, 257, 2100]),
 }
 
 

@@ -236,3 +236,21 @@ def test_selection_edge_cases():
     s = np.array([4.0, 1.0, 2.0, 3.0])
     sel, m = M.select_row(s, 4, 3)
     assert sel.tolist() == [0, 3, 4] and m == pytest.approx((3.0 - 2.0) / 3.0)
+
+
+def test_nvfp4_index_keys_exact_when_representable():
+    """Keys whose 16-groups have amax 6 and E2M1 values quantise exactly (global 1):
+    the scores equal the exact dot-product maxima."""
+    from oracle import run as orun
+    rng = np.random.default_rng(19)
+    vals = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    L, I, D, BS = 600, 2, 128, 128
+    keys = rng.choice(vals, (L, I, D)) * rng.choice([-1, 1], (L, I, D))
+    keys.reshape(L, I, D // 16, 16)[..., 0] = 6.0                 # amax 6 in every group -> block scale 1
+    dec, scale = orun.cached_index_keys(keys.astype(np.float32), "nvfp4", 1.0)
+    assert scale is None and np.array_equal(dec, keys)
+    qi = rng.standard_normal((1, I, D))
+    S = M.index_scores(qi, dec, None, L, BS)
+    ell = (L - 1) // BS
+    want = np.einsum("id,tid->it", qi[0], keys[: ell * BS]).reshape(I, ell, BS).max(-1)
+    np.testing.assert_allclose(S[0, :, :ell], want, rtol=1e-13)
