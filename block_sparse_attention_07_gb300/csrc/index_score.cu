@@ -12,13 +12,16 @@
 // A producer thread streams each unit's page (I heads x 128 tokens x 128 B of
 // E4M3 keys, contiguous, plus I x 512 B of per-token scales) into a ring of
 // shared-memory stages with bulk copies completed on mbarriers. One consumer
-// warp per index head turns 16 tokens x 16 dims of keys into an fp16 mma A
+// warp pair per index head (each warp takes half of the page's 128 tokens)
+// turns 16 tokens x 16 dims of keys into an fp16 mma A
 // fragment (cvt e4m3x2 -> f16x2 is exact), multiplies by the Q positions'
 // index queries (the 8 columns of m16n8k16; fp16 after an exact power-of-two
 // rescale of each query row), applies the per-token scale and keeps the running
 // max. The dims a thread feeds to the mma are a fixed permutation of 0..127,
 // applied identically to keys and queries, so each thread reads whole 16-byte
-// runs of a key row.
+// runs of a key row. The two warps of a pair merge their column maxima through
+// a shared-memory slot per stage: the second to arrive (a parity ticket) writes
+// the score, so neither waits for the other.
 #include "msa_internal.h"
 
 namespace msa {
@@ -26,6 +29,8 @@ namespace msa {
 constexpr int kIdxStages = 3;       // 66.5 KB pages (FP8 keys, 4 heads)
 constexpr int kIdxStagesFp4 = 5;    // 36 KB pages (NVFP4 keys, 4 heads)
 constexpr int kMaxIdxHeads = 4;
+constexpr int kWarpsPerHead = 2;    // consumer warps per index head (token halves of a page)
+constexpr int kTilesPerWarp = kBlock / 16 / kWarpsPerHead;
 constexpr uint32_t kFull = 0xffffffffu;
 
 struct IdxParams {
@@ -103,8 +108,13 @@ __host__ __device__ constexpr uint32_t scale_bytes_per_head() { return kFp4Keys 
 
 // kFp4Keys = false: E4M3 keys + fp32 per-token scale. true: NVFP4 keys (E2M1
 // pairs, E4M3 scale per 16 values, fp32 global scale).
-template <int kStages, bool kFp4Keys>
-__global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_kernel(IdxParams p) {
+// kGroupCols (NVFP4 keys, one query position): the 8 mma columns are the 8
+// scale groups of the key row instead of query positions. Column n of the B
+// operand holds the query's dims of group n and zeros elsewhere, so the
+// accumulator is the per-group partial dot product q . code, and the block
+// scales multiply those fp32 partials rather than every decoded key value.
+template <int kStages, bool kFp4Keys, bool kGroupCols>
+__global__ void __launch_bounds__(32 * (1 + kWarpsPerHead * kMaxIdxHeads), 1) index_score_fp8_kernel(IdxParams p) {
   extern __shared__ __align__(1024) uint8_t smem_fp8[];
   uint8_t* smem = smem_fp8;
   const int I = p.I;
@@ -114,7 +124,9 @@ __global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_ke
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * stage_bytes);
   uint64_t* empty = full + kStages;
   int* valid = reinterpret_cast<int*>(empty + kStages);
-  int* pref = valid + kStages;
+  float* part = reinterpret_cast<float*>(valid + kStages);          // [stage][head][warp of pair][8 columns]
+  uint32_t* ticket = reinterpret_cast<uint32_t*>(part + kStages * kMaxIdxHeads * kWarpsPerHead * 8);
+  int* pref = reinterpret_cast<int*>(ticket + kStages * kMaxIdxHeads);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_launch_dependents();
@@ -123,10 +135,11 @@ __global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_ke
   if (threadIdx.x == 32) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_addr(&full[s]), 1);
-      mbar_init(smem_addr(&empty[s]), I);
+      mbar_init(smem_addr(&empty[s]), kWarpsPerHead * I);
     }
     fence_mbar_init();
   }
+  for (int x = threadIdx.x; x < kStages * kMaxIdxHeads; x += blockDim.x) ticket[x] = 0u;
   __syncthreads();
   fill_tails(p, pref);
 
@@ -191,7 +204,8 @@ __global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_ke
   }
 
   // ------------------------------------------------------------ consumers --
-  const int g = warp - 1;
+  const int g = (warp - 1) / kWarpsPerHead, half = (warp - 1) % kWarpsPerHead;
+  const int t0 = half * kTilesPerWarp;
   const int gr = lane >> 2, c = lane & 3;
   const uint16_t* qbase = static_cast<const uint16_t*>(p.q);
   uint32_t qb[8][2];
@@ -207,10 +221,10 @@ __global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_ke
       const int L = p.seq_lens[b];
       // Index-query fragment of position gr for this request and head.
       float qv[32];
-      if (gr < p.Q) {
+      if (kGroupCols || gr < p.Q) {
         // dims this thread feeds to the mma: FP8 keys 16c..16c+15 and 64+16c..64+16c+15
         // (two 16-byte runs of a key row), NVFP4 keys 32c..32c+31 (one 16-byte run)
-        const uint16_t* qp = qbase + ((static_cast<int64_t>(b) * p.Q + gr) * I + g) * kDim;
+        const uint16_t* qp = qbase + ((static_cast<int64_t>(b) * p.Q + (kGroupCols ? 0 : gr)) * I + g) * kDim;
         const int o0 = kFp4Keys ? 32 * c : 16 * c, o1 = kFp4Keys ? 32 * c + 16 : 64 + 16 * c;
         const uint4 a0 = *reinterpret_cast<const uint4*>(qp + o0);
         const uint4 a1 = *reinterpret_cast<const uint4*>(qp + o0 + 8);
@@ -234,14 +248,20 @@ __global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_ke
       amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
       const int sh = fp16_shift_for(amax);
       const float f = exp2_int(sh);
-      const float inv = gr < p.Q ? exp2_int(-sh) * (kFp4Keys ? p.global_scale : 1.f) : 0.f;
+      const float inv = (kGroupCols || gr < p.Q) ? exp2_int(-sh) * (kFp4Keys ? p.global_scale : 1.f) : 0.f;
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        qb[s][0] = pack_f16x2(qv[4 * s] * f, qv[4 * s + 1] * f);
-        qb[s][1] = pack_f16x2(qv[4 * s + 2] * f, qv[4 * s + 3] * f);
+        // k-step s covers this thread's dims 32c+4s..32c+4s+3 (group 2c + s/4)
+        const bool live = !kGroupCols || gr == 2 * c + (s >> 2);
+        qb[s][0] = live ? pack_f16x2(qv[4 * s] * f, qv[4 * s + 1] * f) : 0u;
+        qb[s][1] = live ? pack_f16x2(qv[4 * s + 2] * f, qv[4 * s + 3] * f) : 0u;
       }
-      inv_col0 = __shfl_sync(kFull, inv, 8 * c);
-      inv_col1 = __shfl_sync(kFull, inv, 8 * c + 4);
+      if (kGroupCols) {
+        inv_col0 = inv_col1 = inv;
+      } else {
+        inv_col0 = __shfl_sync(kFull, inv, 8 * c);
+        inv_col1 = __shfl_sync(kFull, inv, 8 * c + 4);
+      }
       ell_col0 = (L - p.Q + 2 * c) / kBlock;
       ell_col1 = (L - p.Q + 2 * c + 1) / kBlock;
       cur_b = b;
@@ -257,7 +277,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_ke
       const uint8_t* kb = smem + s * stage_bytes + g * (kBlock * kDim);
       const float* sc = reinterpret_cast<const float*>(smem + s * stage_bytes + key_bytes) + g * kBlock;
 #pragma unroll 2
-      for (int t = 0; t < 8; ++t) {
+      for (int t = t0; t < t0 + kTilesPerWarp; ++t) {
         const uint8_t* r0 = kb + (16 * t + gr) * kDim + 16 * c;
         const uint4 x0 = *reinterpret_cast<const uint4*>(r0);
         const uint4 x1 = *reinterpret_cast<const uint4*>(r0 + 64);
@@ -278,13 +298,49 @@ __global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_ke
         m0 = fmaxf(m0, fmaxf(acc[0] * s0, acc[2] * s1));
         m1 = fmaxf(m1, fmaxf(acc[1] * s0, acc[3] * s1));
       }
+    } else if (valid[s] && kGroupCols) {
+      // NVFP4 keys, one position: acc[0..1] = row r0's partials of groups 2c,
+      // 2c+1, acc[2..3] the same for row r1; scaled, summed over the 4 threads
+      // of the row, then maxed.
+      const uint8_t* kb = smem + s * stage_bytes + g * (kBlock * kDim / 2);
+      const uint8_t* sb = smem + s * stage_bytes + key_bytes + g * (kBlock * kDim / 16);
+#pragma unroll 2
+      for (int t = t0; t < t0 + kTilesPerWarp; ++t) {
+        const int r0 = 16 * t + gr, r1 = r0 + 8;
+        const uint4 x = *reinterpret_cast<const uint4*>(kb + r0 * (kDim / 2) + 16 * c);
+        const uint4 y = *reinterpret_cast<const uint4*>(kb + r1 * (kDim / 2) + 16 * c);
+        const uint32_t sx = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sb + r0 * (kDim / 16) + 2 * c));
+        const uint32_t sy = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sb + r1 * (kDim / 16) + 2 * c));
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+        const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t hx[4], hy[4];
+          e2m1x8_to_f16x2x4(xw[j], hx);
+          e2m1x8_to_f16x2x4(yw[j], hy);
+          const uint32_t a0[4] = {hx[0], hy[0], hx[1], hy[1]};
+          const uint32_t a1[4] = {hx[2], hy[2], hx[3], hy[3]};
+          mma_f16(acc, a0, qb[2 * j][0], qb[2 * j][1]);
+          mma_f16(acc, a1, qb[2 * j + 1][0], qb[2 * j + 1][1]);
+        }
+        const __half2 hsx = *reinterpret_cast<const __half2*>(&sx);
+        const __half2 hsy = *reinterpret_cast<const __half2*>(&sy);
+        float v0 = acc[0] * __low2float(hsx) + acc[1] * __high2float(hsx);
+        float v1 = acc[2] * __low2float(hsy) + acc[3] * __high2float(hsy);
+        v0 += __shfl_xor_sync(kFull, v0, 1);
+        v1 += __shfl_xor_sync(kFull, v1, 1);
+        v0 += __shfl_xor_sync(kFull, v0, 2);
+        v1 += __shfl_xor_sync(kFull, v1, 2);
+        m0 = fmaxf(m0, fmaxf(v0, v1));
+      }
     } else if (valid[s]) {
       // NVFP4 keys: 64 B of E2M1 pairs per token row, 8 E4M3 scales; e2m1 x e4m3
       // is exact in fp16, so the fragment is the decoded key up to the global scale.
       const uint8_t* kb = smem + s * stage_bytes + g * (kBlock * kDim / 2);
       const uint8_t* sb = smem + s * stage_bytes + key_bytes + g * (kBlock * kDim / 16);
 #pragma unroll 2
-      for (int t = 0; t < 8; ++t) {
+      for (int t = t0; t < t0 + kTilesPerWarp; ++t) {
         const int r0 = 16 * t + gr, r1 = r0 + 8;
         const uint4 x = *reinterpret_cast<const uint4*>(kb + r0 * (kDim / 2) + 16 * c);
         const uint4 y = *reinterpret_cast<const uint4*>(kb + r1 * (kDim / 2) + 16 * c);
@@ -315,14 +371,40 @@ __global__ void __launch_bounds__(32 * (1 + kMaxIdxHeads), 1) index_score_fp8_ke
         m1 = fmaxf(m1, fmaxf(acc[1], acc[3]));
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       m0 = fmaxf(m0, __shfl_xor_sync(kFull, m0, o));
       m1 = fmaxf(m1, __shfl_xor_sync(kFull, m1, o));
     }
-    if (gr == 0) {
+    // Merge with the other warp of the pair. Each writes its maxima to the slot
+    // of (stage, head), then takes a ticket; the second ticket holder reads the
+    // other half and writes the score. The slot is reused only after every warp
+    // has released the stage, which each does after its last read of the slot.
+    bool writer = true;
+    if constexpr (kWarpsPerHead == 2) {
+      float* slot = part + (s * kMaxIdxHeads + g) * (kWarpsPerHead * 8);
+      if (gr == 0) {
+        slot[half * 8 + 2 * c] = m0;
+        slot[half * 8 + 2 * c + 1] = m1;
+      }
+      __syncwarp();
+      uint32_t tk = 0;
+      if (lane == 0) {
+        __threadfence_block();
+        tk = atomicAdd(&ticket[s * kMaxIdxHeads + g], 1u);
+        __threadfence_block();
+      }
+      writer = (__shfl_sync(kFull, tk, 0) & 1u) != 0u;
+      __syncwarp();
+      if (writer && gr == 0) {
+        const volatile float* other = slot + (half ^ 1) * 8;
+        m0 = fmaxf(m0, other[2 * c]);
+        m1 = fmaxf(m1, other[2 * c + 1]);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+    if (writer && gr == 0) {
       const int64_t base = (static_cast<int64_t>(b) * p.Q) * I + g;
       const int j0 = 2 * c, j1 = 2 * c + 1;
       if (j0 < p.Q) p.scores[(base + static_cast<int64_t>(j0) * I) * p.NB + n] = n < ell_col0 ? m0 * inv_col0 : -INFINITY;
@@ -412,15 +494,20 @@ cudaError_t launch_index_score(const IndexArgs& a, cudaStream_t stream, Dispatch
     const int stages = a.fp4 ? kIdxStagesFp4 : kIdxStages;
     const size_t stage = a.fp4 ? static_cast<size_t>(a.I) * (key_bytes_per_head<true>() + scale_bytes_per_head<true>())
                                : static_cast<size_t>(a.I) * (key_bytes_per_head<false>() + scale_bytes_per_head<false>());
-    const size_t smem = stages * stage + 2 * stages * 8 + stages * 4 + (a.B + 1) * 4;
-    auto kern = a.fp4 ? index_score_fp8_kernel<kIdxStagesFp4, true> : index_score_fp8_kernel<kIdxStages, false>;
+    const size_t smem = stages * stage + 2 * stages * 8 + stages * 4 +
+                        stages * kMaxIdxHeads * (kWarpsPerHead * 8 * 4 + 4) + (a.B + 1) * 4;
+    auto kern = !a.fp4 ? index_score_fp8_kernel<kIdxStages, false, false>
+                : a.Q == 1 ? index_score_fp8_kernel<kIdxStagesFp4, true, true>
+                           : index_score_fp8_kernel<kIdxStagesFp4, true, false>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     const int grid = sms;
-    err = launch_pdl(kern, dim3(grid), dim3(32 * (1 + a.I)), smem, stream, p);
+    const int block = 32 * (1 + kWarpsPerHead * a.I);
+    err = launch_pdl(kern, dim3(grid), dim3(block), smem, stream, p);
     if (err != cudaSuccess) return err;
     rec->set("index_score %s grid=%d block=%d smem=%zu stages=%d q_len=%d idx_heads=%d",
-             a.fp4 ? "nvfp4_mma_f16" : "fp8_mma_f16", grid, 32 * (1 + a.I), smem, stages, a.Q, a.I);
+             !a.fp4 ? "fp8_mma_f16" : a.Q == 1 ? "nvfp4_group_cols_mma_f16" : "nvfp4_mma_f16", grid, block, smem,
+             stages, a.Q, a.I);
   } else {
     const size_t smem = ((static_cast<size_t>(a.B) + 1) * 4 + 15) / 16 * 16 + 4 * 8 * kDim * 4;
     err = cudaFuncSetAttribute(index_score_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -167,6 +167,18 @@ __device__ __forceinline__ void e2m1x4_to_f16x2x2(uint16_t v, uint32_t& lo, uint
       : "h"(v));
 }
 
+// Eight E2M1 codes in 32 bits -> four f16x2 words; word i holds the two codes of byte i. Exact.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t v, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(v));
+}
+
 // fp32 pair -> two E4M3 codes, round to nearest even, saturating (element 0 in the low byte).
 __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float e0, float e1) {
   uint16_t r;

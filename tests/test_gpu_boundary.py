@@ -85,6 +85,10 @@ def test_dispatch_record_names_the_variant():
     w5 = synth.scaled(synth.WORKLOADS["b32_32k_fp4idx"], batch=1, ctx=700)
     dw5 = parity.build(w5)
     dw5.index_score()
+    assert "index_score nvfp4_group_cols_mma_f16" in msa.last_dispatch()
+    w6 = synth.scaled(synth.WORKLOADS["spec8"], batch=1, ctx=700, idx_dtype="nvfp4")
+    dw6 = parity.build(w6)
+    dw6.index_score()
     assert "index_score nvfp4_mma_f16" in msa.last_dispatch()
     wt = synth.scaled(synth.WORKLOADS["tiny"], batch=1, ctx=700)
     dwt = parity.build(wt)

@@ -23,6 +23,9 @@ REDUCED = {
     "nvfp4_256k": synth.scaled(W["nvfp4_256k"], batch=2, ctx=3000),
     "b32_32k_fp4idx": synth.scaled(W["b32_32k_fp4idx"], batch=3, ctx=2300),
     "fp4_256k": synth.scaled(W["fp4_256k"], batch=2, ctx=2900),
+    # NVFP4 index keys with 8 query positions (the per-value block-scale path;
+    # one position takes the per-group path)
+    "spec8_fp4idx": synth.scaled(W["spec8"], batch=3, ctx=3000, idx_dtype="nvfp4"),
 }
 
 
@@ -41,13 +44,14 @@ EDGE_LENS = {
     "nvfp4_edges": ("nvfp4_256k", [1, 128, 129, 1500, 2049]),
     "tiny_f32_edges": ("tiny", [1, 200, 4095]),
     "fp4idx_edges": ("b32_32k_fp4idx", [1, 129, 257, 2100]),
+    "spec_fp4idx_edges": ("spec8", [8, 9, 136, 1028, 2951], {"idx_dtype": "nvfp4"}),
 }
 
 
 @pytest.mark.parametrize("case", list(EDGE_LENS))
 def test_edge_lengths(case):
-    base, lens = EDGE_LENS[case]
-    w = synth.scaled(W[base], batch=len(lens), ctx=None, ctx_range=None)
+    base, lens, *more = EDGE_LENS[case]
+    w = synth.scaled(W[base], batch=len(lens), ctx=None, ctx_range=None, **(more[0] if more else {}))
     lens = np.array(lens, dtype=np.int32)
     dw = parity.build(w, lens=lens)
     parity.verify_workload(dw, w, lens)
