@@ -7,30 +7,33 @@
 // is loaded once for all query positions of its request, and no positive
 // score scale is applied.
 //
-// FP8 path (the hot one): a persistent kernel, one CTA per SM. Work units are
+// FP8 / NVFP4 paths: a persistent kernel, one CTA per SM (two for NVFP4 keys,
+// whose pages are half the size). Work units are
 // the (request, block) pairs that some position of the request can select.
 // A producer thread streams each unit's page (I heads x 128 tokens x 128 B of
 // E4M3 keys, contiguous, plus I x 512 B of per-token scales) into a ring of
 // shared-memory stages with bulk copies completed on mbarriers. One consumer
-// warp pair per index head (each warp takes half of the page's 128 tokens)
+// warp group per index head (each warp takes a share of the page's 128 tokens)
 // turns 16 tokens x 16 dims of keys into an fp16 mma A
 // fragment (cvt e4m3x2 -> f16x2 is exact), multiplies by the Q positions'
 // index queries (the 8 columns of m16n8k16; fp16 after an exact power-of-two
 // rescale of each query row), applies the per-token scale and keeps the running
 // max. The dims a thread feeds to the mma are a fixed permutation of 0..127,
 // applied identically to keys and queries, so each thread reads whole 16-byte
-// runs of a key row. The two warps of a pair merge their column maxima through
-// a shared-memory slot per stage: the second to arrive (a parity ticket) writes
-// the score, so neither waits for the other.
+// runs of a key row. The warps of a head merge their column maxima through a
+// shared-memory slot per stage: the last to arrive (by a ticket counter) writes
+// the score, so none waits for another.
 #include "msa_internal.h"
 
 namespace msa {
 
-constexpr int kIdxStages = 3;       // 66.5 KB pages (FP8 keys, 4 heads)
-constexpr int kIdxStagesFp4 = 5;    // 36 KB pages (NVFP4 keys, 4 heads)
+constexpr int kIdxStages = 3;       // 66.5 KB pages (FP8 keys, 4 heads), one CTA per SM
+constexpr int kIdxStagesFp4 = 3;    // 36 KB pages (NVFP4 keys, 4 heads), two CTAs per SM
+constexpr int kFp4CtasPerSm = 2;    // two independent pipelines per SM hide more of the per-page latency
 constexpr int kMaxIdxHeads = 4;
-constexpr int kWarpsPerHead = 2;    // consumer warps per index head (token halves of a page)
+constexpr int kWarpsPerHead = 2;    // consumer warps per index head (each takes a share of the page's tokens)
 constexpr int kTilesPerWarp = kBlock / 16 / kWarpsPerHead;
+constexpr int kIdxThreads = 32 * (1 + kWarpsPerHead * kMaxIdxHeads);
 constexpr uint32_t kFull = 0xffffffffu;
 
 struct IdxParams {
@@ -114,7 +117,7 @@ __host__ __device__ constexpr uint32_t scale_bytes_per_head() { return kFp4Keys 
 // accumulator is the per-group partial dot product q . code, and the block
 // scales multiply those fp32 partials rather than every decoded key value.
 template <int kStages, bool kFp4Keys, bool kGroupCols>
-__global__ void __launch_bounds__(32 * (1 + kWarpsPerHead * kMaxIdxHeads), 1) index_score_fp8_kernel(IdxParams p) {
+__global__ void __launch_bounds__(kIdxThreads, kFp4Keys ? kFp4CtasPerSm : 1) index_score_fp8_kernel(IdxParams p) {
   extern __shared__ __align__(1024) uint8_t smem_fp8[];
   uint8_t* smem = smem_fp8;
   const int I = p.I;
@@ -204,8 +207,8 @@ __global__ void __launch_bounds__(32 * (1 + kWarpsPerHead * kMaxIdxHeads), 1) in
   }
 
   // ------------------------------------------------------------ consumers --
-  const int g = (warp - 1) / kWarpsPerHead, half = (warp - 1) % kWarpsPerHead;
-  const int t0 = half * kTilesPerWarp;
+  const int g = (warp - 1) / kWarpsPerHead, slice = (warp - 1) % kWarpsPerHead;
+  const int t0 = slice * kTilesPerWarp;
   const int gr = lane >> 2, c = lane & 3;
   const uint16_t* qbase = static_cast<const uint16_t*>(p.q);
   uint32_t qb[8][2];
@@ -304,7 +307,7 @@ __global__ void __launch_bounds__(32 * (1 + kWarpsPerHead * kMaxIdxHeads), 1) in
       // of the row, then maxed.
       const uint8_t* kb = smem + s * stage_bytes + g * (kBlock * kDim / 2);
       const uint8_t* sb = smem + s * stage_bytes + key_bytes + g * (kBlock * kDim / 16);
-#pragma unroll 2
+#pragma unroll
       for (int t = t0; t < t0 + kTilesPerWarp; ++t) {
         const int r0 = 16 * t + gr, r1 = r0 + 8;
         const uint4 x = *reinterpret_cast<const uint4*>(kb + r0 * (kDim / 2) + 16 * c);
@@ -376,16 +379,17 @@ __global__ void __launch_bounds__(32 * (1 + kWarpsPerHead * kMaxIdxHeads), 1) in
       m0 = fmaxf(m0, __shfl_xor_sync(kFull, m0, o));
       m1 = fmaxf(m1, __shfl_xor_sync(kFull, m1, o));
     }
-    // Merge with the other warp of the pair. Each writes its maxima to the slot
-    // of (stage, head), then takes a ticket; the second ticket holder reads the
-    // other half and writes the score. The slot is reused only after every warp
-    // has released the stage, which each does after its last read of the slot.
+    // Merge with the other warps of the head. Each writes its maxima to the
+    // slot of (stage, head), then takes a ticket; the last ticket holder of the
+    // unit (every unit takes exactly kWarpsPerHead tickets) reads the other
+    // parts and writes the score. The slot is reused only after every warp has
+    // released the stage, which each does after its last read of the slot.
     bool writer = true;
-    if constexpr (kWarpsPerHead == 2) {
+    if constexpr (kWarpsPerHead > 1) {
       float* slot = part + (s * kMaxIdxHeads + g) * (kWarpsPerHead * 8);
       if (gr == 0) {
-        slot[half * 8 + 2 * c] = m0;
-        slot[half * 8 + 2 * c + 1] = m1;
+        slot[slice * 8 + 2 * c] = m0;
+        slot[slice * 8 + 2 * c + 1] = m1;
       }
       __syncwarp();
       uint32_t tk = 0;
@@ -394,12 +398,16 @@ __global__ void __launch_bounds__(32 * (1 + kWarpsPerHead * kMaxIdxHeads), 1) in
         tk = atomicAdd(&ticket[s * kMaxIdxHeads + g], 1u);
         __threadfence_block();
       }
-      writer = (__shfl_sync(kFull, tk, 0) & 1u) != 0u;
+      writer = __shfl_sync(kFull, tk, 0) % kWarpsPerHead == kWarpsPerHead - 1;
       __syncwarp();
       if (writer && gr == 0) {
-        const volatile float* other = slot + (half ^ 1) * 8;
-        m0 = fmaxf(m0, other[2 * c]);
-        m1 = fmaxf(m1, other[2 * c + 1]);
+        const volatile float* other = slot;
+#pragma unroll
+        for (int h = 0; h < kWarpsPerHead; ++h) {
+          if (h == slice) continue;
+          m0 = fmaxf(m0, other[h * 8 + 2 * c]);
+          m1 = fmaxf(m1, other[h * 8 + 2 * c + 1]);
+        }
       }
       __syncwarp();
     }
@@ -501,7 +509,7 @@ cudaError_t launch_index_score(const IndexArgs& a, cudaStream_t stream, Dispatch
                            : index_score_fp8_kernel<kIdxStagesFp4, true, false>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    const int grid = sms;
+    const int grid = a.fp4 ? kFp4CtasPerSm * sms : sms;
     const int block = 32 * (1 + kWarpsPerHead * a.I);
     err = launch_pdl(kern, dim3(grid), dim3(block), smem, stream, p);
     if (err != cudaSuccess) return err;

@@ -36,6 +36,7 @@ constexpr int kTileBytes = 4 * kBoxBytes;        // K lo/hi + V lo/hi = 64 KB
 constexpr int kFp4StageBytes = 2 * (kBlock * kDim / 2 + kBlock * kDim / 16);  // 18 KB
 constexpr uint32_t kAll = 0xffffffffu;
 constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kRescaleSlack = 8.f;    // log2 units: probabilities below 256 before normalisation
 
 struct GqaParams {
   const uint16_t* q;
@@ -87,26 +88,30 @@ struct RowPos {
 };
 
 // (request, KV head, position) of enumeration row r; positions are adjacent.
-__device__ __forceinline__ RowPos row_pos(const GqaParams& p, int64_t r) {
+// Rows and items fit in 32 bits (at most 4096 x 8 x 4 rows of 16 slots).
+__device__ __forceinline__ RowPos row_pos(const GqaParams& p, int64_t r64) {
+  const uint32_t r = static_cast<uint32_t>(r64);
+  const uint32_t rq = r / static_cast<uint32_t>(p.Q);
   RowPos o;
-  o.j = static_cast<int>(r % p.Q);
-  o.g = static_cast<int>((r / p.Q) % p.G);
-  o.b = static_cast<int>(r / (static_cast<int64_t>(p.Q) * p.G));
+  o.j = static_cast<int>(r - rq * static_cast<uint32_t>(p.Q));
+  o.b = static_cast<int>(rq / static_cast<uint32_t>(p.G));
+  o.g = static_cast<int>(rq - static_cast<uint32_t>(o.b) * static_cast<uint32_t>(p.G));
   return o;
 }
 
 struct ItemInfo {
-  int blk, page, valid;
+  int blk, page, valid, g;
 };
 
 // Selected block, page and validity of item x (x >= x1: an empty slot). Checks
 // the device-side invariants; only the producer reports problems.
 __device__ __forceinline__ ItemInfo load_item(const GqaParams& p, int64_t x, int64_t x1, bool report) {
-  ItemInfo it{-1, -1, 0};
+  ItemInfo it{-1, -1, 0, 0};
   if (x >= x1) return it;
-  const int64_t r = x / p.K;
-  const int e = static_cast<int>(x % p.K);
+  const uint32_t r = static_cast<uint32_t>(x) / static_cast<uint32_t>(p.K);
+  const int e = static_cast<int>(static_cast<uint32_t>(x) - r * static_cast<uint32_t>(p.K));
   const RowPos rp = row_pos(p, r);
+  it.g = rp.g;
   it.blk = p.selected[((static_cast<int64_t>(rp.b) * p.Q + rp.j) * p.G + rp.g) * p.K + e];
   if (it.blk < 0) return it;
   const int L = p.seq_lens[rp.b];
@@ -212,6 +217,8 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     const uint64_t pol = l2_evict_first_policy();
     ItemInfo cur = load_item(p, x0 + lane, x1, true);
     int64_t i = 0;
+    int s = 0;
+    uint32_t phase = 0;
     bool ok = true;
     for (int64_t base = x0; base < x1 && ok; base += 32) {
       const ItemInfo nxt = load_item(p, base + 32 + lane, x1, true);
@@ -219,10 +226,9 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
       for (int k = 0; k < n; ++k) {
         if (!__shfl_sync(kAll, cur.valid, k)) continue;
         const int page = __shfl_sync(kAll, cur.page, k);
+        const int g = __shfl_sync(kAll, cur.g, k);
         if (lane == 0) {
-          const int g = row_pos(p, (base + k) / p.K).g;
-          const int s = static_cast<int>(i % kGqaStages);
-          if (!mbar_wait(smem_addr(&empty[s]), static_cast<uint32_t>(((i / kGqaStages) & 1) ^ 1))) {
+          if (!mbar_wait(smem_addr(&empty[s]), phase ^ 1u)) {
             set_flag(p.flags, MSA_FLAG_TIMEOUT);
             ok = false;
           } else {
@@ -248,6 +254,7 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
         ok = __shfl_sync(kAll, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         ++i;
+        if (++s == kGqaStages) { s = 0; phase ^= 1u; }
       }
       cur = nxt;
     }
@@ -270,7 +277,6 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
   float m_r[2], l_r[2], mul_r[2];
   int64_t seg_row = -1;
   int seg_b = 0, seg_g = 0, seg_j = 0, seg_p = 0, seg_ell = 0;
-  int64_t i = 0;
   bool ok = true;
 
   auto begin_segment = [&](int64_t r) {
@@ -440,19 +446,22 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
   };
 
   ItemInfo cur = load_item(p, x0 + lane, x1, false);
+  int64_t xrow = x0 / p.K;                    // row and slot of the current item, advanced by one per item
+  int xslot = static_cast<int>(x0 - xrow * p.K);
+  int s = 0;
+  uint32_t phase = 0;
   for (int64_t base = x0; base < x1 && ok; base += 32) {
    const ItemInfo nxt = load_item(p, base + 32 + lane, x1, false);
    const int nk = static_cast<int>(x1 - base < 32 ? x1 - base : 32);
    for (int kx = 0; kx < nk; ++kx) {
-    const int64_t xrow = (base + kx) / p.K;
     if (xrow != seg_row) {
       if (seg_row >= 0 && !end_segment()) { ok = false; break; }
       begin_segment(xrow);
     }
+    if (++xslot == p.K) { xslot = 0; ++xrow; }
     if (!__shfl_sync(kAll, cur.valid, kx)) continue;
     const int it_blk = __shfl_sync(kAll, cur.blk, kx);
-    const int s = static_cast<int>(i % kGqaStages);
-    if (!mbar_wait(smem_addr(&full[s]), static_cast<uint32_t>((i / kGqaStages) & 1))) { ok = false; break; }
+    if (!mbar_wait(smem_addr(&full[s]), phase)) { ok = false; break; }
     uint32_t kt = base_addr + Ly.stages + s * kStageBytes;   // bf16 tile: K lo, K hi, V lo, V hi
     if (kFp4) {
       // Expand this page's NVFP4 K and V into the fp16 tile. Thread ct expands
@@ -534,8 +543,13 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
         if (t0 + 1 > seg_p) { sc[nt][1] = -INFINITY; sc[nt][3] = -INFINITY; }
       }
     }
-    // ---- online softmax (log2 domain), rows gr and gr + 8
+    // ---- online softmax (log2 domain), rows gr and gr + 8. The reference max
+    // m_r is raised only when a block's max exceeds it by more than
+    // kRescaleSlack, so the unnormalised probabilities stay below 2^kRescaleSlack
+    // and most blocks leave the output accumulator unscaled (the final division
+    // by l makes the choice of reference immaterial up to rounding).
     float pr[4][4];
+    float bmax[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       float mx = -INFINITY;
@@ -543,26 +557,38 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
       for (int nt = 0; nt < 4; ++nt) mx = fmaxf(mx, fmaxf(sc[nt][2 * r], sc[nt][2 * r + 1]));
       mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 2));
-      const float mnew = fmaxf(m_r[r], mx * mul_r[r]);
-      const float alpha = mnew == -INFINITY ? 1.f : exp2f(m_r[r] - mnew);
+      bmax[r] = mx * mul_r[r];
+    }
+    const bool raise0 = bmax[0] > m_r[0] + kRescaleSlack, raise1 = bmax[1] > m_r[1] + kRescaleSlack;
+    if (__any_sync(kAll, raise0 || raise1)) {
+      float alpha[2] = {1.f, 1.f};
+      if (raise0) { alpha[0] = exp2f(m_r[0] - bmax[0]); m_r[0] = bmax[0]; }
+      if (raise1) { alpha[1] = exp2f(m_r[1] - bmax[1]); m_r[1] = bmax[1]; }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        l_r[r] *= alpha[r];
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          o[n][2 * r] *= alpha[r];
+          o[n][2 * r + 1] *= alpha[r];
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const float mref = m_r[r];
       float ls = 0.f;
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const float v = sc[nt][2 * r + e];
-          const float pv = (v == -INFINITY || mnew == -INFINITY) ? 0.f : exp2f(v * mul_r[r] - mnew);
+          const float pv = (v == -INFINITY || mref == -INFINITY) ? 0.f : exp2f(v * mul_r[r] - mref);
           pr[nt][2 * r + e] = pv;
           ls += pv;
         }
       }
-      l_r[r] = l_r[r] * alpha + ls;
-      m_r[r] = mnew;
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        o[n][2 * r] *= alpha;
-        o[n][2 * r + 1] *= alpha;
-      }
+      l_r[r] += ls;
     }
     // ---- O += P V (2 k-steps of 16 tokens, 16 n-tiles of 8 dims)
 #pragma unroll
@@ -598,7 +624,7 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
     }
-    ++i;
+    if (++s == kGqaStages) { s = 0; phase ^= 1u; }
    }
    cur = nxt;
   }
