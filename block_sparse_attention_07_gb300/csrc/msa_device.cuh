@@ -220,6 +220,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 
 // 2^e as fp32 for e in [-126, 127].
+// 2^x by the PTX ex2.approx.ftz instruction (about 22 correct bits; results
+// below 2^-126 flush to zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float exp2_int(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
 
 // Power-of-two factor 2^s (s in [-126, 126]) that brings amax into [2^14, 2^15):

@@ -30,7 +30,12 @@ namespace msa {
 
 template <bool kFp4>
 constexpr int stages_for() { return kFp4 ? 6 : 3; }   // 64 KB bf16 pages / 18 KB NVFP4 pages
-constexpr int kCWarps = 4;
+constexpr int kTokPerWarp = 32;                  // tokens of every block that one consumer warp owns
+constexpr int kCWarps = kBlock / kTokPerWarp;    // consumer warps (one per SM sub-partition)
+constexpr int kNT = kTokPerWarp / 8;             // QK^T n-tiles of 8 tokens per warp
+constexpr int kKK = kTokPerWarp / 16;            // PV k-steps of 16 tokens per warp
+constexpr int kCombWarps = kCWarps < 4 ? kCWarps : 4;   // states staged in shared memory at a row's end
+constexpr int kLanesPerRow = 32 / kTokPerWarp;   // NVFP4 expansion: lanes per token row
 constexpr int kBoxBytes = kBlock * 64 * 2;       // 128 rows x 128 B (64 fp16/bf16)
 constexpr int kTileBytes = 4 * kBoxBytes;        // K lo/hi + V lo/hi = 64 KB
 constexpr int kFp4StageBytes = 2 * (kBlock * kDim / 2 + kBlock * kDim / 16);  // 18 KB
@@ -72,9 +77,9 @@ __host__ __device__ constexpr SmemLayout gqa_layout() {
   const uint32_t stage_bytes = kFp4 ? kFp4StageBytes : kTileBytes;
   s.tiles = s.stages + stages_for<kFp4>() * stage_bytes;
   s.comb_o = s.tiles + (kFp4 ? kTileBytes : 0);
-  s.comb_ml = s.comb_o + kCWarps * kGroup * kDim * 4;
-  s.bars = s.comb_ml + kCWarps * kGroup * 2 * 4;
-  s.total = s.bars + (2 * stages_for<kFp4>() + 2) * 8 + 16;   // + the last-arriver flag
+  s.comb_ml = s.comb_o + kCombWarps * kGroup * kDim * 4;
+  s.bars = s.comb_ml + kCombWarps * kGroup * 2 * 4;
+  s.total = s.bars + (2 * stages_for<kFp4>() + 3) * 8 + 16;   // + the last-arriver flag
   return s;
 }
 
@@ -174,11 +179,11 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
   uint8_t* sm = smem_raw + (base_addr - raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + Ly.bars);
   uint64_t* empty = full + kGqaStages;
-  uint64_t* gbar = empty + kGqaStages;   // [0]: partials written, [1]: partials read
+  uint64_t* gbar = empty + kGqaStages;   // [0]: partials written, [1]: partials read, [2]: upper warps staged
   float* comb_o = reinterpret_cast<float*>(sm + Ly.comb_o);
   float* comb_m = reinterpret_cast<float*>(sm + Ly.comb_ml);
-  float* comb_l = comb_m + kCWarps * kGroup;
-  int* last_flag = reinterpret_cast<int*>(sm + Ly.bars + (2 * kGqaStages + 2) * 8);
+  float* comb_l = comb_m + kCombWarps * kGroup;
+  int* last_flag = reinterpret_cast<int*>(sm + Ly.bars + (2 * kGqaStages + 3) * 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_launch_dependents();
@@ -189,6 +194,7 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     }
     mbar_init(smem_addr(&gbar[0]), kCWarps);
     mbar_init(smem_addr(&gbar[1]), kCWarps);
+    mbar_init(smem_addr(&gbar[2]), kCWarps);
     fence_mbar_init();
     if (!kFp4) {
       prefetch_tensormap(&tk);
@@ -267,10 +273,10 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
   }
 
   // -------------------------------------------------------------- consumers --
-  const int w = warp - 1;          // token slice [32w, 32w + 32) of every block
-  const int ct = threadIdx.x - 32; // 0..127
+  const int w = warp - 1;          // token slice [kTokPerWarp w, kTokPerWarp (w + 1)) of every block
+  const int ct = threadIdx.x - 32; // 0 .. 32 kCWarps - 1; the first 128 merge a row's states
   const int gr = lane >> 2, c = lane & 3;
-  uint32_t gph[2] = {0u, 0u};
+  uint32_t gph[3] = {0u, 0u, 0u};
 
   uint32_t qf[8][4];
   float o[16][4];
@@ -287,49 +293,47 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     seg_p = L - p.Q + rp.j;
     seg_ell = seg_p / kBlock;
     const uint16_t* qh = p.q + ((static_cast<int64_t>(rp.b) * p.Q + rp.j) * p.H + static_cast<int64_t>(rp.g) * kGroup) * kDim;
-    float qv[2][32];
+    // The bf16 query words are the mma A fragments as loaded: qf[s] holds rows
+    // gr / gr + 8 at dims 16 s + 2 c (+1) and 16 s + 8 + 2 c (+1).
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const uint16_t* row = qh + (gr + 8 * r) * kDim + 16 * s + 2 * c;
-        const uint32_t lo = *reinterpret_cast<const uint32_t*>(row);
-        const uint32_t hi = *reinterpret_cast<const uint32_t*>(row + 8);
-        qv[r][4 * s + 0] = bf16_bits_to_f32(lo & 0xFFFF);
-        qv[r][4 * s + 1] = bf16_bits_to_f32(lo >> 16);
-        qv[r][4 * s + 2] = bf16_bits_to_f32(hi & 0xFFFF);
-        qv[r][4 * s + 3] = bf16_bits_to_f32(hi >> 16);
+        qf[s][r] = *reinterpret_cast<const uint32_t*>(row);
+        qf[s][2 + r] = *reinterpret_cast<const uint32_t*>(row + 8);
       }
     }
-    float f[2] = {1.f, 1.f};
     if (kFp4) {
+      // fp16 operands: rescale each query row by an exact power of two that
+      // keeps it inside the fp16 range; the logit multiplier undoes it.
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         float amax = 0.f;
 #pragma unroll
-        for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(qv[r][k]));
+        for (int s = 0; s < 8; ++s) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t wq = qf[s][2 * h + r];
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_f32(wq & 0xFFFF)), fabsf(bf16_bits_to_f32(wq >> 16))));
+          }
+        }
         amax = fmaxf(amax, __shfl_xor_sync(kAll, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(kAll, amax, 2));
         const int sh = fp16_shift_for(amax);
-        f[r] = exp2_int(sh);
+        const float f = exp2_int(sh);
         mul_r[r] = p.scale_log2 * p.k_global * exp2_int(-sh);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t wq = qf[s][2 * h + r];
+            qf[s][2 * h + r] = pack_f16x2(bf16_bits_to_f32(wq & 0xFFFF) * f, bf16_bits_to_f32(wq >> 16) * f);
+          }
+        }
       }
     } else {
       mul_r[0] = mul_r[1] = p.scale_log2;
-    }
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      if (kFp4) {
-        qf[s][0] = pack_f16x2(qv[0][4 * s] * f[0], qv[0][4 * s + 1] * f[0]);
-        qf[s][1] = pack_f16x2(qv[1][4 * s] * f[1], qv[1][4 * s + 1] * f[1]);
-        qf[s][2] = pack_f16x2(qv[0][4 * s + 2] * f[0], qv[0][4 * s + 3] * f[0]);
-        qf[s][3] = pack_f16x2(qv[1][4 * s + 2] * f[1], qv[1][4 * s + 3] * f[1]);
-      } else {
-        qf[s][0] = pack_bf16x2(qv[0][4 * s], qv[0][4 * s + 1]);
-        qf[s][1] = pack_bf16x2(qv[1][4 * s], qv[1][4 * s + 1]);
-        qf[s][2] = pack_bf16x2(qv[0][4 * s + 2], qv[0][4 * s + 3]);
-        qf[s][3] = pack_bf16x2(qv[1][4 * s + 2], qv[1][4 * s + 3]);
-      }
     }
 #pragma unroll
     for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -337,8 +341,25 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     l_r[0] = l_r[1] = 0.f;
   };
 
-  // Merges the four warps' states of the current row; writes the final output
-  // when this CTA covered the whole row, a split-K partial otherwise.
+  // Stages this warp's state (o, m, l) of the current row in slot k.
+  auto stage_state = [&](int k, const float (&lt)[2]) {
+    float* mo = comb_o + k * kGroup * kDim;
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      *reinterpret_cast<float2*>(mo + gr * kDim + 8 * n + 2 * c) = make_float2(o[n][0], o[n][1]);
+      *reinterpret_cast<float2*>(mo + (gr + 8) * kDim + 8 * n + 2 * c) = make_float2(o[n][2], o[n][3]);
+    }
+    if (c == 0) {
+      comb_m[k * kGroup + gr] = m_r[0];
+      comb_m[k * kGroup + gr + 8] = m_r[1];
+      comb_l[k * kGroup + gr] = lt[0];
+      comb_l[k * kGroup + gr + 8] = lt[1];
+    }
+  };
+
+  // Merges the warps' states of the current row; writes the final output when
+  // this CTA covered the whole row, a split-K partial otherwise. Every consumer
+  // warp takes every barrier; the merge itself runs on the first 128 threads.
   auto end_segment = [&]() -> bool {
     float lt[2];
 #pragma unroll
@@ -348,37 +369,53 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
       v += __shfl_xor_sync(kAll, v, 2);
       lt[r] = v;
     }
-    float* mo = comb_o + w * kGroup * kDim;
+    if constexpr (kCWarps > kCombWarps) {
+      // Warp w + 4 hands its state to warp w, which folds it into its registers
+      // and then reuses the slot for the merged state.
+      if (w >= kCombWarps) stage_state(w - kCombWarps, lt);
+      if (!group_sync(smem_addr(&gbar[2]), gph[2], lane)) return false;
+      if (w < kCombWarps) {
+        const float* po = comb_o + w * kGroup * kDim;
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      *reinterpret_cast<float2*>(mo + gr * kDim + 8 * n + 2 * c) = make_float2(o[n][0], o[n][1]);
-      *reinterpret_cast<float2*>(mo + (gr + 8) * kDim + 8 * n + 2 * c) = make_float2(o[n][2], o[n][3]);
+        for (int r = 0; r < 2; ++r) {
+          const float mp = comb_m[w * kGroup + gr + 8 * r], lp = comb_l[w * kGroup + gr + 8 * r];
+          const float M = fmaxf(m_r[r], mp);
+          const float fa = M == -INFINITY ? 0.f : ex2_approx(m_r[r] - M);
+          const float fb = M == -INFINITY ? 0.f : ex2_approx(mp - M);
+          lt[r] = lt[r] * fa + lp * fb;
+          m_r[r] = M;
+#pragma unroll
+          for (int n = 0; n < 16; ++n) {
+            const float2 x = *reinterpret_cast<const float2*>(po + (gr + 8 * r) * kDim + 8 * n + 2 * c);
+            o[n][2 * r] = o[n][2 * r] * fa + x.x * fb;
+            o[n][2 * r + 1] = o[n][2 * r + 1] * fa + x.y * fb;
+          }
+        }
+      }
     }
-    if (c == 0) {
-      comb_m[w * kGroup + gr] = m_r[0];
-      comb_m[w * kGroup + gr + 8] = m_r[1];
-      comb_l[w * kGroup + gr] = lt[0];
-      comb_l[w * kGroup + gr + 8] = lt[1];
-    }
+    if (w < kCombWarps) stage_state(w, lt);
     if (!group_sync(smem_addr(&gbar[0]), gph[0], lane)) return false;
-    const int hh = ct >> 3, d0 = (ct & 7) * 16;
+    const bool merger = ct < kCombWarps * 32;
+    const int hh = (ct >> 3) & (kGroup - 1), d0 = (ct & 7) * 16;
     float M = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < kCWarps; ++k) M = fmaxf(M, comb_m[k * kGroup + hh]);
-    float fw[kCWarps];
     float Ls = 0.f;
-#pragma unroll
-    for (int k = 0; k < kCWarps; ++k) {
-      fw[k] = M == -INFINITY ? 0.f : exp2f(comb_m[k * kGroup + hh] - M);
-      Ls += fw[k] * comb_l[k * kGroup + hh];
-    }
     float acc[16];
+    if (merger) {
 #pragma unroll
-    for (int d = 0; d < 16; ++d) {
-      float v = 0.f;
+      for (int k = 0; k < kCombWarps; ++k) M = fmaxf(M, comb_m[k * kGroup + hh]);
+      float fw[kCombWarps];
 #pragma unroll
-      for (int k = 0; k < kCWarps; ++k) v += fw[k] * comb_o[(k * kGroup + hh) * kDim + d0 + d];
-      acc[d] = v * (kFp4 ? p.v_global : 1.f);
+      for (int k = 0; k < kCombWarps; ++k) {
+        fw[k] = M == -INFINITY ? 0.f : ex2_approx(comb_m[k * kGroup + hh] - M);
+        Ls += fw[k] * comb_l[k * kGroup + hh];
+      }
+#pragma unroll
+      for (int d = 0; d < 16; ++d) {
+        float v = 0.f;
+#pragma unroll
+        for (int k = 0; k < kCombWarps; ++k) v += fw[k] * comb_o[(k * kGroup + hh) * kDim + d0 + d];
+        acc[d] = v * (kFp4 ? p.v_global : 1.f);
+      }
     }
     const int64_t r = seg_row;
     const bool whole = x0 <= r * p.K && (r + 1) * p.K <= x1;
@@ -394,7 +431,7 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
       if (p.lse != nullptr && (ct & 7) == 0) p.lse[head] = ll > 0.f ? (mm + log2f(ll)) * kLn2 : -INFINITY;
     };
     if (whole) {
-      write_out(acc, M, Ls);
+      if (merger) write_out(acc, M, Ls);
       return group_sync(smem_addr(&gbar[1]), gph[1], lane);
     }
     // Split row: publish this CTA's partial; the CTA that delivers the last
@@ -403,12 +440,14 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     const int nslots = cta_of(r * p.K + p.K - 1, p.W, C) - first + 1;
     float* rowp = p.ws + r * p.K * static_cast<int64_t>(kPartialFloats);
     float* part = rowp + (static_cast<int>(blockIdx.x) - first) * static_cast<int64_t>(kPartialFloats);
-    float4* dst = reinterpret_cast<float4*>(part + hh * kDim + d0);
+    if (merger) {
+      float4* dst = reinterpret_cast<float4*>(part + hh * kDim + d0);
 #pragma unroll
-    for (int d = 0; d < 4; ++d) dst[d] = make_float4(acc[4 * d], acc[4 * d + 1], acc[4 * d + 2], acc[4 * d + 3]);
-    if ((ct & 7) == 0) {
-      part[kGroup * kDim + hh] = M;
-      part[kGroup * kDim + kGroup + hh] = Ls;
+      for (int d = 0; d < 4; ++d) dst[d] = make_float4(acc[4 * d], acc[4 * d + 1], acc[4 * d + 2], acc[4 * d + 3]);
+      if ((ct & 7) == 0) {
+        part[kGroup * kDim + hh] = M;
+        part[kGroup * kDim + kGroup + hh] = Ls;
+      }
     }
     if (!group_sync(smem_addr(&gbar[1]), gph[1], lane)) return false;
     if (ct == 0) {
@@ -418,7 +457,7 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
       *last_flag = last ? 1 : 0;
     }
     if (!group_sync(smem_addr(&gbar[0]), gph[0], lane)) return false;
-    if (*last_flag) {
+    if (*last_flag && merger) {
       float M2 = -INFINITY;
       for (int q = 0; q < nslots; ++q) M2 = fmaxf(M2, __ldcg(rowp + q * kPartialFloats + kGroup * kDim + hh));
       float L2 = 0.f;
@@ -428,7 +467,7 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
       if (M2 != -INFINITY) {
         for (int q = 0; q < nslots; ++q) {
           const float* pq = rowp + q * kPartialFloats;
-          const float f = exp2f(__ldcg(pq + kGroup * kDim + hh) - M2);
+          const float f = ex2_approx(__ldcg(pq + kGroup * kDim + hh) - M2);
           L2 += f * __ldcg(pq + kGroup * kDim + kGroup + hh);
 #pragma unroll
           for (int d4 = 0; d4 < 4; ++d4) {
@@ -445,100 +484,55 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     return true;
   };
 
-  ItemInfo cur = load_item(p, x0 + lane, x1, false);
-  int64_t xrow = x0 / p.K;                    // row and slot of the current item, advanced by one per item
-  int xslot = static_cast<int>(x0 - xrow * p.K);
-  int s = 0;
-  uint32_t phase = 0;
-  for (int64_t base = x0; base < x1 && ok; base += 32) {
-   const ItemInfo nxt = load_item(p, base + 32 + lane, x1, false);
-   const int nk = static_cast<int>(x1 - base < 32 ? x1 - base : 32);
-   for (int kx = 0; kx < nk; ++kx) {
-    if (xrow != seg_row) {
-      if (seg_row >= 0 && !end_segment()) { ok = false; break; }
-      begin_segment(xrow);
-    }
-    if (++xslot == p.K) { xslot = 0; ++xrow; }
-    if (!__shfl_sync(kAll, cur.valid, kx)) continue;
-    const int it_blk = __shfl_sync(kAll, cur.blk, kx);
-    if (!mbar_wait(smem_addr(&full[s]), phase)) { ok = false; break; }
-    uint32_t kt = base_addr + Ly.stages + s * kStageBytes;   // bf16 tile: K lo, K hi, V lo, V hi
-    if (kFp4) {
-      // Expand this page's NVFP4 K and V into the fp16 tile. Thread ct expands
-      // token row ct = 32 w + lane, which only its own warp reads afterwards, so
-      // a warp-level barrier suffices and the tile can be reused at once.
-      const uint32_t tile = base_addr + Ly.tiles;
-      const uint8_t* st = sm + Ly.stages + s * kStageBytes;
-      const int t = ct;
+  // QK^T of this warp's tokens for the tile at kt (K lo / K hi boxes).
+  // ldmatrix addresses within a tile, per thread. A row's 16-byte chunk q sits
+  // at row * 128 + ((q ^ (row & 7)) << 4) of its box; every row this thread
+  // addresses has row & 7 == lane & 7, so only the chunk's low bits vary with
+  // the loop indices and the rest are compile-time offsets.
+  //   QK^T (K boxes): row 8 nt + (lane & 7) of the warp's slice, chunk 4 (sp & 1) + (lane >> 3)
+  //   PV (V boxes):   row 16 kk + 8 ((lane >> 3) & 1) + (lane & 7), chunk 2 (np & 3) + (lane >> 4)
+  const uint32_t warp_rows = static_cast<uint32_t>(kTokPerWarp * w) * 128u;
+  uint32_t k_off[2], v_off[4];
 #pragma unroll
-      for (int kv = 0; kv < 2; ++kv) {
-        const uint8_t* codes = st + kv * (kBlock * kDim / 2 + kBlock * kDim / 16);
-        const uint8_t* scl = codes + kBlock * kDim / 2;
-        const uint32_t dbox = tile + kv * 2 * kBoxBytes;
+  for (int h = 0; h < 2; ++h)
+    k_off[h] = warp_rows + (lane & 7) * 128u + ((((4 * h) + (lane >> 3)) ^ (lane & 7)) << 4);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int qq = (q + (t >> 1)) & 3;      // rotate 16-byte chunks: no bank conflicts
-          const uint4 cw = *reinterpret_cast<const uint4*>(codes + t * 64 + qq * 16);
-          const uint16_t sc2 = *reinterpret_cast<const uint16_t*>(scl + t * 8 + 2 * qq);
-          const uint32_t s2 = e4m3x2_to_f16x2(sc2);
-          const __half2 sa = __half2half2(__ushort_as_half(static_cast<unsigned short>(s2 & 0xFFFF)));
-          const __half2 sb = __half2half2(__ushort_as_half(static_cast<unsigned short>(s2 >> 16)));
-          const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {            // 8 codes -> 8 fp16 -> one 16-byte chunk
-            uint32_t h[4];
-            e2m1x4_to_f16x2x2(static_cast<uint16_t>(words[k] & 0xFFFF), h[0], h[1]);
-            e2m1x4_to_f16x2x2(static_cast<uint16_t>(words[k] >> 16), h[2], h[3]);
-            const __half2 scl2 = k < 2 ? sa : sb;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h[e]), scl2);
-              h[e] = *reinterpret_cast<uint32_t*>(&v);
-            }
-            const int chunk = 4 * qq + k;          // dims 8*chunk .. 8*chunk+7
-            const uint32_t a = swz(dbox + (chunk >> 3) * kBoxBytes, t, chunk & 7);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(h[0]), "r"(h[1]), "r"(h[2]),
-                         "r"(h[3])
-                         : "memory");
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
-      kt = tile;
-    }
+  for (int h = 0; h < 4; ++h)
+    v_off[h] = warp_rows + (8 * ((lane >> 3) & 1) + (lane & 7)) * 128u + ((((2 * h) + (lane >> 4)) ^ (lane & 7)) << 4);
 
-    // ---- S = Q K^T for this warp's 32 tokens (4 n-tiles of 8 tokens).
-    // The four n-tiles are independent accumulation chains, interleaved per
-    // pair of k-steps so that the mma latencies overlap.
-    float sc[4][4];
+  auto qk = [&](uint32_t kt, float (&sc)[kNT][4]) {
+    // ---- S = Q K^T for this warp's tokens (kNT n-tiles of 8 tokens). The
+    // n-tiles are independent accumulation chains, interleaved per pair of
+    // k-steps so that the mma latencies overlap.
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+    for (int nt = 0; nt < kNT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
     for (int sp = 0; sp < 4; ++sp) {
-      const int chunk = 4 * sp + (lane >> 3);
-      uint32_t b[4][4];
+      const uint32_t kb = kt + (sp >> 1) * kBoxBytes + k_off[sp & 1];
+      uint32_t b[kNT][4];
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int tok = 32 * w + 8 * nt + (lane & 7);
-        ldsm_x4(swz(kt + (chunk >> 3) * kBoxBytes, tok, chunk & 7), b[nt][0], b[nt][1], b[nt][2], b[nt][3]);
-      }
+      for (int nt = 0; nt < kNT; ++nt) ldsm_x4(kb + nt * 8 * 128, b[nt][0], b[nt][1], b[nt][2], b[nt][3]);
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
+      for (int nt = 0; nt < kNT; ++nt) {
         if (kFp4) mma_f16(sc[nt], qf[2 * sp], b[nt][0], b[nt][1]);
         else mma_bf16(sc[nt], qf[2 * sp], b[nt][0], b[nt][1]);
       }
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
+      for (int nt = 0; nt < kNT; ++nt) {
         if (kFp4) mma_f16(sc[nt], qf[2 * sp + 1], b[nt][2], b[nt][3]);
         else mma_bf16(sc[nt], qf[2 * sp + 1], b[nt][2], b[nt][3]);
       }
     }
+  };
+
+  // Causal limit and the first half of the online softmax for one tile: block
+  // maxima and, when the reference max rises, the rescale of the accumulators.
+  auto softmax_prep = [&](float (&sc)[kNT][4], int it_blk) {
     // ---- causal limit inside the local block
     if (it_blk == seg_ell) {
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int t0 = it_blk * kBlock + 32 * w + 8 * nt + 2 * c;
+      for (int nt = 0; nt < kNT; ++nt) {
+        const int t0 = it_blk * kBlock + kTokPerWarp * w + 8 * nt + 2 * c;
         if (t0 > seg_p) { sc[nt][0] = -INFINITY; sc[nt][2] = -INFINITY; }
         if (t0 + 1 > seg_p) { sc[nt][1] = -INFINITY; sc[nt][3] = -INFINITY; }
       }
@@ -548,13 +542,12 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     // kRescaleSlack, so the unnormalised probabilities stay below 2^kRescaleSlack
     // and most blocks leave the output accumulator unscaled (the final division
     // by l makes the choice of reference immaterial up to rounding).
-    float pr[4][4];
     float bmax[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       float mx = -INFINITY;
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) mx = fmaxf(mx, fmaxf(sc[nt][2 * r], sc[nt][2 * r + 1]));
+      for (int nt = 0; nt < kNT; ++nt) mx = fmaxf(mx, fmaxf(sc[nt][2 * r], sc[nt][2 * r + 1]));
       mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 2));
       bmax[r] = mx * mul_r[r];
@@ -562,8 +555,8 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     const bool raise0 = bmax[0] > m_r[0] + kRescaleSlack, raise1 = bmax[1] > m_r[1] + kRescaleSlack;
     if (__any_sync(kAll, raise0 || raise1)) {
       float alpha[2] = {1.f, 1.f};
-      if (raise0) { alpha[0] = exp2f(m_r[0] - bmax[0]); m_r[0] = bmax[0]; }
-      if (raise1) { alpha[1] = exp2f(m_r[1] - bmax[1]); m_r[1] = bmax[1]; }
+      if (raise0) { alpha[0] = ex2_approx(m_r[0] - bmax[0]); m_r[0] = bmax[0]; }
+      if (raise1) { alpha[1] = ex2_approx(m_r[1] - bmax[1]); m_r[1] = bmax[1]; }
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         l_r[r] *= alpha[r];
@@ -574,25 +567,31 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
         }
       }
     }
+  };
+
+  // Second half: probabilities, row sums and O += P V from the V boxes at kt.
+  auto softmax_pv = [&](uint32_t kt, const float (&sc)[kNT][4]) {
+    float pr[kNT][4];
+    // p = 2^(s * mul - m): masked logits (-inf) give 0 since mul > 0; while the
+    // reference is still -inf every logit so far is -inf, and 0 stands in for it.
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      const float mref = m_r[r];
+      const float neg_ref = m_r[r] == -INFINITY ? 0.f : -m_r[r];
       float ls = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
+      for (int nt = 0; nt < kNT; ++nt) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float v = sc[nt][2 * r + e];
-          const float pv = (v == -INFINITY || mref == -INFINITY) ? 0.f : exp2f(v * mul_r[r] - mref);
+          const float pv = ex2_approx(fmaf(sc[nt][2 * r + e], mul_r[r], neg_ref));
           pr[nt][2 * r + e] = pv;
           ls += pv;
         }
       }
       l_r[r] += ls;
     }
-    // ---- O += P V (2 k-steps of 16 tokens, 16 n-tiles of 8 dims)
+    // ---- O += P V (kKK k-steps of 16 tokens, 16 n-tiles of 8 dims)
 #pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
+    for (int kk = 0; kk < kKK; ++kk) {
       uint32_t a[4];
       if (kFp4) {
         a[0] = pack_f16x2(pr[2 * kk][0], pr[2 * kk][1]);
@@ -605,12 +604,10 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
         a[2] = pack_bf16x2(pr[2 * kk + 1][0], pr[2 * kk + 1][1]);
         a[3] = pack_bf16x2(pr[2 * kk + 1][2], pr[2 * kk + 1][3]);
       }
-      const int tok = 32 * w + 16 * kk + 8 * ((lane >> 3) & 1) + (lane & 7);
 #pragma unroll
       for (int np = 0; np < 8; ++np) {
-        const int chunk = 2 * np + (lane >> 4);
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(swz(kt + 2 * kBoxBytes + (chunk >> 3) * kBoxBytes, tok, chunk & 7), b0, b1, b2, b3);
+        ldsm_x4_t(kt + (2 + (np >> 2)) * kBoxBytes + kk * 16 * 128 + v_off[np & 3], b0, b1, b2, b3);
         if (kFp4) {
           mma_f16(o[2 * np], a, b0, b1);
           mma_f16(o[2 * np + 1], a, b2, b3);
@@ -620,13 +617,98 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
         }
       }
     }
-    if (!kFp4) {
+  };
+
+  // NVFP4: expands stage s into the warp's rows of the fp16 tile, releases the stage.
+  auto expand = [&](int s) -> uint32_t {
+    // Expand this page's NVFP4 K and V into the fp16 tile. The warp expands
+    // its own token rows (kLanesPerRow lanes per row), which only it reads
+    // afterwards, so a warp-level barrier suffices and the tile can be reused
+    // at once.
+    const uint32_t tile = base_addr + Ly.tiles;
+    const uint8_t* st = sm + Ly.stages + s * kStageBytes;
+    const int t = kTokPerWarp * w + lane / kLanesPerRow;
+    const int sub = lane % kLanesPerRow;
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+      const uint8_t* codes = st + kv * (kBlock * kDim / 2 + kBlock * kDim / 16);
+      const uint8_t* scl = codes + kBlock * kDim / 2;
+      const uint32_t dbox = tile + kv * 2 * kBoxBytes;
+#pragma unroll
+      for (int q = 0; q < 4 / kLanesPerRow; ++q) {
+        const int qq = (q * kLanesPerRow + sub + (t >> 1)) & 3;   // rotate 16-byte chunks: fewer bank conflicts
+        const uint4 cw = *reinterpret_cast<const uint4*>(codes + t * 64 + qq * 16);
+        const uint16_t sc2 = *reinterpret_cast<const uint16_t*>(scl + t * 8 + 2 * qq);
+        const uint32_t s2 = e4m3x2_to_f16x2(sc2);
+        const __half2 sa = __half2half2(__ushort_as_half(static_cast<unsigned short>(s2 & 0xFFFF)));
+        const __half2 sb = __half2half2(__ushort_as_half(static_cast<unsigned short>(s2 >> 16)));
+        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {            // 8 codes -> 8 fp16 -> one 16-byte chunk
+          uint32_t h[4];
+          e2m1x4_to_f16x2x2(static_cast<uint16_t>(words[k] & 0xFFFF), h[0], h[1]);
+          e2m1x4_to_f16x2x2(static_cast<uint16_t>(words[k] >> 16), h[2], h[3]);
+          const __half2 scl2 = k < 2 ? sa : sb;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h[e]), scl2);
+            h[e] = *reinterpret_cast<uint32_t*>(&v);
+          }
+          const int chunk = 4 * qq + k;          // dims 8*chunk .. 8*chunk+7
+          const uint32_t a = swz(dbox + (chunk >> 3) * kBoxBytes, t, chunk & 7);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(h[0]), "r"(h[1]), "r"(h[2]),
+                       "r"(h[3])
+                       : "memory");
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+    return tile;
+  };
+
+  // Item cursor: `cur` holds the infos of items base .. base + 31, `nxt` of the
+  // 32 after them (loaded one chunk ahead).
+  ItemInfo cur = load_item(p, x0 + lane, x1, false);
+  ItemInfo nxt = load_item(p, x0 + 32 + lane, x1, false);
+  int64_t base = x0;
+  int kx = 0;
+  int64_t xrow = x0 / p.K;                    // row and slot of the current item, advanced by one per item
+  int xslot = static_cast<int>(x0 - xrow * p.K);
+  int s = 0;
+  uint32_t phase = 0;
+  float sc[kNT][4];
+  while (ok && base + kx < x1) {
+    if (xrow != seg_row) {
+      if (seg_row >= 0 && !end_segment()) { ok = false; break; }
+      begin_segment(xrow);
+    }
+    const int valid = __shfl_sync(kAll, cur.valid, kx);
+    const int it_blk = __shfl_sync(kAll, cur.blk, kx);
+    if (++xslot == p.K) { xslot = 0; ++xrow; }
+    if (++kx == 32) {
+      kx = 0;
+      base += 32;
+      cur = nxt;
+      nxt = load_item(p, base + 32 + lane, x1, false);
+    }
+    if (!valid) continue;
+    uint32_t kt = base_addr + Ly.stages + s * kStageBytes;   // bf16 tile: K lo, K hi, V lo, V hi
+    if (kFp4) {
+      if (!mbar_wait(smem_addr(&full[s]), phase)) { ok = false; break; }
+      kt = expand(s);
+      qk(kt, sc);
+      softmax_prep(sc, it_blk);
+      softmax_pv(kt, sc);
+    } else {
+      if (!mbar_wait(smem_addr(&full[s]), phase)) { ok = false; break; }
+      qk(kt, sc);
+      softmax_prep(sc, it_blk);
+      softmax_pv(kt, sc);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
     }
     if (++s == kGqaStages) { s = 0; phase ^= 1u; }
-   }
-   cur = nxt;
   }
   if (ok && seg_row >= 0) ok = end_segment();
   if (!ok && lane == 0) set_flag(p.flags, MSA_FLAG_TIMEOUT);
