@@ -46,8 +46,8 @@ FALLBACK_HBM_GBS = 6800.0
 # workload, keyed by the hash of the kernel's sources when it was measured (a
 # changed kernel reports null until it is measured again). Summaries: profiles/.
 NCU_TRAFFIC = {
-    ("index_score", "1097b3c4487c882a"): 551638272 + 3004672,
-    ("sparse_gqa", "8987f8d2488a11f7"): 134868224 + 324096,
+    ("index_score", "66e3ad521ee48e05"): 551615232 + 3003392,
+    ("sparse_gqa", "9b162ab162f6477b"): 134881280 + 104192,
 }
 
 
