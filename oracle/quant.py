@@ -18,6 +18,10 @@ quantisation formulas; the readings below are this project's:
   (token, KV head) row: sb = E4M3((amax16 / 6) / g); codes = E2M1(x / (sb * g));
   if sb decodes to 0 every code is 0. Nibble order: the low nibble holds the
   even element.
+* NVFP4 index keys: the same rule per (token, index head) row, with the index
+  cache's own global scale (the pages name the format but not its rule:
+  "MiniMax-M3.1-Flash Day-0 対応", section "何が新しいか" — the NVFP4 cache
+  covers the indexer — and section "試し方" — indexer_kv_dtype nvfp4).
 
 These steps are carried out in fp32 with IEEE round-to-nearest operations (one
 rounding per operation, in the order written), which is the precision in which
