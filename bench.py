@@ -211,18 +211,22 @@ def run_ours(args, world, rank, local):
     names = ("insert", "index_score", "select", "sparse_gqa")
 
     def timed_steps(n, events):
-        """n steps; events "step" records only step boundaries plus the index-score
-        kernel (the others launch back to back and overlap through programmatic
-        dependent launch), "all" records between every kernel (no overlap)."""
+        """n steps. events "step": records only at step boundaries, so the four
+        kernels launch back to back and overlap through programmatic dependent
+        launch; "index": also around the index-score kernel (its duration for
+        the roofline; the events cut the overlap on both sides of it); "all":
+        between every kernel (no overlap; the per-kernel breakdown)."""
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
         for s in range(n):
             flush(s)
             e = ev[s]
             e[0].record(stream)
             dw.insert_step_tokens()
-            e[1].record(stream)
+            if events != "step":
+                e[1].record(stream)
             dw.index_score()
-            e[2].record(stream)
+            if events != "step":
+                e[2].record(stream)
             dw.select()
             if events == "all":
                 e[3].record(stream)
@@ -230,7 +234,7 @@ def run_ours(args, world, rank, local):
             e[4].record(stream)
         torch.cuda.synchronize(dev)
         step = [ev[s][0].elapsed_time(ev[s][4]) for s in range(n)]
-        idx = [ev[s][1].elapsed_time(ev[s][2]) for s in range(n)]
+        idx = [ev[s][1].elapsed_time(ev[s][2]) for s in range(n)] if events != "step" else None
         per = None
         if events == "all":
             per = {nm: [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(n)] for i, nm in enumerate(names)}
@@ -242,9 +246,11 @@ def run_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
-    step_ms, idx_launch_ms, _ = timed_steps(args.steps, "step")
+    step_ms, _, _ = timed_steps(args.steps, "step")
     barrier(world)
     wall = time.perf_counter() - wall0
+    # the index-score kernel's launch duration (roofline), timed live over K more steps
+    idx_step_ms, idx_launch_ms, _ = timed_steps(args.steps, "index")
     clk = clocks.stop()
     launches = args.steps * 4          # insert, index, select, attention (split-K combine fused)
     # per-kernel breakdown, outside the timed region, with an event between every kernel
@@ -281,6 +287,32 @@ def run_ours(args, world, rank, local):
     e2e_tot, _ = aggregate(sum(e2e_ms) / 1e3, 0, world, dev)
     assert dw.check_flags() == 0, "device flags raised"
 
+    def event_timed(fn, n):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for s in range(n):
+            flush(s)
+            ev[s][0].record(stream)
+            fn()
+            ev[s][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in ev]
+
+    # The same step replayed from one CUDA graph per step.
+    graph = dw.capture(dw.step)
+    for _ in range(args.warmup):
+        graph.replay()
+    graph_ms = event_timed(graph.replay, args.steps)
+    assert dw.check_flags() == 0, "device flags raised (graph replay)"
+    # A layer that reuses this step's selection: K/V insert + sparse GQA only.
+    reuse_ms = None
+    if not args.no_layer_reuse:
+        layer = DeviceWorkload.layer_like(dw, 1)
+        for _ in range(args.warmup):
+            layer.reuse_step(dw.selected)
+        reuse_ms = event_timed(lambda: layer.reuse_step(dw.selected), args.steps)
+        assert layer.check_flags() == 0, "device flags raised (reusing layer)"
+        del layer
+
     if rank != 0:
         return None
     peak, peak_kind = measured_peaks()
@@ -306,17 +338,28 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": "index_score", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": ib, "avg_launch_ms": idx_ms},
+                     "algorithmic_bytes_per_launch": ib, "avg_launch_ms": idx_ms,
+                     "timed_in": f"{args.steps} further steps with events around the kernel "
+                                 f"({statistics.mean(idx_step_ms):.4f} ms per step there)"},
         "kernels_ms": {n: statistics.mean(v) for n, v in per.items()},
         "sparse_gqa_roofline": {"achieved": ab / (att_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                                 "frac": ab / (att_ms / 1e3) / 1e9 / peak, "algorithmic_bytes_per_launch": ab,
                                 "traffic": att_traffic},
         "e2e": {"value": B * Q * args.steps * world / e2e_tot, "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
+        "graph": {"value": B * Q / (statistics.mean(graph_ms) / 1e3), "unit": "query-tokens/s",
+                  "ms_per_step": statistics.mean(graph_ms),
+                  "what": "the same step (4 kernels) replayed from one captured CUDA graph per step"},
         "gpu_launches": launches,
         "clocks": clk,
         "wall_s_timed_region": wall,
     }
+    if reuse_ms is not None:
+        line["selection_reuse_layer"] = {
+            "value": B * Q / (statistics.mean(reuse_ms) / 1e3), "unit": "query-tokens/s",
+            "ms_per_step": statistics.mean(reuse_ms),
+            "what": "a second layer (own q/K/V) reusing this step's block selection: K/V insert + sparse GQA, "
+                    "no index keys, scoring or selection"}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_requests)
     return line
@@ -394,6 +437,8 @@ def main(argv=None):
                          "read a 512 MB buffer, or write one")
     ap.add_argument("--cpu-requests", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-layer-reuse", action="store_true",
+                    help="skip building a second layer for the selection-reuse timing")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -139,7 +139,10 @@ __device__ __forceinline__ ItemInfo load_item(const GqaParams& p, int64_t x, int
 
 // Counts this CTA's partial of a row: the ticket word holds (epoch << 32 | count)
 // and a count from another epoch is read as 0, so the workspace needs no
-// initialisation. Returns true for the CTA that delivers the last partial.
+// initialisation. Returns true for the CTA that delivers the last partial,
+// which also clears the word: no other CTA of this launch touches it again,
+// and a replay of a captured graph (whose epoch is fixed at capture) starts
+// from zero.
 __device__ bool ticket_is_last(const GqaParams& p, int64_t row, int nslots) {
   unsigned long long* t = p.tickets + row;
   unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(t);
@@ -147,7 +150,11 @@ __device__ bool ticket_is_last(const GqaParams& p, int64_t row, int nslots) {
     const uint32_t cnt = static_cast<uint32_t>(cur >> 32) == p.epoch ? static_cast<uint32_t>(cur) : 0u;
     const unsigned long long nw = (static_cast<unsigned long long>(p.epoch) << 32) | (cnt + 1u);
     const unsigned long long prev = atomicCAS(t, cur, nw);
-    if (prev == cur) return static_cast<int>(cnt + 1u) == nslots;
+    if (prev == cur) {
+      const bool last = static_cast<int>(cnt + 1u) == nslots;
+      if (last) atomicExch(t, 0ull);
+      return last;
+    }
     cur = prev;
   }
   set_flag(p.flags, MSA_FLAG_TIMEOUT);

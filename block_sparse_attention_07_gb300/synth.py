@@ -79,6 +79,10 @@ NVFP4_SYNTH_GLOBAL = 6.0 / (6.0 * 448.0)
 NVFP4_IDX_SYNTH_GLOBAL = 8.0 / (6.0 * 448.0)
 
 
+# Seed offset between the attention layers of one model (layer l uses seed + l * stride).
+LAYER_SEED_STRIDE = 7919
+
+
 def scaled(w: Workload, **changes) -> Workload:
     """A copy of a workload with some fields replaced (smaller parity cases)."""
     return dataclasses.replace(w, **changes)

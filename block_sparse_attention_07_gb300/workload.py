@@ -22,10 +22,14 @@ class DeviceWorkload:
 
     ``which`` restricts the batch to a subset of requests (keeping their
     seeded streams), so tests can run full-length requests of a large workload.
+    ``index_cache=False`` builds a layer without an index cache: one that reuses
+    another layer's block selection (``reuse_step``) and writes no index keys.
     """
 
-    def __init__(self, w: synth.Workload, device="cuda", which=None, lens=None, workers: int = 8):
+    def __init__(self, w: synth.Workload, device="cuda", which=None, lens=None, workers: int = 8,
+                 index_cache: bool = True):
         self.w = w
+        self.has_index = index_cache
         self.device = torch.device(device)
         full_lens = synth.seq_lens(w) if lens is None else np.asarray(lens, dtype=np.int32)
         self.which = list(range(w.batch)) if which is None else list(which)
@@ -47,7 +51,10 @@ class DeviceWorkload:
                                      torch.zeros((P, G, BS, D // 2), dtype=torch.uint8, device=dev),
                                      torch.zeros((P, G, BS, D // 16), dtype=torch.uint8, device=dev),
                                      torch.zeros((P, G, BS, D // 16), dtype=torch.uint8, device=dev), g, g)
-        if w.idx_dtype == "f32":
+        if not index_cache:
+            self.idx_cache = None
+            self.q_idx_dtype = self.idx_new_dtype = msa.BF16
+        elif w.idx_dtype == "f32":
             self.idx_cache = msa.IndexCache(msa.F32, torch.zeros((P, I, BS, D), dtype=torch.float32, device=dev))
             self.q_idx_dtype = msa.F32
             self.idx_new_dtype = msa.F32
@@ -85,7 +92,8 @@ class DeviceWorkload:
         self.q_idx = (torch.from_numpy(qi) if w.idx_dtype == "f32" else _bf16(qi)).to(dev)
         self.new_k = _bf16(new_k.reshape(B * Q, G, D)).to(dev)
         self.new_v = _bf16(new_v.reshape(B * Q, G, D)).to(dev)
-        self.new_idx = (torch.from_numpy(new_i) if w.idx_dtype == "f32" else _bf16(new_i)).reshape(B * Q, I, D).to(dev)
+        self.new_idx = ((torch.from_numpy(new_i) if w.idx_dtype == "f32" else _bf16(new_i)).reshape(B * Q, I, D).to(dev)
+                        if index_cache else None)
         self.new_slots = torch.from_numpy(new_slots.reshape(-1)).to(dev)
         self.scores = torch.empty((B, Q, I, nb), dtype=torch.float32, device=dev)
         self.selected = torch.empty((B, Q, I, w.topk), dtype=torch.int32, device=dev)
@@ -100,7 +108,9 @@ class DeviceWorkload:
         dev = self.device
         kd = _bf16(k).to(dev)
         vd = _bf16(v).to(dev)
-        idd = (torch.from_numpy(idx) if idx.dtype == np.float32 else _bf16(idx)).to(dev)
+        idd = None
+        if self.has_index:
+            idd = (torch.from_numpy(idx) if idx.dtype == np.float32 else _bf16(idx)).to(dev)
         sd = torch.from_numpy(slots).to(dev)
         msa.kv_insert_quant(self.dims, kd, vd, idd, self.idx_new_dtype, sd, self.cache, self.idx_cache, self.flags)
 
@@ -111,12 +121,14 @@ class DeviceWorkload:
             self._prep = dict(
                 insert=msa.kv_insert_quant(self.dims, self.new_k, self.new_v, self.new_idx, self.idx_new_dtype,
                                            self.new_slots, self.cache, self.idx_cache, self.flags, prepare=True),
-                index=msa.index_score(self.dims, self.q_idx, self.q_idx_dtype, self.idx_cache, self.block_table_d,
-                                      self.seq_lens_d, self.scores, self.flags, prepare=True),
-                select=msa.select_blocks(self.dims, self.scores, self.seq_lens_d, self.selected, self.flags,
-                                         prepare=True),
                 attend=msa.sparse_gqa_decode(self.dims, self.q, self.cache, self.block_table_d, self.seq_lens_d,
                                              self.selected, self.out, self.lse, self.workspace, self.flags,
+                                             prepare=True))
+            if self.has_index:
+                self._prep.update(
+                    index=msa.index_score(self.dims, self.q_idx, self.q_idx_dtype, self.idx_cache,
+                                          self.block_table_d, self.seq_lens_d, self.scores, self.flags, prepare=True),
+                    select=msa.select_blocks(self.dims, self.scores, self.seq_lens_d, self.selected, self.flags,
                                              prepare=True))
         return self._prep
 
@@ -150,6 +162,33 @@ class DeviceWorkload:
         self.index_score(stream)
         self.select(stream)
         self.attend(stream)
+
+    def reuse_step(self, selected, stream=None):
+        """One decode step of a layer that reuses another layer's selection
+        (logical block ids of the same requests): insert this step's K/V only,
+        then attend over ``selected``."""
+        msa.kv_insert_quant(self.dims, self.new_k, self.new_v, None, self.idx_new_dtype, self.new_slots,
+                            self.cache, None, self.flags, stream)
+        self.attend(stream if stream is not None else torch.cuda.current_stream(self.device), selected)
+
+    def capture(self, fn) -> torch.cuda.CUDAGraph:
+        """Captures ``fn(stream)`` (a step of this workload) into a CUDA graph;
+        ``graph.replay()`` then reruns its kernels with the same buffers."""
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize(self.device)
+        with torch.cuda.graph(g):
+            fn(torch.cuda.current_stream(self.device))
+        torch.cuda.synchronize(self.device)
+        return g
+
+    @classmethod
+    def layer_like(cls, src: "DeviceWorkload", layer: int, **kw) -> "DeviceWorkload":
+        """Another attention layer of the same requests (same lengths, own
+        seeded q/K/V, own caches), built without an index cache."""
+        w = synth.scaled(src.w, seed=src.w.seed + synth.LAYER_SEED_STRIDE * layer)
+        full = np.zeros(src.w.batch, dtype=np.int32)
+        full[src.which] = src.lens
+        return cls(w, src.device, which=src.which, lens=full, index_cache=False, **kw)
 
     def check_flags(self) -> int:
         return msa.read_device_flags(self.flags)

@@ -25,7 +25,15 @@
  *     allocates nothing and keeps no pointer after a call returns.
  *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL = the legacy default stream). Only msa_read_device_flags
- *     synchronises.
+ *     synchronises. The launching calls may be captured into a CUDA graph
+ *     (they allocate nothing, never synchronise and read no device memory on
+ *     the host); a replay reruns them with the captured arguments.
+ *   - Cross-layer selection reuse ("vLLM、AMD Instinct MI355X上で…", question 3:
+ *     adjacent sparse layers pick nearly the same blocks, so one layer's top-k
+ *     decision serves the layers after it, which also write no index keys):
+ *     a reusing layer calls msa_kv_insert_quant with idx_k_new = NULL and
+ *     msa_sparse_gqa_decode with the source layer's `selected` (logical block
+ *     ids, valid with the reusing layer's own block table).
  *   - Host-side validation runs before any launch. A status other than MSA_OK
  *     means nothing was launched (MSA_ERR_CUDA: a launch was attempted and the
  *     CUDA runtime reported an error).

@@ -1,0 +1,89 @@
+"""A whole decode step replayed from a CUDA graph, and a layer that reuses another
+layer's block selection.
+
+"vLLM、AMD Instinct MI355X上でMiniMax M3のボトルネック最適化手法を公開",
+question 2: graph execution removes the per-kernel launch cost; question 3:
+adjacent sparse layers pick nearly the same blocks, so one layer's top-k
+decision serves the next layers, which then write no index keys either.
+"""
+import numpy as np
+import pytest
+import torch
+
+from block_sparse_attention_07_gb300 import synth
+from block_sparse_attention_07_gb300.workload import DeviceWorkload
+from oracle import run as orun
+
+import parity
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+
+GRAPH_CASES = {
+    # bf16 KV: every CTA owns whole rows
+    "bf16": synth.scaled(W["b32_32k"], batch=3, ctx=2000),
+    # NVFP4 KV: rows split over CTAs and merged by the last arriver (tickets)
+    "nvfp4_split_rows": synth.scaled(W["nvfp4_256k"], batch=2, ctx=3000),
+    # NVFP4 index keys, 8 positions
+    "spec_fp4idx": synth.scaled(W["spec8"], batch=2, ctx=2600, idx_dtype="nvfp4"),
+}
+
+
+@pytest.mark.parametrize("name", list(GRAPH_CASES))
+def test_graph_replay_matches_eager_and_oracle(name):
+    w = GRAPH_CASES[name]
+    dw = parity.build(w)
+    dw.step()
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (dw.scores, dw.selected, dw.out, dw.lse)]
+    g = dw.capture(dw.step)
+    for _ in range(3):                      # replays reuse the captured split-K tickets
+        dw.scores.fill_(7.0)
+        dw.selected.fill_(-7)
+        dw.out.zero_()
+        dw.lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip((dw.scores, dw.selected, dw.out, dw.lse), eager):
+            assert torch.equal(a, b)
+    assert dw.check_flags() == 0
+    parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
+
+
+REUSE_CASES = {
+    "bf16": synth.scaled(W["b32_32k"], batch=2, ctx=2500),
+    "nvfp4": synth.scaled(W["nvfp4_256k"], batch=2, ctx=2200),
+    "spec8": synth.scaled(W["spec8"], batch=2, ctx=2100),
+}
+
+
+@pytest.mark.parametrize("name", list(REUSE_CASES))
+@pytest.mark.parametrize("graph", [False, True])
+def test_layer_reusing_selection(name, graph):
+    w = REUSE_CASES[name]
+    src = parity.build(w)
+    src.step()
+    layer = DeviceWorkload.layer_like(src, 1)
+    assert layer.idx_cache is None
+    if graph:
+        g = layer.capture(lambda st: layer.reuse_step(src.selected, st))
+        g.replay()
+        g.replay()
+    else:
+        layer.reuse_step(src.selected)
+    torch.cuda.synchronize()
+    assert layer.check_flags() == 0 and src.check_flags() == 0
+    sel = src.selected.cpu().numpy()
+    out = layer.out.float().cpu().numpy()
+    lse = layer.lse.cpu().numpy()
+    kg, vg = parity.nvfp4_globals(w)
+    lens = synth.seq_lens(w)
+    for bi, b in enumerate(layer.which):
+        L = int(lens[b])
+        req = synth.request(layer.w, b, L)          # the layer's own q, K, V
+        ora = orun.run_request(req, L, w.topk, w.softmax_scale, w.block_size, w.idx_dtype, w.kv_dtype, kg, vg,
+                               sel=sel[bi], idx_global=parity.idx_global(w))
+        parity.check_attention(out[bi], lse[bi], ora["out"], ora["lse"], f"{w.name} layer 1 b={b}")
+    # a different layer really attends over different data
+    assert not torch.equal(layer.out, src.out)
