@@ -21,6 +21,7 @@ blocks including the local one, at most 2,048 keys per query):
 * ``nvfp4_256k`` batch 16, 262,144 tokens, NVFP4 KV.
 * ``b32_32k_fp4idx`` and ``fp4_256k``: as ``b32_32k`` and ``nvfp4_256k`` with
   NVFP4 index keys.
+* ``fp8kv_32k``: as ``b32_32k`` with FP8 E4M3 K/V (one scale per tensor).
 """
 from __future__ import annotations
 
@@ -42,7 +43,7 @@ class Workload:
     ctx: int | None            # fixed context length, or None for ragged
     ctx_range: tuple | None    # (lo, hi) for ragged lengths
     idx_dtype: str             # "f32" (fp32 index keys/query), "fp8" or "nvfp4" (bf16 source, quantised cache)
-    kv_dtype: str              # "bf16" or "nvfp4"
+    kv_dtype: str              # "bf16", "fp8" or "nvfp4"
     planted: bool              # ragged recipe: 10 % of blocks offset by +2 sigma
     n_heads: int = 64
     n_kv_heads: int = 4
@@ -66,6 +67,8 @@ WORKLOADS = {
     # NVFP4 index keys (the indexer format of the NVFP4 checkpoint's serving recipe)
     "b32_32k_fp4idx": Workload("b32_32k_fp4idx", 32, 1, 32768, None, "nvfp4", "bf16", False, seed=20261207),
     "fp4_256k": Workload("fp4_256k", 16, 1, 262144, None, "nvfp4", "nvfp4", False, seed=20261208),
+    # FP8 E4M3 K/V with a per-tensor scale (the other published KV format)
+    "fp8kv_32k": Workload("fp8kv_32k", 32, 1, 32768, None, "fp8", "fp8", False, seed=20261209),
 }
 
 # Field ids of the per-request random streams.
@@ -77,6 +80,8 @@ _F_LEN, _F_PERM, _F_Q, _F_QIDX, _F_IDXK, _F_OFF, _F_K, _F_V, _F_PLANT = range(9)
 NVFP4_SYNTH_GLOBAL = 6.0 / (6.0 * 448.0)
 # Index keys carry block offsets on top of N(0,1); their calibration amax is 8.
 NVFP4_IDX_SYNTH_GLOBAL = 8.0 / (6.0 * 448.0)
+# FP8 K/V per-tensor scale: amax 6 over the largest E4M3 magnitude.
+FP8_KV_SYNTH_SCALE = 6.0 / 448.0
 
 
 # Seed offset between the attention layers of one model (layer l uses seed + l * stride).

@@ -18,6 +18,10 @@ quantisation formulas; the readings below are this project's:
   (token, KV head) row: sb = E4M3((amax16 / 6) / g); codes = E2M1(x / (sb * g));
   if sb decodes to 0 every code is 0. Nibble order: the low nibble holds the
   even element.
+* FP8 K/V ("MiniMax-M3.1-Flash Day-0 対応", section "何が新しいか": 61,440 bytes
+  per token over 60 layers, i.e. one byte per K and V value and no per-token
+  scale): one fp32 scale per tensor s (an input, like the NVFP4 global);
+  code = E4M3(x / s), saturating at +-448.
 * NVFP4 index keys: the same rule per (token, index head) row, with the index
   cache's own global scale (the pages name the format but not its rule:
   "MiniMax-M3.1-Flash Day-0 対応", section "何が新しいか" — the NVFP4 cache
@@ -47,6 +51,14 @@ def quant_index_keys_fp8(x: np.ndarray):
     codes = e4m3_encode(y)
     codes = np.where(scale[..., None] > 0, codes, np.uint8(0)).astype(np.uint8)
     return codes, scale
+
+
+def quant_kv_fp8(x: np.ndarray, scale: float) -> np.ndarray:
+    """[T, G, D] fp32 (or bf16-valued) -> E4M3 codes [T, G, D] uint8, value = code x scale."""
+    x = np.asarray(x, dtype=F32)
+    s = F32(scale)
+    y = (x / s).astype(F32)                               # one RN division per value
+    return e4m3_encode(y)
 
 
 def quant_nvfp4(x: np.ndarray, global_scale: float):

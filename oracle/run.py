@@ -55,6 +55,8 @@ def cached_kv_rows(x: np.ndarray, kv_dtype: str, global_scale: float) -> np.ndar
     f = to_f32(x)
     if kv_dtype == "bf16":
         return f.astype(np.float64)
+    if kv_dtype == "fp8":
+        return formats.e4m3_decode(quant.quant_kv_fp8(f, global_scale)) * float(np.float32(global_scale))
     codes, scales = quant.quant_nvfp4(f, global_scale)
     return formats.nvfp4_decode(codes, scales, global_scale)
 

@@ -115,6 +115,23 @@ def test_nvfp4_quant_properties():
     assert (err[ok] <= half[ok] + 1e-6).all()
 
 
+def test_fp8_kv_quant_matches_torch_and_saturates():
+    """E4M3 K/V with one scale per tensor: codes equal torch's float8_e4m3fn cast of
+    x / s inside the E4M3 range, and saturate to +-448 beyond it."""
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((300, 4, 128)) * 2.5).astype(np.float32)
+    x[0, 0, :4] = [7.0, -9.0, 6.5, -6.0001]                 # beyond the calibrated amax 6
+    s = np.float32(6.0 / 448.0)
+    codes = Qz.quant_kv_fp8(x, s)
+    assert codes.dtype == np.uint8 and codes.shape == x.shape
+    y = x / s
+    inr = np.abs(y) <= 448
+    ref = torch.from_numpy(np.ascontiguousarray(y)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes[inr], ref[inr])
+    dec = F.e4m3_decode(codes)
+    assert (~inr).sum() > 4 and np.array_equal(dec[~inr], np.sign(y[~inr]) * 448.0)
+
+
 def test_kv_byte_counts_match_pages():
     """576 bytes/token/layer NVFP4 (x60 = 34,560) and 1,024 FP8 (x60 = 61,440)."""
     c = load_golden("page_constants.json")
@@ -122,7 +139,7 @@ def test_kv_byte_counts_match_pages():
     x = np.zeros((1, G, D), dtype=np.float32)
     packed, sc = Qz.quant_nvfp4(x, 1.0)
     per_layer_nvfp4 = 2 * (packed.nbytes + sc.nbytes)          # K and V
-    per_layer_fp8 = 2 * G * D * 1
+    per_layer_fp8 = 2 * Qz.quant_kv_fp8(x, 1.0).nbytes           # K and V
     assert per_layer_nvfp4 * c["layers"] == c["nvfp4_kv_bytes_per_token_all_layers"]
     assert per_layer_fp8 * c["layers"] == c["fp8_kv_bytes_per_token_all_layers"]
     saving = 100 * (1 - per_layer_nvfp4 / per_layer_fp8)

@@ -254,3 +254,23 @@ def test_nvfp4_index_keys_exact_when_representable():
     ell = (L - 1) // BS
     want = np.einsum("id,tid->it", qi[0], keys[: ell * BS]).reshape(I, ell, BS).max(-1)
     np.testing.assert_allclose(S[0, :, :ell], want, rtol=1e-13)
+
+
+def test_fp8_kv_cache_exact_when_representable():
+    """K/V values that are E4M3 codes times a power-of-two tensor scale are stored
+    exactly, so a request on an FP8 cache equals the same request on a bf16 cache."""
+    from oracle import formats as F
+    from oracle import run as orun
+    from block_sparse_attention_07_gb300 import synth
+    w = synth.scaled(synth.WORKLOADS["tiny"], batch=1, ctx=700)
+    req = synth.request(w, 0, 700)
+    rng = np.random.default_rng(23)
+    s = 2.0 ** -5
+    for f in ("k", "v"):
+        codes = rng.integers(0, 256, req[f].shape).astype(np.uint8)
+        codes[(codes & 0x7F) == 0x7F] = 0                           # no NaN codes
+        req[f] = synth.f32_to_bf16_bits((F.e4m3_decode(codes) * s).astype(np.float32))
+    a = orun.run_request(req, 700, w.topk, w.softmax_scale, w.block_size, w.idx_dtype, "bf16")
+    b = orun.run_request(req, 700, w.topk, w.softmax_scale, w.block_size, w.idx_dtype, "fp8", s, s)
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["lse"], b["lse"])
+    assert np.array_equal(orun.cached_kv_rows(req["k"], "fp8", s), orun.to_f32(req["k"]).astype(np.float64))
