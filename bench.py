@@ -168,7 +168,8 @@ def attention_bytes(dw, sel):
     """Algorithmic bytes of one sparse-GQA launch: the union over positions of the
     selected blocks' K and V for each (request, KV head), plus q and out."""
     w = dw.w
-    per_tok = 2 * w.head_dim * 2 if w.kv_dtype == "bf16" else 2 * (w.head_dim // 2 + w.head_dim // 16)
+    per_tok = {"bf16": 2 * w.head_dim * 2, "fp8": 2 * w.head_dim,
+               "nvfp4": 2 * (w.head_dim // 2 + w.head_dim // 16)}[w.kv_dtype]
     total = 0
     for bi in range(sel.shape[0]):
         L = int(dw.lens[bi])
@@ -371,7 +372,7 @@ def cpu_baseline(w, n_requests, budget_s=20.0):
     from block_sparse_attention_07_gb300 import synth
     from oracle import run as orun
     lens = synth.seq_lens(w)
-    kg = kv = float(np.float32(synth.NVFP4_SYNTH_GLOBAL)) if w.kv_dtype == "nvfp4" else 1.0
+    kg = kv = synth.kv_scale(w)
     idx_g = float(np.float32(synth.NVFP4_IDX_SYNTH_GLOBAL)) if w.idx_dtype == "nvfp4" else 1.0
     spent, done = 0.0, 0
     for b in range(min(n_requests, w.batch)):
@@ -395,7 +396,7 @@ def run_reference(args, world, rank):
         return None
     w = synth.WORKLOADS[args.workload]
     lens = synth.seq_lens(w)
-    kg = kv = float(np.float32(synth.NVFP4_SYNTH_GLOBAL)) if w.kv_dtype == "nvfp4" else 1.0
+    kg = kv = synth.kv_scale(w)
     idx_g = float(np.float32(synth.NVFP4_IDX_SYNTH_GLOBAL)) if w.idx_dtype == "nvfp4" else 1.0
     reqs = {}
 

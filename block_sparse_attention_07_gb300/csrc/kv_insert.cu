@@ -1,4 +1,5 @@
-// Cache insertion and quantisation: writes new tokens' K/V (bf16 copy or NVFP4)
+// Cache insertion and quantisation: writes new tokens' K/V (bf16 copy, FP8 E4M3
+// with a per-tensor scale, or NVFP4)
 // and index keys (fp32 copy or FP8 E4M3 + per-token scale) into the paged
 // caches. One warp per (token, head); every step of the quantisers is an IEEE
 // round-to-nearest fp32 operation so the bytes are a pure function of the input.
@@ -15,6 +16,7 @@ struct InsertParams {
   int T, G;
   int64_t num_slots;          // P * BS
   int kv_nvfp4;
+  int kv_fp8;
   void* k; void* v;           // caches
   uint8_t* k_scale; uint8_t* v_scale;
   float k_global, v_global;
@@ -76,7 +78,20 @@ __global__ void __launch_bounds__(256) kv_insert_kernel(InsertParams p) {
     const int64_t row = (page * p.G + h) * kBlock + off;   // (page, head, offset) row of any [P, G, BS, ...] cache
     const int64_t src = (static_cast<int64_t>(t) * p.G + h) * kDim;
 
-    if (!p.kv_nvfp4) {
+    if (p.kv_fp8) {
+      // code = E4M3_RNE_satfinite(x / s), one fp32 RN division per value
+      const uint2 kk = *reinterpret_cast<const uint2*>(p.k_new + src + 4 * lane);
+      const uint2 vv = *reinterpret_cast<const uint2*>(p.v_new + src + 4 * lane);
+      auto enc = [](uint2 raw, float s) -> uint32_t {
+        const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(bf16_bits_to_f32(raw.x & 0xFFFF), s),
+                                            __fdiv_rn(bf16_bits_to_f32(raw.x >> 16), s));
+        const uint16_t hi = f32x2_to_e4m3x2(__fdiv_rn(bf16_bits_to_f32(raw.y & 0xFFFF), s),
+                                            __fdiv_rn(bf16_bits_to_f32(raw.y >> 16), s));
+        return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+      };
+      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.k) + row * kDim + 4 * lane) = enc(kk, p.k_global);
+      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.v) + row * kDim + 4 * lane) = enc(vv, p.v_global);
+    } else if (!p.kv_nvfp4) {
       const uint2 kk = *reinterpret_cast<const uint2*>(p.k_new + src + 4 * lane);
       const uint2 vv = *reinterpret_cast<const uint2*>(p.v_new + src + 4 * lane);
       *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.k) + row * kDim + 4 * lane) = kk;
@@ -133,6 +148,7 @@ cudaError_t launch_kv_insert(const InsertArgs& a, cudaStream_t stream, DispatchR
   p.G = a.G;
   p.num_slots = a.num_slots;
   p.kv_nvfp4 = a.kv_nvfp4;
+  p.kv_fp8 = a.kv_fp8;
   p.k = a.k; p.v = a.v;
   p.k_scale = static_cast<uint8_t*>(a.k_scale);
   p.v_scale = static_cast<uint8_t*>(a.v_scale);
@@ -151,7 +167,7 @@ cudaError_t launch_kv_insert(const InsertArgs& a, cudaStream_t stream, DispatchR
   if (blocks < 1) blocks = 1;
   const cudaError_t err = launch_pdl(kv_insert_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
   if (err != cudaSuccess) return err;
-  rec->set("kv_insert %s%s grid=%lld block=256 tokens=%d", a.kv_nvfp4 ? "nvfp4" : "bf16",
+  rec->set("kv_insert %s%s grid=%lld block=256 tokens=%d", a.kv_nvfp4 ? "nvfp4" : a.kv_fp8 ? "fp8" : "bf16",
            a.idx_new ? (a.idx_fp4 ? "+idx_nvfp4" : a.idx_fp8 ? "+idx_fp8" : "+idx_f32") : "",
            static_cast<long long>(blocks), a.T);
   return cudaGetLastError();

@@ -91,6 +91,11 @@ msa_status_t msa_kv_insert_quant(const msa_dims_t* dims, const void* k_new, cons
         cache->v_global > 3.0e38f)
       return MSA_ERR_INVALID_ARG;
     a.kv_nvfp4 = 1;
+  } else if (cache->dtype == MSA_FP8_E4M3) {
+    if (!(cache->k_global > 0.f) || !(cache->v_global > 0.f) || cache->k_global > 3.0e38f ||
+        cache->v_global > 3.0e38f)
+      return MSA_ERR_INVALID_ARG;
+    a.kv_fp8 = 1;
   } else if (cache->dtype != MSA_BF16) {
     return MSA_ERR_UNSUPPORTED;
   }
@@ -214,6 +219,11 @@ msa_status_t msa_sparse_gqa_decode(const msa_dims_t* dims, const void* q, const 
       return MSA_ERR_INVALID_ARG;
     if (!(cache->k_global > 0.f) || !(cache->v_global > 0.f)) return MSA_ERR_INVALID_ARG;
     a.nvfp4 = 1;
+  } else if (cache->dtype == MSA_FP8_E4M3) {
+    if (!(cache->k_global > 0.f) || !(cache->v_global > 0.f) || cache->k_global > 3.0e38f ||
+        cache->v_global > 3.0e38f)
+      return MSA_ERR_INVALID_ARG;
+    a.fp8 = 1;
   } else if (cache->dtype != MSA_BF16) {
     return MSA_ERR_UNSUPPORTED;
   }

@@ -52,6 +52,7 @@ struct InsertArgs {
   int T, G;
   int64_t num_slots;
   int kv_nvfp4;
+  int kv_fp8;
   void* k;
   void* v;
   void* k_scale;
@@ -90,7 +91,8 @@ struct SelectArgs {
 struct GqaArgs {
   const uint16_t* q;       // bf16 [B, Q, H, D]
   int nvfp4;
-  const void* k;           // bf16 [P, G, BS, D] or u8 [P, G, BS, D/2]
+  int fp8;
+  const void* k;           // bf16 [P, G, BS, D], u8 E4M3 [P, G, BS, D] or u8 [P, G, BS, D/2]
   const void* v;
   const uint8_t* k_scale;  // nvfp4 [P, G, BS, D/16]
   const uint8_t* v_scale;

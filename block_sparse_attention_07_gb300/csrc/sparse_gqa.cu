@@ -28,8 +28,10 @@
 
 namespace msa {
 
-template <bool kFp4>
-constexpr int stages_for() { return kFp4 ? 6 : 3; }   // 64 KB bf16 pages / 18 KB NVFP4 pages
+// K/V cache formats (template argument of the kernel).
+constexpr int kKvBf16 = 0, kKvNvfp4 = 1, kKvFp8 = 2;
+template <int kKv>
+constexpr int stages_for() { return kKv == kKvBf16 ? 3 : 6; }   // 64 KB bf16 / 32 KB FP8 / 18 KB NVFP4 pages
 constexpr int kTokPerWarp = 32;                  // tokens of every block that one consumer warp owns
 constexpr int kCWarps = kBlock / kTokPerWarp;    // consumer warps (one per SM sub-partition)
 constexpr int kNT = kTokPerWarp / 8;             // QK^T n-tiles of 8 tokens per warp
@@ -39,6 +41,12 @@ constexpr int kLanesPerRow = 32 / kTokPerWarp;   // NVFP4 expansion: lanes per t
 constexpr int kBoxBytes = kBlock * 64 * 2;       // 128 rows x 128 B (64 fp16/bf16)
 constexpr int kTileBytes = 4 * kBoxBytes;        // K lo/hi + V lo/hi = 64 KB
 constexpr int kFp4StageBytes = 2 * (kBlock * kDim / 2 + kBlock * kDim / 16);  // 18 KB
+constexpr int kFp8BoxBytes = kBlock * kDim;      // 128 rows x 128 E4M3 codes
+constexpr int kFp8StageBytes = 2 * kFp8BoxBytes; // K + V = 32 KB
+template <int kKv>
+constexpr uint32_t stage_bytes_for() {
+  return kKv == kKvBf16 ? kTileBytes : kKv == kKvFp8 ? kFp8StageBytes : kFp4StageBytes;
+}
 constexpr uint32_t kAll = 0xffffffffu;
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kRescaleSlack = 8.f;    // log2 units: probabilities below 256 before normalisation
@@ -70,16 +78,15 @@ struct SmemLayout {
   uint32_t total;
 };
 
-template <bool kFp4>
+template <int kKv>
 __host__ __device__ constexpr SmemLayout gqa_layout() {
   SmemLayout s{};
   s.stages = 0;
-  const uint32_t stage_bytes = kFp4 ? kFp4StageBytes : kTileBytes;
-  s.tiles = s.stages + stages_for<kFp4>() * stage_bytes;
-  s.comb_o = s.tiles + (kFp4 ? kTileBytes : 0);
+  s.tiles = s.stages + stages_for<kKv>() * stage_bytes_for<kKv>();
+  s.comb_o = s.tiles + (kKv == kKvNvfp4 ? kTileBytes : 0);
   s.comb_ml = s.comb_o + kCombWarps * kGroup * kDim * 4;
   s.bars = s.comb_ml + kCombWarps * kGroup * 2 * 4;
-  s.total = s.bars + (2 * stages_for<kFp4>() + 3) * 8 + 16;   // + the last-arriver flag
+  s.total = s.bars + (2 * stages_for<kKv>() + 3) * 8 + 16;   // + the last-arriver flag
   return s;
 }
 
@@ -174,13 +181,15 @@ __device__ __forceinline__ uint32_t swz(uint32_t box, int row, int chunk) {
   return box + row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
-template <bool kFp4>
+template <int kKv>
 __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     sparse_gqa_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, GqaParams p) {
   extern __shared__ uint8_t smem_raw[];
-  constexpr SmemLayout Ly = gqa_layout<kFp4>();
-  constexpr uint32_t kStageBytes = kFp4 ? kFp4StageBytes : kTileBytes;
-  constexpr int kGqaStages = stages_for<kFp4>();
+  constexpr bool kFp4 = kKv == kKvNvfp4, kFp8 = kKv == kKvFp8;
+  static_assert(!kFp8 || kNT == 4, "the FP8 fragment loads take 4 n-tiles per ldmatrix.x4");
+  constexpr SmemLayout Ly = gqa_layout<kKv>();
+  constexpr uint32_t kStageBytes = stage_bytes_for<kKv>();
+  constexpr int kGqaStages = stages_for<kKv>();
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base_addr = (raw + 1023u) & ~1023u;
   uint8_t* sm = smem_raw + (base_addr - raw);
@@ -249,7 +258,11 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
             const uint32_t dst = base_addr + Ly.stages + s * kStageBytes;
             const int64_t ph = static_cast<int64_t>(page) * p.G + g;   // (page, kv head) slab
             mbar_arrive_expect_tx(fb, kStageBytes);
-            if (!kFp4) {
+            if (kFp8) {
+              const int y = static_cast<int>(ph * kBlock);
+              tma_load_2d(dst, &tk, 0, y, fb);
+              tma_load_2d(dst + kFp8BoxBytes, &tv, 0, y, fb);
+            } else if (!kFp4) {
               const int y = static_cast<int>(ph * kBlock);
               tma_load_2d(dst, &tk, 0, y, fb);
               tma_load_2d(dst + kBoxBytes, &tk, 64, y, fb);
@@ -301,17 +314,25 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     seg_ell = seg_p / kBlock;
     const uint16_t* qh = p.q + ((static_cast<int64_t>(rp.b) * p.Q + rp.j) * p.H + static_cast<int64_t>(rp.g) * kGroup) * kDim;
     // The bf16 query words are the mma A fragments as loaded: qf[s] holds rows
-    // gr / gr + 8 at dims 16 s + 2 c (+1) and 16 s + 8 + 2 c (+1).
+    // gr / gr + 8 at dims 16 s + 2 c (+1) and 16 s + 8 + 2 c (+1). With FP8
+    // keys the k-slots of step s are dims 16 s + 4 c .. 16 s + 4 c + 3 instead
+    // (the four bytes one ldmatrix lane receives of a key row).
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const uint16_t* row = qh + (gr + 8 * r) * kDim + 16 * s + 2 * c;
-        qf[s][r] = *reinterpret_cast<const uint32_t*>(row);
-        qf[s][2 + r] = *reinterpret_cast<const uint32_t*>(row + 8);
+        if (kFp8) {
+          const uint2 wq = *reinterpret_cast<const uint2*>(qh + (gr + 8 * r) * kDim + 16 * s + 4 * c);
+          qf[s][r] = wq.x;
+          qf[s][2 + r] = wq.y;
+        } else {
+          const uint16_t* row = qh + (gr + 8 * r) * kDim + 16 * s + 2 * c;
+          qf[s][r] = *reinterpret_cast<const uint32_t*>(row);
+          qf[s][2 + r] = *reinterpret_cast<const uint32_t*>(row + 8);
+        }
       }
     }
-    if (kFp4) {
+    if (kFp4 || kFp8) {
       // fp16 operands: rescale each query row by an exact power of two that
       // keeps it inside the fp16 range; the logit multiplier undoes it.
 #pragma unroll
@@ -353,8 +374,19 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     float* mo = comb_o + k * kGroup * kDim;
 #pragma unroll
     for (int n = 0; n < 16; ++n) {
-      *reinterpret_cast<float2*>(mo + gr * kDim + 8 * n + 2 * c) = make_float2(o[n][0], o[n][1]);
-      *reinterpret_cast<float2*>(mo + (gr + 8) * kDim + 8 * n + 2 * c) = make_float2(o[n][2], o[n][3]);
+      if (kFp8) {
+        // n-tile n holds the even (n even) or odd dims of chunk n / 2: column
+        // 2 c + e is dim 16 (n / 2) + 4 c + 2 e + (n & 1)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int d = 16 * (n >> 1) + 4 * c + 2 * e + (n & 1);
+          mo[gr * kDim + d] = o[n][e];
+          mo[(gr + 8) * kDim + d] = o[n][2 + e];
+        }
+      } else {
+        *reinterpret_cast<float2*>(mo + gr * kDim + 8 * n + 2 * c) = make_float2(o[n][0], o[n][1]);
+        *reinterpret_cast<float2*>(mo + (gr + 8) * kDim + 8 * n + 2 * c) = make_float2(o[n][2], o[n][3]);
+      }
     }
     if (c == 0) {
       comb_m[k * kGroup + gr] = m_r[0];
@@ -421,7 +453,7 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
         float v = 0.f;
 #pragma unroll
         for (int k = 0; k < kCombWarps; ++k) v += fw[k] * comb_o[(k * kGroup + hh) * kDim + d0 + d];
-        acc[d] = v * (kFp4 ? p.v_global : 1.f);
+        acc[d] = v * ((kFp4 || kFp8) ? p.v_global : 1.f);
       }
     }
     const int64_t r = seg_row;
@@ -507,7 +539,28 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
   for (int h = 0; h < 4; ++h)
     v_off[h] = warp_rows + (8 * ((lane >> 3) & 1) + (lane & 7)) * 128u + ((((2 * h) + (lane >> 4)) ^ (lane & 7)) << 4);
 
+  const uint32_t lane_x = (lane & 7) << 4;     // FP8 tiles: XOR of the 128-byte swizzle for this lane's rows
+  const uint32_t k8_row = (static_cast<uint32_t>(kTokPerWarp * w) + 8u * (lane >> 3) + (lane & 7)) * 128u;
+  const uint32_t v8_row = (static_cast<uint32_t>(kTokPerWarp * w) + 8u * ((lane >> 3) & 1) + (lane & 7)) * 128u;
+
   auto qk = [&](uint32_t kt, float (&sc)[kNT][4]) {
+    if (kFp8) {
+      // FP8 K: one ldmatrix.x4 per 16-dim chunk q gives lane (gr, c) the codes
+      // of dims 16 q + 4 c .. + 3 of token row gr of each of the 4 n-tiles
+      // (matrix m = n-tile m); two exact cvts make its b0 / b1 fragments.
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        uint32_t r[4];
+        ldsm_x4(kt + k8_row + ((static_cast<uint32_t>(q) << 4) ^ lane_x), r[0], r[1], r[2], r[3]);
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+          mma_f16(sc[nt], qf[q], e4m3x2_to_f16x2(static_cast<uint16_t>(r[nt] & 0xFFFF)),
+                  e4m3x2_to_f16x2(static_cast<uint16_t>(r[nt] >> 16)));
+      }
+      return;
+    }
     // ---- S = Q K^T for this warp's tokens (kNT n-tiles of 8 tokens). The
     // n-tiles are independent accumulation chains, interleaved per pair of
     // k-steps so that the mma latencies overlap.
@@ -600,7 +653,7 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
 #pragma unroll
     for (int kk = 0; kk < kKK; ++kk) {
       uint32_t a[4];
-      if (kFp4) {
+      if (kFp4 || kFp8) {
         a[0] = pack_f16x2(pr[2 * kk][0], pr[2 * kk][1]);
         a[1] = pack_f16x2(pr[2 * kk][2], pr[2 * kk][3]);
         a[2] = pack_f16x2(pr[2 * kk + 1][0], pr[2 * kk + 1][1]);
@@ -610,6 +663,30 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
         a[1] = pack_bf16x2(pr[2 * kk][2], pr[2 * kk][3]);
         a[2] = pack_bf16x2(pr[2 * kk + 1][0], pr[2 * kk + 1][1]);
         a[3] = pack_bf16x2(pr[2 * kk + 1][2], pr[2 * kk + 1][3]);
+      }
+      if (kFp8) {
+        // FP8 V: one ldmatrix.x4.trans per chunk pair (matrices: tokens 0-7 and
+        // 8-15 of the k-step, for chunks 2 qp and 2 qp + 1) gives lane (gr, c)
+        // tokens 2c, 2c+1 of dims 2 gr, 2 gr + 1 of a chunk; a byte permute
+        // pairs the two tokens of each dim, and exact cvts make the fragments
+        // of the chunk's even-dim (n-tile 2 chunk) and odd-dim (2 chunk + 1)
+        // n-tiles.
+        const uint32_t vt = kt + kFp8BoxBytes + kk * 16 * 128 + v8_row;
+#pragma unroll
+        for (int qp = 0; qp < 4; ++qp) {
+          uint32_t v[4];
+          ldsm_x4_t(vt + (((static_cast<uint32_t>(2 * qp) + (lane >> 4)) << 4) ^ lane_x), v[0], v[1], v[2], v[3]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t t0 = __byte_perm(v[2 * h], 0, 0x3120), t1 = __byte_perm(v[2 * h + 1], 0, 0x3120);
+            const int n = 2 * (2 * qp + h);
+            mma_f16(o[n], a, e4m3x2_to_f16x2(static_cast<uint16_t>(t0 & 0xFFFF)),
+                    e4m3x2_to_f16x2(static_cast<uint16_t>(t1 & 0xFFFF)));
+            mma_f16(o[n + 1], a, e4m3x2_to_f16x2(static_cast<uint16_t>(t0 >> 16)),
+                    e4m3x2_to_f16x2(static_cast<uint16_t>(t1 >> 16)));
+          }
+        }
+        continue;
       }
 #pragma unroll
       for (int np = 0; np < 8; ++np) {
@@ -747,15 +824,17 @@ static EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// 2-D map over a bf16 cache [P*G*BS rows, 128 dims]; 128-row x 64-dim boxes, 128 B swizzle.
-static cudaError_t make_kv_map(CUtensorMap* map, const void* base, int64_t rows) {
+// 2-D map over a cache [P*G*BS rows, 128 dims] with 128-row boxes of 128 bytes
+// and 128 B swizzle: bf16 (64-dim boxes, two per row) or FP8 codes (one box).
+static cudaError_t make_kv_map(CUtensorMap* map, const void* base, int64_t rows, bool fp8) {
   EncodeTiledFn fn = encode_tiled();
   if (fn == nullptr) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlock)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim) * (fp8 ? 1 : 2)};
+  const cuuint32_t box[2] = {fp8 ? 128u : 64u, static_cast<cuuint32_t>(kBlock)};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  const CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -790,11 +869,11 @@ cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRec
   const int64_t cache_rows = static_cast<int64_t>(a.P) * a.G * kBlock;
   cudaError_t err;
   if (!a.nvfp4) {
-    if ((err = make_kv_map(&tk, a.k, cache_rows)) != cudaSuccess) return err;
-    if ((err = make_kv_map(&tv, a.v, cache_rows)) != cudaSuccess) return err;
+    if ((err = make_kv_map(&tk, a.k, cache_rows, a.fp8 != 0)) != cudaSuccess) return err;
+    if ((err = make_kv_map(&tv, a.v, cache_rows, a.fp8 != 0)) != cudaSuccess) return err;
   }
-  // Work split. bf16 pages (64 KB per block) stream best when every CTA owns
-  // whole rows: no split-K partials, no merge. NVFP4 pages (18 KB) are latency
+  // Work split. bf16 and FP8 pages (64 / 32 KB per block) stream best when
+  // every CTA owns whole rows: no split-K partials, no merge. NVFP4 pages (18 KB) are latency
   // bound per block, so their item ranges are balanced exactly over all SMs
   // and the CTAs that share a row merge through the workspace.
   const int sms = device_sm_count();
@@ -807,18 +886,21 @@ cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRec
     p.row_aligned = 0;
     C = static_cast<int>(p.W < sms ? p.W : sms);
   }
-  const size_t smem = (a.nvfp4 ? gqa_layout<true>().total : gqa_layout<false>().total) + 1024;
+  const size_t smem = (a.nvfp4 ? gqa_layout<kKvNvfp4>().total
+                               : a.fp8 ? gqa_layout<kKvFp8>().total : gqa_layout<kKvBf16>().total) + 1024;
   static std::atomic<uint32_t> epoch{1};
   p.epoch = epoch.fetch_add(1);
   if (p.epoch == 0) p.epoch = epoch.fetch_add(1);    // 0 never tags a ticket
   p.tickets = reinterpret_cast<unsigned long long*>(a.workspace + (p.W / p.K) * p.K * kPartialFloats);
-  auto kern = a.nvfp4 ? sparse_gqa_kernel<true> : sparse_gqa_kernel<false>;
+  auto kern = a.nvfp4 ? sparse_gqa_kernel<kKvNvfp4> : a.fp8 ? sparse_gqa_kernel<kKvFp8> : sparse_gqa_kernel<kKvBf16>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   err = launch_pdl(kern, dim3(C), dim3(32 * (1 + kCWarps)), smem, stream, tk, tv, p);
   rec->set("sparse_gqa %s persistent %s grid=%d block=%d smem=%zu stages=%d items=%lld",
-           a.nvfp4 ? "nvfp4_dequant_f16_mma" : "bf16_tma_mma", p.row_aligned ? "whole_rows" : "split_k_fused_combine",
-           C, 32 * (1 + kCWarps), smem, a.nvfp4 ? stages_for<true>() : stages_for<false>(), static_cast<long long>(p.W));
+           a.nvfp4 ? "nvfp4_dequant_f16_mma" : a.fp8 ? "fp8_tma_cvt_f16_mma" : "bf16_tma_mma",
+           p.row_aligned ? "whole_rows" : "split_k_fused_combine", C, 32 * (1 + kCWarps), smem,
+           a.nvfp4 ? stages_for<kKvNvfp4>() : a.fp8 ? stages_for<kKvFp8>() : stages_for<kKvBf16>(),
+           static_cast<long long>(p.W));
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 

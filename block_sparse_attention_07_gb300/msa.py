@@ -120,7 +120,8 @@ def make_dims(batch, q_len, n_heads=64, n_kv_heads=4, n_idx_heads=4, head_dim=12
 
 @dataclasses.dataclass
 class KVCache:
-    """bf16: k, v [P, G, BS, D]. NVFP4: k, v uint8 [P, G, BS, D/2], k_scale, v_scale uint8 [P, G, BS, D/16]."""
+    """bf16: k, v [P, G, BS, D]. FP8_E4M3: k, v uint8 E4M3 [P, G, BS, D], k_global / v_global the
+    per-tensor scales. NVFP4: k, v uint8 [P, G, BS, D/2], k_scale, v_scale uint8 [P, G, BS, D/16]."""
     dtype: int
     k: object
     v: object

@@ -88,6 +88,12 @@ FP8_KV_SYNTH_SCALE = 6.0 / 448.0
 LAYER_SEED_STRIDE = 7919
 
 
+def kv_scale(w: Workload) -> float:
+    """The per-tensor K/V scale of the workload's cache format (fp32 value)."""
+    s = {"bf16": 1.0, "fp8": FP8_KV_SYNTH_SCALE, "nvfp4": NVFP4_SYNTH_GLOBAL}[w.kv_dtype]
+    return float(np.float32(s))
+
+
 def scaled(w: Workload, **changes) -> Workload:
     """A copy of a workload with some fields replaced (smaller parity cases)."""
     return dataclasses.replace(w, **changes)

@@ -45,8 +45,12 @@ class DeviceWorkload:
         if w.kv_dtype == "bf16":
             self.cache = msa.KVCache(msa.BF16, torch.zeros((P, G, BS, D), dtype=torch.bfloat16, device=dev),
                                      torch.zeros((P, G, BS, D), dtype=torch.bfloat16, device=dev))
+        elif w.kv_dtype == "fp8":
+            s = synth.kv_scale(w)
+            self.cache = msa.KVCache(msa.FP8_E4M3, torch.zeros((P, G, BS, D), dtype=torch.uint8, device=dev),
+                                     torch.zeros((P, G, BS, D), dtype=torch.uint8, device=dev), None, None, s, s)
         else:
-            g = float(np.float32(synth.NVFP4_SYNTH_GLOBAL))
+            g = synth.kv_scale(w)
             self.cache = msa.KVCache(msa.NVFP4, torch.zeros((P, G, BS, D // 2), dtype=torch.uint8, device=dev),
                                      torch.zeros((P, G, BS, D // 2), dtype=torch.uint8, device=dev),
                                      torch.zeros((P, G, BS, D // 16), dtype=torch.uint8, device=dev),

@@ -106,6 +106,10 @@ typedef struct {
 
 /* Paged K/V cache of one layer (host struct holding device pointers).
  *   MSA_BF16:  k, v  = bf16 [P, G, BS, D]; k_scale = v_scale = NULL.
+ *   MSA_FP8_E4M3: k, v = uint8 E4M3 codes [P, G, BS, D]; k_global, v_global =
+ *              fp32 per-tensor scales (host values, > 0); value = e4m3 * global
+ *              (61,440 bytes per token over 60 layers: "MiniMax-M3.1-Flash
+ *              Day-0 対応", section "何が新しいか"); k_scale = v_scale = NULL.
  *   MSA_NVFP4: k, v  = uint8 [P, G, BS, D/2] E2M1 pairs, low nibble = even
  *              element; k_scale, v_scale = uint8 E4M3 [P, G, BS, D/16], one
  *              per 16 consecutive elements; k_global, v_global = fp32
@@ -158,6 +162,7 @@ msa_status_t msa_get_last_dispatch(char* buf, size_t len);
  *     IEEE division), code = E4M3_RNE_satfinite(x / s); s = 0 -> codes 0.
  *   NVFP4 K/V and NVFP4 index keys: per 16 values sb = E4M3_RNE((amax16 / 6) /
  *     global), code = E2M1_RNE_satfinite(x / (sb * global)); sb == 0 -> codes 0.
+ *   FP8 K/V: code = E4M3_RNE_satfinite(x / global) (fp32 IEEE division).
  *   bf16 K/V and fp32 index keys are copied.
  * k_new, v_new: bf16 [T, G, D]. idx_k_new: [T, I, D] of idx_new_dtype
  * (MSA_F32 or MSA_BF16; MSA_BF16 requires an FP8 or NVFP4 index cache), or NULL to

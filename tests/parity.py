@@ -105,9 +105,10 @@ def check_attention(gpu_out, gpu_lse, ora_out, ora_lse, where="", heads=None):
         assert le.max() <= LSE_ABS, f"{where}: lse max-abs {le.max():.3g}"
 
 
-def nvfp4_globals(w):
-    g = float(np.float32(synth.NVFP4_SYNTH_GLOBAL))
-    return (g, g) if w.kv_dtype == "nvfp4" else (1.0, 1.0)
+def kv_globals(w):
+    """Per-tensor K/V scales of the workload's cache (1 for bf16)."""
+    s = synth.kv_scale(w)
+    return s, s
 
 
 def verify_workload(dw, w, full_lens, sample=None, heads=None, run_step=True):
@@ -121,7 +122,7 @@ def verify_workload(dw, w, full_lens, sample=None, heads=None, run_step=True):
     sel = dw.selected.cpu().numpy()
     out = dw.out.float().cpu().numpy()
     lse = dw.lse.cpu().numpy()
-    kg, vg = nvfp4_globals(w)
+    kg, vg = kv_globals(w)
     idx = range(len(dw.which)) if sample is None else sample
     for bi in idx:
         b = dw.which[bi]

@@ -89,6 +89,19 @@ def test_dtype_combinations_rejected(m):
     st = m.lib.msa_kv_insert_quant(ctypes.byref(d), fake, fake, None, m.F32, fake, 4, ctypes.byref(kv), None,
                                    fake, None)
     assert st == m.ERR_INVALID_ARG
+    for ks, vs in ((0.0, 1.0), (1.0, -2.0), (float("nan"), 1.0)):    # FP8 K/V: per-tensor scales > 0
+        kv = m._KVCache(m.FP8_E4M3, fake, fake, None, None, ks, vs)
+        st = m.lib.msa_kv_insert_quant(ctypes.byref(d), fake, fake, None, m.F32, fake, 4, ctypes.byref(kv), None,
+                                       fake, None)
+        assert st == m.ERR_INVALID_ARG
+        need = m.lib.msa_sparse_gqa_workspace_size(ctypes.byref(d), m.FP8_E4M3)
+        st = m.lib.msa_sparse_gqa_decode(ctypes.byref(d), fake, ctypes.byref(kv), fake, fake, fake, fake, None,
+                                         fake, need, fake, None)
+        assert st == m.ERR_INVALID_ARG
+    kv = m._KVCache(m.F32, fake, fake, None, None, 1.0, 1.0)         # no fp32 K/V cache
+    st = m.lib.msa_kv_insert_quant(ctypes.byref(d), fake, fake, None, m.F32, fake, 4, ctypes.byref(kv), None,
+                                   fake, None)
+    assert st == m.ERR_UNSUPPORTED
 
 
 def test_dispatch_record_before_any_launch(m):

@@ -90,6 +90,10 @@ def test_dispatch_record_names_the_variant():
     dw6 = parity.build(w6)
     dw6.index_score()
     assert "index_score nvfp4_mma_f16" in msa.last_dispatch()
+    w8 = synth.scaled(synth.WORKLOADS["fp8kv_32k"], batch=1, ctx=700)
+    dw8 = parity.build(w8)
+    dw8.step()
+    assert "sparse_gqa fp8_tma_cvt_f16_mma" in msa.last_dispatch()
     wt = synth.scaled(synth.WORKLOADS["tiny"], batch=1, ctx=700)
     dwt = parity.build(wt)
     dwt.index_score()

@@ -77,7 +77,7 @@ def test_layer_reusing_selection(name, graph):
     sel = src.selected.cpu().numpy()
     out = layer.out.float().cpu().numpy()
     lse = layer.lse.cpu().numpy()
-    kg, vg = parity.nvfp4_globals(w)
+    kg, vg = parity.kv_globals(w)
     lens = synth.seq_lens(w)
     for bi, b in enumerate(layer.which):
         L = int(lens[b])

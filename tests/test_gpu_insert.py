@@ -22,6 +22,9 @@ def _insert(k, v, idx, idx_dtype, kv_dtype, g=1.0, P=4, G=4):
     if kv_dtype == "bf16":
         cache = msa.KVCache(msa.BF16, torch.zeros((P, G, 128, 128), dtype=torch.bfloat16, device="cuda"),
                             torch.zeros((P, G, 128, 128), dtype=torch.bfloat16, device="cuda"))
+    elif kv_dtype == "fp8":
+        cache = msa.KVCache(msa.FP8_E4M3, torch.zeros((P, G, 128, 128), dtype=torch.uint8, device="cuda"),
+                            torch.zeros((P, G, 128, 128), dtype=torch.uint8, device="cuda"), None, None, g, g)
     else:
         cache = msa.KVCache(msa.NVFP4, *[torch.zeros((P, G, 128, n), dtype=torch.uint8, device="cuda")
                                          for n in (64, 64, 8, 8)], g, g)
@@ -50,6 +53,8 @@ def _insert(k, v, idx, idx_dtype, kv_dtype, g=1.0, P=4, G=4):
     if kv_dtype == "bf16":
         out["k"] = tok(cache.k.view(torch.int16)).view(np.uint16)
         out["v"] = tok(cache.v.view(torch.int16)).view(np.uint16)
+    elif kv_dtype == "fp8":
+        out.update(k=tok(cache.k), v=tok(cache.v))
     else:
         out.update(k=tok(cache.k), v=tok(cache.v), ks=tok(cache.k_scale), vs=tok(cache.v_scale))
     return out
@@ -154,3 +159,24 @@ def test_nvfp4_index_keys_bit_exact(src):
     codes, scales = Qz.quant_nvfp4(xv, g)
     assert np.array_equal(got["idx_block_scale"], scales)
     assert np.array_equal(got["idx_keys"], codes)
+
+
+def test_fp8_kv_bit_exact():
+    """FP8 E4M3 K/V with one scale per tensor: E4M3 midpoints (ties to even), values
+    past the saturation point, zeros and random values, byte for byte."""
+    rng = np.random.default_rng(31)
+    T, G = 290, 4
+    s = np.float32(synth.FP8_KV_SYNTH_SCALE)
+    k = (rng.standard_normal((T, G, 128)) * rng.uniform(0.01, 4, (T, G, 1))).astype(np.float32)
+    v = rng.standard_normal((T, G, 128)).astype(np.float32)
+    vals = F.e4m3_decode(np.arange(0, 0x7E))
+    mids = ((vals[:-1] + vals[1:]) / 2 * s).astype(np.float32)          # midpoints of x / s
+    k[0, 0, :] = np.resize(mids, 128)
+    k[1, 1, :8] = [7.0, -7.0, 100.0, -1e4, 6.0, -6.0, 0.0, -0.0]     # saturation and zeros
+    v[2, 3, :] = 0.0
+    kb = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(k))             # the kernel reads bf16
+    vb = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(v))
+    idx = np.zeros((T, G, 128), dtype=np.float32)
+    got = _insert(k, v, idx, "f32", "fp8", g=float(s))
+    assert np.array_equal(got["k"], Qz.quant_kv_fp8(kb, s))
+    assert np.array_equal(got["v"], Qz.quant_kv_fp8(vb, s))

@@ -26,6 +26,9 @@ REDUCED = {
     # NVFP4 index keys with 8 query positions (the per-value block-scale path;
     # one position takes the per-group path)
     "spec8_fp4idx": synth.scaled(W["spec8"], batch=3, ctx=3000, idx_dtype="nvfp4"),
+    "fp8kv_32k": synth.scaled(W["fp8kv_32k"], batch=3, ctx=2400),
+    # FP8 K/V with 8 positions (causal limits inside the local block)
+    "spec8_fp8kv": synth.scaled(W["spec8"], batch=2, ctx=2700, kv_dtype="fp8"),
 }
 
 
@@ -45,6 +48,7 @@ EDGE_LENS = {
     "tiny_f32_edges": ("tiny", [1, 200, 4095]),
     "fp4idx_edges": ("b32_32k_fp4idx", [1, 129, 257, 2100]),
     "spec_fp4idx_edges": ("spec8", [8, 9, 136, 1028, 2951], {"idx_dtype": "nvfp4"}),
+    "fp8kv_edges": ("fp8kv_32k", [1, 127, 128, 129, 1921, 2049]),
 }
 
 
