@@ -36,8 +36,9 @@ constexpr int kTokPerWarp = 32;                  // tokens of every block that o
 constexpr int kCWarps = kBlock / kTokPerWarp;    // consumer warps (one per SM sub-partition)
 constexpr int kNT = kTokPerWarp / 8;             // QK^T n-tiles of 8 tokens per warp
 constexpr int kKK = kTokPerWarp / 16;            // PV k-steps of 16 tokens per warp
-constexpr int kCombWarps = kCWarps < 4 ? kCWarps : 4;   // states staged in shared memory at a row's end
+constexpr int kCombWarps = kCWarps;              // states staged in shared memory at a row's end
 constexpr int kLanesPerRow = 32 / kTokPerWarp;   // NVFP4 expansion: lanes per token row
+static_assert(kCWarps == 4, "the row merge runs on 4 warps x 32 threads");
 constexpr int kBoxBytes = kBlock * 64 * 2;       // 128 rows x 128 B (64 fp16/bf16)
 constexpr int kTileBytes = 4 * kBoxBytes;        // K lo/hi + V lo/hi = 64 KB
 constexpr int kFp4StageBytes = 2 * (kBlock * kDim / 2 + kBlock * kDim / 16);  // 18 KB
@@ -86,7 +87,7 @@ __host__ __device__ constexpr SmemLayout gqa_layout() {
   s.comb_o = s.tiles + (kKv == kKvNvfp4 ? kTileBytes : 0);
   s.comb_ml = s.comb_o + kCombWarps * kGroup * kDim * 4;
   s.bars = s.comb_ml + kCombWarps * kGroup * 2 * 4;
-  s.total = s.bars + (2 * stages_for<kKv>() + 3) * 8 + 16;   // + the last-arriver flag
+  s.total = s.bars + (2 * stages_for<kKv>() + 2) * 8 + 16;   // + the last-arriver flag
   return s;
 }
 
@@ -195,11 +196,11 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
   uint8_t* sm = smem_raw + (base_addr - raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + Ly.bars);
   uint64_t* empty = full + kGqaStages;
-  uint64_t* gbar = empty + kGqaStages;   // [0]: partials written, [1]: partials read, [2]: upper warps staged
+  uint64_t* gbar = empty + kGqaStages;   // [0]: partials written, [1]: partials read
   float* comb_o = reinterpret_cast<float*>(sm + Ly.comb_o);
   float* comb_m = reinterpret_cast<float*>(sm + Ly.comb_ml);
   float* comb_l = comb_m + kCombWarps * kGroup;
-  int* last_flag = reinterpret_cast<int*>(sm + Ly.bars + (2 * kGqaStages + 3) * 8);
+  int* last_flag = reinterpret_cast<int*>(sm + Ly.bars + (2 * kGqaStages + 2) * 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_launch_dependents();
@@ -210,7 +211,6 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     }
     mbar_init(smem_addr(&gbar[0]), kCWarps);
     mbar_init(smem_addr(&gbar[1]), kCWarps);
-    mbar_init(smem_addr(&gbar[2]), kCWarps);
     fence_mbar_init();
     if (!kFp4) {
       prefetch_tensormap(&tk);
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
   const int w = warp - 1;          // token slice [kTokPerWarp w, kTokPerWarp (w + 1)) of every block
   const int ct = threadIdx.x - 32; // 0 .. 32 kCWarps - 1; the first 128 merge a row's states
   const int gr = lane >> 2, c = lane & 3;
-  uint32_t gph[3] = {0u, 0u, 0u};
+  uint32_t gph[2] = {0u, 0u};
 
   uint32_t qf[8][4];
   float o[16][4];
@@ -408,31 +408,7 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
       v += __shfl_xor_sync(kAll, v, 2);
       lt[r] = v;
     }
-    if constexpr (kCWarps > kCombWarps) {
-      // Warp w + 4 hands its state to warp w, which folds it into its registers
-      // and then reuses the slot for the merged state.
-      if (w >= kCombWarps) stage_state(w - kCombWarps, lt);
-      if (!group_sync(smem_addr(&gbar[2]), gph[2], lane)) return false;
-      if (w < kCombWarps) {
-        const float* po = comb_o + w * kGroup * kDim;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const float mp = comb_m[w * kGroup + gr + 8 * r], lp = comb_l[w * kGroup + gr + 8 * r];
-          const float M = fmaxf(m_r[r], mp);
-          const float fa = M == -INFINITY ? 0.f : ex2_approx(m_r[r] - M);
-          const float fb = M == -INFINITY ? 0.f : ex2_approx(mp - M);
-          lt[r] = lt[r] * fa + lp * fb;
-          m_r[r] = M;
-#pragma unroll
-          for (int n = 0; n < 16; ++n) {
-            const float2 x = *reinterpret_cast<const float2*>(po + (gr + 8 * r) * kDim + 8 * n + 2 * c);
-            o[n][2 * r] = o[n][2 * r] * fa + x.x * fb;
-            o[n][2 * r + 1] = o[n][2 * r + 1] * fa + x.y * fb;
-          }
-        }
-      }
-    }
-    if (w < kCombWarps) stage_state(w, lt);
+    stage_state(w, lt);
     if (!group_sync(smem_addr(&gbar[0]), gph[0], lane)) return false;
     const bool merger = ct < kCombWarps * 32;
     const int hh = (ct >> 3) & (kGroup - 1), d0 = (ct & 7) * 16;
