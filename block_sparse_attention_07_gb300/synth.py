@@ -88,6 +88,20 @@ FP8_KV_SYNTH_SCALE = 6.0 / 448.0
 LAYER_SEED_STRIDE = 7919
 
 
+# Synthetic parameters of the norm / rotary step in front of the decode path
+# (the pages give none): RMSNorm epsilon and rotary base.
+PROLOGUE_EPS = 1e-6
+PROLOGUE_THETA = 10000.0
+
+
+def norm_weights(w: Workload) -> dict:
+    """Per-dim fp32 RMSNorm weights of the query, key, index query and index key
+    projections: 1 + 0.1 * N(0, 1), seeded per workload."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([w.seed, 99991])))
+    return {name: (1.0 + 0.1 * rng.standard_normal(w.head_dim)).astype(np.float32)
+            for name in ("q", "k", "idx_q", "idx_k")}
+
+
 def kv_scale(w: Workload) -> float:
     """The per-tensor K/V scale of the workload's cache format (fp32 value)."""
     s = {"bf16": 1.0, "fp8": FP8_KV_SYNTH_SCALE, "nvfp4": NVFP4_SYNTH_GLOBAL}[w.kv_dtype]
