@@ -304,6 +304,25 @@ def run_ours(args, world, rank, local):
         graph.replay()
     graph_ms = event_timed(graph.replay, args.steps)
     assert dw.check_flags() == 0, "device flags raised (graph replay)"
+    # The fused QK-norm + RoPE + K/V/index insert of the step's tokens, alone and
+    # as the first kernel of a step (in place of the plain insert).
+    prologue_ms = pro_step_ms = None
+    if w.idx_dtype != "f32":
+        # per launch: 20 launches back to back from one captured graph (a launch
+        # marshalled from Python takes longer on the host than the kernel on the GPU)
+        burst = dw.capture(lambda st: [dw.qk_norm_rope_insert(st) for _ in range(20)])
+        for _ in range(args.warmup):
+            burst.replay()
+        prologue_ms = [t / 20 for t in event_timed(burst.replay, args.steps)]
+
+        def pro_step():
+            dw.qk_norm_rope_insert()
+            dw.index_score()
+            dw.select()
+            dw.attend()
+        pro_step_ms = event_timed(pro_step, args.steps)
+        assert dw.check_flags() == 0, "device flags raised (fused norm/RoPE/insert)"
+        dw.insert_step_tokens()           # restore the plain-insert cache contents
     # A layer that reuses this step's selection: K/V insert + sparse GQA only.
     reuse_ms = None
     if not args.no_layer_reuse:
@@ -355,6 +374,14 @@ def run_ours(args, world, rank, local):
         "clocks": clk,
         "wall_s_timed_region": wall,
     }
+    if prologue_ms is not None:
+        line["qk_norm_rope_insert"] = {
+            "ms_per_launch": statistics.mean(prologue_ms),
+            "step_value": B * Q / (statistics.mean(pro_step_ms) / 1e3), "unit": "query-tokens/s",
+            "step_ms": statistics.mean(pro_step_ms),
+            "what": "fused RMSNorm + RoPE of the step's query/key/index projections and K/V/index-key insert "
+                    "(ms_per_launch: 20 launches replayed from one graph); step_value: that kernel in place of "
+                    "the plain insert, then score, select, attend"}
     if reuse_ms is not None:
         line["selection_reuse_layer"] = {
             "value": B * Q / (statistics.mean(reuse_ms) / 1e3), "unit": "query-tokens/s",

@@ -3,6 +3,9 @@
 // and index keys (fp32 copy or FP8 E4M3 + per-token scale) into the paged
 // caches. One warp per (token, head); every step of the quantisers is an IEEE
 // round-to-nearest fp32 operation so the bytes are a pure function of the input.
+#include <cmath>
+#include <cstring>
+
 #include "msa_internal.h"
 
 namespace msa {
@@ -50,12 +53,71 @@ __device__ __forceinline__ void quant_nvfp4_vals(const float (&x)[4], uint8_t* c
   if ((lane & 3) == 0) scales[lane >> 2] = sb_code;
 }
 
-__device__ __forceinline__ void quant_nvfp4_row(const uint16_t* src, uint8_t* codes, uint8_t* scales, float g,
-                                                int lane) {
-  const uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
-  const float x[4] = {bf16_bits_to_f32(raw.x & 0xFFFF), bf16_bits_to_f32(raw.x >> 16),
-                      bf16_bits_to_f32(raw.y & 0xFFFF), bf16_bits_to_f32(raw.y >> 16)};
-  quant_nvfp4_vals(x, codes, scales, g, lane);
+// The row writers below take one (token, head) row of D = 128 values, 4 per
+// lane (dims 4 lane .. 4 lane + 3), as fp32 values (bf16-exact for bf16, FP8 and
+// NVFP4 caches) and store it into row `row` of a [P, heads, BS, ...] cache.
+
+// K or V row into the K/V cache (bf16 copy, FP8 E4M3 with the tensor scale, NVFP4).
+__device__ __forceinline__ void store_kv_row(const InsertParams& p, bool is_v, int64_t row, const float (&x)[4],
+                                             int lane) {
+  void* base = is_v ? p.v : p.k;
+  if (p.kv_fp8) {
+    // code = E4M3_RNE_satfinite(x / s), one fp32 RN division per value
+    const float s = is_v ? p.v_global : p.k_global;
+    const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(x[0], s), __fdiv_rn(x[1], s));
+    const uint16_t hi = f32x2_to_e4m3x2(__fdiv_rn(x[2], s), __fdiv_rn(x[3], s));
+    *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(base) + row * kDim + 4 * lane) =
+        static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  } else if (!p.kv_nvfp4) {
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(base) + row * kDim + 4 * lane) =
+        make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+  } else {
+    quant_nvfp4_vals(x, static_cast<uint8_t*>(base) + row * (kDim / 2),
+                     (is_v ? p.v_scale : p.k_scale) + row * (kDim / 16), is_v ? p.v_global : p.k_global, lane);
+  }
+}
+
+// Index key row into the index cache (fp32 copy, FP8 E4M3 + per-(token, head)
+// scale s = amax / 448, or NVFP4).
+__device__ __forceinline__ void store_idx_row(const InsertParams& p, int64_t row, const float (&x)[4], int lane) {
+  if (p.idx_fp4) {
+    quant_nvfp4_vals(x, static_cast<uint8_t*>(p.idx_keys) + row * (kDim / 2), p.idx_block_scale + row * (kDim / 16),
+                     p.idx_global, lane);
+  } else if (!p.idx_fp8) {
+    *reinterpret_cast<float4*>(static_cast<float*>(p.idx_keys) + row * kDim + 4 * lane) =
+        make_float4(x[0], x[1], x[2], x[3]);
+  } else {
+    float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const float s = __fdiv_rn(a, 448.0f);
+    uint32_t word = 0;
+    if (s > 0.f) {
+      const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(x[0], s), __fdiv_rn(x[1], s));
+      const uint16_t hi = f32x2_to_e4m3x2(__fdiv_rn(x[2], s), __fdiv_rn(x[3], s));
+      word = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    }
+    *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.idx_keys) + row * kDim + 4 * lane) = word;
+    if (lane == 0) p.idx_scale[row] = s;
+  }
+}
+
+__device__ __forceinline__ void load_bf16x4(const uint16_t* src, float (&x)[4]) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(src);
+  x[0] = bf16_bits_to_f32(raw.x & 0xFFFF);
+  x[1] = bf16_bits_to_f32(raw.x >> 16);
+  x[2] = bf16_bits_to_f32(raw.y & 0xFFFF);
+  x[3] = bf16_bits_to_f32(raw.y >> 16);
+}
+
+// Cache row of a slot, or -1 (negative slot: skip; out of range: skip and flag).
+__device__ __forceinline__ int64_t slot_row(const InsertParams& p, int64_t slot, int h, int heads, int lane) {
+  if (slot < 0) return -1;
+  if (slot >= p.num_slots) {
+    if (lane == 0) set_flag(p.flags, MSA_FLAG_BAD_SLOT);
+    return -1;
+  }
+  return ((slot / kBlock) * heads + h) * kBlock + slot % kBlock;   // (page, head, offset) row
 }
 
 __global__ void __launch_bounds__(256) kv_insert_kernel(InsertParams p) {
@@ -68,72 +130,141 @@ __global__ void __launch_bounds__(256) kv_insert_kernel(InsertParams p) {
   for (int64_t w = warp; w < total; w += nwarps) {
     const int t = static_cast<int>(w / p.G);
     const int h = static_cast<int>(w % p.G);
-    const int64_t slot = p.slots[t];
-    if (slot < 0) continue;
-    if (slot >= p.num_slots) {
-      if (lane == 0) set_flag(p.flags, MSA_FLAG_BAD_SLOT);
-      continue;
-    }
-    const int64_t page = slot / kBlock, off = slot % kBlock;
-    const int64_t row = (page * p.G + h) * kBlock + off;   // (page, head, offset) row of any [P, G, BS, ...] cache
-    const int64_t src = (static_cast<int64_t>(t) * p.G + h) * kDim;
-
-    if (p.kv_fp8) {
-      // code = E4M3_RNE_satfinite(x / s), one fp32 RN division per value
-      const uint2 kk = *reinterpret_cast<const uint2*>(p.k_new + src + 4 * lane);
-      const uint2 vv = *reinterpret_cast<const uint2*>(p.v_new + src + 4 * lane);
-      auto enc = [](uint2 raw, float s) -> uint32_t {
-        const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(bf16_bits_to_f32(raw.x & 0xFFFF), s),
-                                            __fdiv_rn(bf16_bits_to_f32(raw.x >> 16), s));
-        const uint16_t hi = f32x2_to_e4m3x2(__fdiv_rn(bf16_bits_to_f32(raw.y & 0xFFFF), s),
-                                            __fdiv_rn(bf16_bits_to_f32(raw.y >> 16), s));
-        return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-      };
-      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.k) + row * kDim + 4 * lane) = enc(kk, p.k_global);
-      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.v) + row * kDim + 4 * lane) = enc(vv, p.v_global);
-    } else if (!p.kv_nvfp4) {
-      const uint2 kk = *reinterpret_cast<const uint2*>(p.k_new + src + 4 * lane);
-      const uint2 vv = *reinterpret_cast<const uint2*>(p.v_new + src + 4 * lane);
-      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.k) + row * kDim + 4 * lane) = kk;
-      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.v) + row * kDim + 4 * lane) = vv;
-    } else {
-      quant_nvfp4_row(p.k_new + src, static_cast<uint8_t*>(p.k) + row * (kDim / 2), p.k_scale + row * (kDim / 16),
-                      p.k_global, lane);
-      quant_nvfp4_row(p.v_new + src, static_cast<uint8_t*>(p.v) + row * (kDim / 2), p.v_scale + row * (kDim / 16),
-                      p.v_global, lane);
-    }
-
+    const int64_t row = slot_row(p, p.slots[t], h, p.G, lane);
+    if (row < 0) continue;
+    const int64_t src = (static_cast<int64_t>(t) * p.G + h) * kDim + 4 * lane;
+    float x[4];
+    load_bf16x4(p.k_new + src, x);
+    store_kv_row(p, false, row, x, lane);
+    load_bf16x4(p.v_new + src, x);
+    store_kv_row(p, true, row, x, lane);
     if (p.idx_new != nullptr) {
-      float x[4];
       if (p.idx_new_bf16) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.idx_new) + src + 4 * lane);
-        x[0] = bf16_bits_to_f32(raw.x & 0xFFFF); x[1] = bf16_bits_to_f32(raw.x >> 16);
-        x[2] = bf16_bits_to_f32(raw.y & 0xFFFF); x[3] = bf16_bits_to_f32(raw.y >> 16);
+        load_bf16x4(static_cast<const uint16_t*>(p.idx_new) + src, x);
       } else {
-        const float4 raw = *reinterpret_cast<const float4*>(static_cast<const float*>(p.idx_new) + src + 4 * lane);
+        const float4 raw = *reinterpret_cast<const float4*>(static_cast<const float*>(p.idx_new) + src);
         x[0] = raw.x; x[1] = raw.y; x[2] = raw.z; x[3] = raw.w;
       }
-      if (p.idx_fp4) {
-        quant_nvfp4_vals(x, static_cast<uint8_t*>(p.idx_keys) + row * (kDim / 2),
-                         p.idx_block_scale + row * (kDim / 16), p.idx_global, lane);
-      } else if (!p.idx_fp8) {
-        *reinterpret_cast<float4*>(static_cast<float*>(p.idx_keys) + row * kDim + 4 * lane) =
-            make_float4(x[0], x[1], x[2], x[3]);
-      } else {
-        float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+      store_idx_row(p, row, x, lane);
+    }
+  }
+}
+
+// ------------------------------------------- QK-norm + RoPE + cache insert --
+// "MiniMax-M3.1-Flash Day-0 対応", section "最適化と数値" (QKV GEMM + norm + RoPE
+// + KV insert fused) and "MiniMax M3 vLLM サポート：…", section "カーネル融合"
+// (QKNorm + RoPE + KV insertion in one kernel). kPrologueParts CTAs per token,
+// each taking every kPrologueParts-th head row (query heads, key heads, V heads,
+// index query heads, index key heads). A CTA computes the token's 64 rotary
+// (cos, sin) pairs (angle pos * theta^(-2i/128) with the inverse frequencies
+// from the host in double precision, reduced modulo 2 pi in double so large
+// positions keep their phase, then an fp32 sincos), while each warp loads all
+// of its rows; then per row: RMSNorm (fp32, IEEE sqrt and division), rotation
+// of the pairs (i, i + 64) — lane l holds dims 4l..4l+3, its partner lane
+// l ^ 16 the other half — rounding to bf16, and the query goes to its output,
+// the key (and V, unrotated) through the cache's quantiser. Index rows take the
+// same path with their own weights unless the layer reuses another layer's
+// selection (null index pointers).
+constexpr int kPrologueParts = 4;
+constexpr int kPrologueWarps = 8;
+constexpr int kPrologueRowsPerWarp = 3;   // ceil(80 rows / (4 parts x 8 warps))
+
+struct PrologueParams {
+  InsertParams ins;
+  const uint16_t* q;          // bf16 [T, H, D]
+  const uint16_t* idx_q;      // bf16 [T, I, D] or null
+  uint16_t* q_out;
+  uint16_t* idx_q_out;
+  const int32_t* positions;   // [T]
+  const float* wq;
+  const float* wk;
+  const float* wiq;
+  const float* wik;
+  float eps;
+  int H, I;
+  double inv_freq[kDim / 2];  // theta^(-2i/D)
+};
+
+__global__ void __launch_bounds__(32 * kPrologueWarps) qk_norm_rope_insert_kernel(const __grid_constant__ PrologueParams pp) {
+  __shared__ float2 cs[kDim / 2];
+  griddep_launch_dependents();
+  griddep_wait();
+  const InsertParams& p = pp.ins;
+  const int t = blockIdx.x / kPrologueParts, part = blockIdx.x % kPrologueParts;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool with_idx = pp.idx_q != nullptr;
+  const int nq = pp.H, nk = p.G, ni = with_idx ? pp.I : 0;
+  const int rows = nq + 2 * nk + 2 * ni;     // q heads, k heads, v heads, index q heads, index k heads
+
+  // this warp's rows, loaded before anything waits on them
+  int kind[kPrologueRowsPerWarp], head[kPrologueRowsPerWarp];
+  float x[kPrologueRowsPerWarp][4];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-        const float s = __fdiv_rn(a, 448.0f);
-        uint32_t word = 0;
-        if (s > 0.f) {
-          const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(x[0], s), __fdiv_rn(x[1], s));
-          const uint16_t hi = f32x2_to_e4m3x2(__fdiv_rn(x[2], s), __fdiv_rn(x[3], s));
-          word = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-        }
-        *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.idx_keys) + row * kDim + 4 * lane) = word;
-        if (lane == 0) p.idx_scale[row] = s;
+  for (int j = 0; j < kPrologueRowsPerWarp; ++j) {
+    const int r = part + kPrologueParts * (warp + kPrologueWarps * j);
+    kind[j] = -1;
+    if (r >= rows) continue;
+    int k, h;                                  // 0 q, 1 k, 2 v, 3 index q, 4 index k
+    if (r < nq) { k = 0; h = r; }
+    else if (r < nq + nk) { k = 1; h = r - nq; }
+    else if (r < nq + 2 * nk) { k = 2; h = r - nq - nk; }
+    else if (r < nq + 2 * nk + ni) { k = 3; h = r - nq - 2 * nk; }
+    else { k = 4; h = r - nq - 2 * nk - ni; }
+    kind[j] = k;
+    head[j] = h;
+    const uint16_t* src = k == 0 ? pp.q + (static_cast<int64_t>(t) * nq + h) * kDim
+                        : k == 1 ? p.k_new + (static_cast<int64_t>(t) * nk + h) * kDim
+                        : k == 2 ? p.v_new + (static_cast<int64_t>(t) * nk + h) * kDim
+                        : k == 3 ? pp.idx_q + (static_cast<int64_t>(t) * pp.I + h) * kDim
+                                 : static_cast<const uint16_t*>(p.idx_new) + (static_cast<int64_t>(t) * pp.I + h) * kDim;
+    load_bf16x4(src + 4 * lane, x[j]);
+  }
+  if (threadIdx.x < kDim / 2) {
+    constexpr double kTwoPi = 6.283185307179586476925286766559;
+    const double ang = static_cast<double>(pp.positions[t]) * pp.inv_freq[threadIdx.x];
+    const double red = fma(-rint(ang * (1.0 / kTwoPi)), kTwoPi, ang);     // |red| <= pi
+    float sn, cn;
+    sincosf(static_cast<float>(red), &sn, &cn);
+    cs[threadIdx.x] = make_float2(cn, sn);
+  }
+  __syncthreads();
+  const int64_t slot = p.slots[t];
+  const float rms_scale = 1.0f / kDim;
+#pragma unroll
+  for (int j = 0; j < kPrologueRowsPerWarp; ++j) {
+    const int k = kind[j], h = head[j];
+    if (k < 0) continue;
+    if (k != 2) {
+      // RMSNorm
+      float ss = x[j][0] * x[j][0] + x[j][1] * x[j][1] + x[j][2] * x[j][2] + x[j][3] * x[j][3];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float rinv = __fdiv_rn(1.0f, __fsqrt_rn(__fmaf_rn(ss, rms_scale, pp.eps)));
+      const float* wv = k == 0 ? pp.wq : k == 1 ? pp.wk : k == 3 ? pp.wiq : pp.wik;
+      const float4 wt = *reinterpret_cast<const float4*>(wv + 4 * lane);
+      const float y0 = x[j][0] * rinv * wt.x, y1 = x[j][1] * rinv * wt.y;
+      const float y2 = x[j][2] * rinv * wt.z, y3 = x[j][3] * rinv * wt.w;
+      const float yv[4] = {y0, y1, y2, y3};
+      // rotary: lane l < 16 holds y_i (i = 4l + e), lane l + 16 holds y_{i+64};
+      // the results are rounded to bf16, the values the caches and outputs hold
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float other = __shfl_xor_sync(0xffffffffu, yv[e], 16);
+        const float2 c = cs[(4 * lane + e) & (kDim / 2 - 1)];
+        const float z = lane < 16 ? yv[e] * c.x - other * c.y : other * c.y + yv[e] * c.x;
+        x[j][e] = bf16_bits_to_f32(static_cast<uint16_t>(pack_bf16x2(z, 0.f) & 0xFFFF));
       }
     }
+    if (k == 0 || k == 3) {
+      uint16_t* dst = k == 0 ? pp.q_out + (static_cast<int64_t>(t) * nq + h) * kDim
+                             : pp.idx_q_out + (static_cast<int64_t>(t) * pp.I + h) * kDim;
+      *reinterpret_cast<uint2*>(dst + 4 * lane) = make_uint2(pack_bf16x2(x[j][0], x[j][1]), pack_bf16x2(x[j][2], x[j][3]));
+      continue;
+    }
+    const int64_t row = slot_row(p, slot, h, k == 4 ? pp.I : p.G, lane);
+    if (row < 0) continue;
+    if (k == 4) store_idx_row(p, row, x[j], lane);
+    else store_kv_row(p, k == 2, row, x[j], lane);
   }
 }
 
@@ -170,6 +301,52 @@ cudaError_t launch_kv_insert(const InsertArgs& a, cudaStream_t stream, DispatchR
   rec->set("kv_insert %s%s grid=%lld block=256 tokens=%d", a.kv_nvfp4 ? "nvfp4" : a.kv_fp8 ? "fp8" : "bf16",
            a.idx_new ? (a.idx_fp4 ? "+idx_nvfp4" : a.idx_fp8 ? "+idx_fp8" : "+idx_f32") : "",
            static_cast<long long>(blocks), a.T);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qk_norm_rope_insert(const PrologueArgs& a, cudaStream_t stream, DispatchRecord* rec) {
+  PrologueParams pp;
+  InsertParams& p = pp.ins;
+  memset(&pp, 0, sizeof(pp));
+  p.k_new = static_cast<const uint16_t*>(a.ins.k_new);
+  p.v_new = static_cast<const uint16_t*>(a.ins.v_new);
+  p.idx_new = a.ins.idx_new;
+  p.idx_new_bf16 = 1;
+  p.slots = a.ins.slots;
+  p.T = a.ins.T;
+  p.G = a.ins.G;
+  p.num_slots = a.ins.num_slots;
+  p.kv_nvfp4 = a.ins.kv_nvfp4;
+  p.kv_fp8 = a.ins.kv_fp8;
+  p.k = a.ins.k; p.v = a.ins.v;
+  p.k_scale = static_cast<uint8_t*>(a.ins.k_scale);
+  p.v_scale = static_cast<uint8_t*>(a.ins.v_scale);
+  p.k_global = a.ins.k_global; p.v_global = a.ins.v_global;
+  p.idx_fp8 = a.ins.idx_fp8;
+  p.idx_fp4 = a.ins.idx_fp4;
+  p.idx_keys = a.ins.idx_keys;
+  p.idx_scale = a.ins.idx_scale;
+  p.idx_block_scale = static_cast<uint8_t*>(a.ins.idx_block_scale);
+  p.idx_global = a.ins.idx_global;
+  p.flags = a.ins.flags;
+  pp.q = static_cast<const uint16_t*>(a.q);
+  pp.idx_q = static_cast<const uint16_t*>(a.idx_q);
+  pp.q_out = static_cast<uint16_t*>(a.q_out);
+  pp.idx_q_out = static_cast<uint16_t*>(a.idx_q_out);
+  pp.positions = a.positions;
+  pp.wq = a.wq; pp.wk = a.wk; pp.wiq = a.wiq; pp.wik = a.wik;
+  pp.eps = a.eps;
+  pp.H = a.H;
+  pp.I = a.I;
+  for (int i = 0; i < kDim / 2; ++i) pp.inv_freq[i] = pow(static_cast<double>(a.theta), -2.0 * i / kDim);
+  const int rows = a.H + 2 * a.ins.G + (a.idx_q ? 2 * a.I : 0);
+  if (rows > kPrologueParts * kPrologueWarps * kPrologueRowsPerWarp) return cudaErrorInvalidValue;
+  const cudaError_t err = launch_pdl(qk_norm_rope_insert_kernel, dim3(static_cast<unsigned>(a.ins.T) * kPrologueParts),
+                                     dim3(32 * kPrologueWarps), 0, stream, pp);
+  if (err != cudaSuccess) return err;
+  rec->set("qk_norm_rope_insert %s%s grid=%d block=256 heads=%d+%d+%d", a.ins.kv_nvfp4 ? "nvfp4" : a.ins.kv_fp8 ? "fp8" : "bf16",
+           a.idx_q ? (a.ins.idx_fp4 ? "+idx_nvfp4" : "+idx_fp8") : "", a.ins.T * kPrologueParts, a.H, a.ins.G,
+           a.idx_q ? a.I : 0);
   return cudaGetLastError();
 }
 

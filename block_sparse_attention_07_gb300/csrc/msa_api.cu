@@ -68,22 +68,13 @@ msa_status_t msa_get_last_dispatch(char* buf, size_t len) {
   return MSA_OK;
 }
 
-msa_status_t msa_kv_insert_quant(const msa_dims_t* dims, const void* k_new, const void* v_new,
-                                 const void* idx_k_new, msa_dtype_t idx_new_dtype, const int64_t* slot_mapping,
-                                 int32_t num_tokens, const msa_kv_cache_t* cache,
-                                 const msa_index_cache_t* idx_cache, uint32_t* dev_flags, void* stream) {
-  msa_status_t st = check_dims(dims);
-  if (st != MSA_OK) return st;
-  if (num_tokens < 0 || cache == nullptr || dev_flags == nullptr) return MSA_ERR_INVALID_ARG;
-  if (num_tokens == 0) {
-    g_record.set("kv_insert empty");
-    return MSA_OK;
-  }
-  if (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr || cache->k == nullptr || cache->v == nullptr)
-    return MSA_ERR_INVALID_ARG;
-  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(cache->k) || !aligned16(cache->v))
-    return MSA_ERR_INVALID_ARG;
-  InsertArgs a;
+// Validates the caches of an insert and fills the shared launch arguments
+// (everything but the source rows). idx_bf16_only: index sources must be bf16.
+static msa_status_t insert_targets(const msa_dims_t* dims, bool with_idx, msa_dtype_t idx_new_dtype,
+                                   const msa_kv_cache_t* cache, const msa_index_cache_t* idx_cache,
+                                   uint32_t* dev_flags, InsertArgs& a) {
+  if (cache == nullptr || dev_flags == nullptr || cache->k == nullptr || cache->v == nullptr) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(cache->k) || !aligned16(cache->v)) return MSA_ERR_INVALID_ARG;
   memset(&a, 0, sizeof(a));
   if (cache->dtype == MSA_NVFP4) {
     if (cache->k_scale == nullptr || cache->v_scale == nullptr) return MSA_ERR_INVALID_ARG;
@@ -99,9 +90,8 @@ msa_status_t msa_kv_insert_quant(const msa_dims_t* dims, const void* k_new, cons
   } else if (cache->dtype != MSA_BF16) {
     return MSA_ERR_UNSUPPORTED;
   }
-  if (idx_k_new != nullptr) {
-    if (idx_cache == nullptr || idx_cache->keys == nullptr || !aligned16(idx_k_new) || !aligned16(idx_cache->keys))
-      return MSA_ERR_INVALID_ARG;
+  if (with_idx) {
+    if (idx_cache == nullptr || idx_cache->keys == nullptr || !aligned16(idx_cache->keys)) return MSA_ERR_INVALID_ARG;
     if (idx_cache->dtype == MSA_FP8_E4M3) {
       if (idx_cache->scale == nullptr) return MSA_ERR_INVALID_ARG;
       if (idx_new_dtype != MSA_F32 && idx_new_dtype != MSA_BF16) return MSA_ERR_UNSUPPORTED;
@@ -118,15 +108,10 @@ msa_status_t msa_kv_insert_quant(const msa_dims_t* dims, const void* k_new, cons
     } else {
       return MSA_ERR_UNSUPPORTED;
     }
-    a.idx_new = idx_k_new;
     a.idx_new_bf16 = idx_new_dtype == MSA_BF16;
     a.idx_keys = idx_cache->keys;
     a.idx_scale = idx_cache->scale;
   }
-  a.k_new = k_new;
-  a.v_new = v_new;
-  a.slots = slot_mapping;
-  a.T = num_tokens;
   a.G = dims->n_kv_heads;
   a.num_slots = static_cast<int64_t>(dims->num_pages) * kBlock;
   a.k = cache->k;
@@ -136,7 +121,86 @@ msa_status_t msa_kv_insert_quant(const msa_dims_t* dims, const void* k_new, cons
   a.k_global = cache->k_global;
   a.v_global = cache->v_global;
   a.flags = dev_flags;
+  return MSA_OK;
+}
+
+msa_status_t msa_kv_insert_quant(const msa_dims_t* dims, const void* k_new, const void* v_new,
+                                 const void* idx_k_new, msa_dtype_t idx_new_dtype, const int64_t* slot_mapping,
+                                 int32_t num_tokens, const msa_kv_cache_t* cache,
+                                 const msa_index_cache_t* idx_cache, uint32_t* dev_flags, void* stream) {
+  msa_status_t st = check_dims(dims);
+  if (st != MSA_OK) return st;
+  if (num_tokens < 0 || cache == nullptr || dev_flags == nullptr) return MSA_ERR_INVALID_ARG;
+  if (num_tokens == 0) {
+    g_record.set("kv_insert empty");
+    return MSA_OK;
+  }
+  if (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || (idx_k_new != nullptr && !aligned16(idx_k_new)))
+    return MSA_ERR_INVALID_ARG;
+  InsertArgs a;
+  st = insert_targets(dims, idx_k_new != nullptr, idx_new_dtype, cache, idx_cache, dev_flags, a);
+  if (st != MSA_OK) return st;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.idx_new = idx_k_new;
+  a.slots = slot_mapping;
+  a.T = num_tokens;
   return cuda_status(launch_kv_insert(a, static_cast<cudaStream_t>(stream), &g_record));
+}
+
+msa_status_t msa_qk_norm_rope_insert(const msa_dims_t* dims, const void* q, const void* k, const void* v,
+                                     const void* idx_q, const void* idx_k, const int32_t* positions,
+                                     const int64_t* slot_mapping, int32_t num_tokens, const msa_norm_rope_t* nr,
+                                     void* q_out, void* idx_q_out, const msa_kv_cache_t* cache,
+                                     const msa_index_cache_t* idx_cache, uint32_t* dev_flags, void* stream) {
+  msa_status_t st = check_dims(dims);
+  if (st != MSA_OK) return st;
+  if (num_tokens < 0 || nr == nullptr || cache == nullptr || dev_flags == nullptr) return MSA_ERR_INVALID_ARG;
+  const bool with_idx = idx_q != nullptr || idx_k != nullptr;
+  if (with_idx && (idx_q == nullptr || idx_k == nullptr || idx_q_out == nullptr || nr->idx_q_weight == nullptr ||
+                   nr->idx_k_weight == nullptr))
+    return MSA_ERR_INVALID_ARG;
+  if (!(nr->eps >= 0.f) || nr->eps > 1.f || !(nr->rope_theta > 1.f) || nr->rope_theta > 3.0e38f)
+    return MSA_ERR_INVALID_ARG;
+  if (num_tokens == 0) {
+    g_record.set("qk_norm_rope_insert empty");
+    return MSA_OK;
+  }
+  if (q == nullptr || k == nullptr || v == nullptr || positions == nullptr || slot_mapping == nullptr ||
+      q_out == nullptr || nr->q_weight == nullptr || nr->k_weight == nullptr)
+    return MSA_ERR_INVALID_ARG;
+  const void* ptrs16[] = {q, k, v, q_out, nr->q_weight, nr->k_weight};
+  for (const void* ptr : ptrs16)
+    if (!aligned16(ptr)) return MSA_ERR_INVALID_ARG;
+  if (with_idx && (!aligned16(idx_q) || !aligned16(idx_k) || !aligned16(idx_q_out) || !aligned16(nr->idx_q_weight) ||
+                   !aligned16(nr->idx_k_weight)))
+    return MSA_ERR_INVALID_ARG;
+  if (with_idx && idx_cache != nullptr && idx_cache->dtype == MSA_F32) return MSA_ERR_UNSUPPORTED;
+  PrologueArgs a;
+  memset(&a, 0, sizeof(a));
+  st = insert_targets(dims, with_idx, MSA_BF16, cache, idx_cache, dev_flags, a.ins);
+  if (st != MSA_OK) return st;
+  a.ins.k_new = k;
+  a.ins.v_new = v;
+  a.ins.idx_new = idx_k;
+  a.ins.idx_new_bf16 = 1;
+  a.ins.slots = slot_mapping;
+  a.ins.T = num_tokens;
+  a.q = q;
+  a.idx_q = with_idx ? idx_q : nullptr;
+  a.q_out = q_out;
+  a.idx_q_out = with_idx ? idx_q_out : nullptr;
+  a.positions = positions;
+  a.wq = nr->q_weight;
+  a.wk = nr->k_weight;
+  a.wiq = nr->idx_q_weight;
+  a.wik = nr->idx_k_weight;
+  a.eps = nr->eps;
+  a.theta = nr->rope_theta;
+  a.H = dims->n_heads;
+  a.I = dims->n_idx_heads;
+  return cuda_status(launch_qk_norm_rope_insert(a, static_cast<cudaStream_t>(stream), &g_record));
 }
 
 msa_status_t msa_index_score(const msa_dims_t* dims, const void* idx_q, msa_dtype_t q_dtype,

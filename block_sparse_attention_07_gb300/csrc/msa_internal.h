@@ -115,6 +115,26 @@ constexpr int kPartialFloats = kGroup * kDim + 2 * kGroup;
 size_t gqa_workspace_bytes(int B, int Q, int G, int K);
 
 cudaError_t launch_kv_insert(const InsertArgs& a, cudaStream_t stream, DispatchRecord* rec);
+
+// QK-norm + RoPE + insert: the insert's arguments (k_new / v_new / idx_new are
+// the un-normalised bf16 projections) plus the queries and the norm / rotary
+// parameters.
+struct PrologueArgs {
+  InsertArgs ins;
+  const void* q;            // bf16 [T, H, D]
+  const void* idx_q;        // bf16 [T, I, D] or null (layer reusing a selection)
+  void* q_out;
+  void* idx_q_out;
+  const int32_t* positions;
+  const float* wq;
+  const float* wk;
+  const float* wiq;
+  const float* wik;
+  float eps;
+  float theta;
+  int H, I;
+};
+cudaError_t launch_qk_norm_rope_insert(const PrologueArgs& a, cudaStream_t stream, DispatchRecord* rec);
 cudaError_t launch_index_score(const IndexArgs& a, cudaStream_t stream, DispatchRecord* rec);
 cudaError_t launch_select_blocks(const SelectArgs& a, cudaStream_t stream, DispatchRecord* rec);
 cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRecord* rec);

@@ -25,7 +25,7 @@ FLAG_BAD_PAGE, FLAG_BAD_BLOCK, FLAG_BAD_SEQLEN, FLAG_BAD_SLOT, FLAG_TIMEOUT, FLA
 # Every function include/msa.h declares.
 EXPORTED = ("msa_abi_version", "msa_status_string", "msa_get_last_dispatch", "msa_kv_insert_quant",
             "msa_index_score", "msa_select_blocks", "msa_sparse_gqa_workspace_size", "msa_sparse_gqa_decode",
-            "msa_sparse_gqa_decode_noalloc", "msa_read_device_flags")
+            "msa_sparse_gqa_decode_noalloc", "msa_read_device_flags", "msa_qk_norm_rope_insert")
 
 
 class Dims(ctypes.Structure):
@@ -45,6 +45,12 @@ class _KVCache(ctypes.Structure):
 class _IndexCache(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int), ("keys", ctypes.c_void_p), ("scale", ctypes.c_void_p),
                 ("block_scale", ctypes.c_void_p), ("global_scale", ctypes.c_float)]
+
+
+class NormRope(ctypes.Structure):
+    """msa_norm_rope_t: device fp32 [D] RMSNorm weights (pointers), eps, rotary base."""
+    _fields_ = [("q_weight", ctypes.c_void_p), ("k_weight", ctypes.c_void_p), ("idx_q_weight", ctypes.c_void_p),
+                ("idx_k_weight", ctypes.c_void_p), ("eps", ctypes.c_float), ("rope_theta", ctypes.c_float)]
 
 
 class MSAError(RuntimeError):
@@ -74,6 +80,9 @@ def _load():
     lib.msa_sparse_gqa_decode_noalloc.argtypes = [ctypes.POINTER(Dims), vp, ctypes.POINTER(_KVCache), vp, vp, vp,
                                                   vp, vp, vp, vp]
     lib.msa_read_device_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+    lib.msa_qk_norm_rope_insert.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, vp, vp, vp, vp, i32,
+                                            ctypes.POINTER(NormRope), vp, vp, ctypes.POINTER(_KVCache),
+                                            ctypes.POINTER(_IndexCache), vp, vp]
     for name in EXPORTED:
         if name != "msa_abi_version" and name != "msa_status_string":
             getattr(lib, name).restype = ctypes.c_int
@@ -180,6 +189,21 @@ def kv_insert_quant(dims: Dims, k_new, v_new, idx_k_new, idx_new_dtype: int, slo
             int(k_new.shape[0]), ctypes.byref(kc), ctypes.byref(ic) if ic is not None else None, _ptr(flags),
             _stream(stream))
     return _call(lib.msa_kv_insert_quant, args, (dims, kc, ic), "msa_kv_insert_quant", prepare)
+
+
+def make_norm_rope(q_weight, k_weight, idx_q_weight=None, idx_k_weight=None, eps=1e-6, rope_theta=10000.0):
+    """msa_norm_rope_t from device fp32 [D] weight tensors (kept alive by the caller)."""
+    return NormRope(_ptr(q_weight), _ptr(k_weight), _ptr(idx_q_weight), _ptr(idx_k_weight), eps, rope_theta)
+
+
+def qk_norm_rope_insert(dims: Dims, q, k, v, idx_q, idx_k, positions, slot_mapping, nr: NormRope, q_out,
+                        idx_q_out, cache: KVCache, idx_cache: IndexCache | None, flags, stream=None, prepare=False):
+    kc = cache.c()
+    ic = idx_cache.c() if idx_cache is not None else None
+    args = (ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(idx_q), _ptr(idx_k), _ptr(positions),
+            _ptr(slot_mapping), int(q.shape[0]), ctypes.byref(nr), _ptr(q_out), _ptr(idx_q_out), ctypes.byref(kc),
+            ctypes.byref(ic) if ic is not None else None, _ptr(flags), _stream(stream))
+    return _call(lib.msa_qk_norm_rope_insert, args, (dims, nr, kc, ic), "msa_qk_norm_rope_insert", prepare)
 
 
 def index_score(dims: Dims, idx_q, q_dtype: int, idx_cache: IndexCache, block_table, seq_lens, scores, flags,

@@ -167,6 +167,40 @@ class DeviceWorkload:
         self.select(stream)
         self.attend(stream)
 
+    # ------------------------------------------- fused norm / RoPE / insert --
+    def _prologue_state(self):
+        if getattr(self, "_pro", None) is None:
+            w = self.w
+            B, Q = len(self.which), w.q_len
+            pos = (self.lens.astype(np.int64)[:, None] - Q + np.arange(Q)[None, :]).astype(np.int32).reshape(-1)
+            wts = {n: torch.from_numpy(a).to(self.device) for n, a in synth.norm_weights(w).items()}
+            self._pro = dict(
+                positions=torch.from_numpy(pos).to(self.device), weights=wts,
+                nr=msa.make_norm_rope(wts["q"], wts["k"], wts["idx_q"], wts["idx_k"], synth.PROLOGUE_EPS,
+                                      synth.PROLOGUE_THETA),
+                q_out=torch.empty((B * Q, w.n_heads, w.head_dim), dtype=torch.bfloat16, device=self.device),
+                idx_q_out=torch.empty((B * Q, w.n_idx_heads, w.head_dim), dtype=torch.bfloat16,
+                                      device=self.device))
+        return self._pro
+
+    def qk_norm_rope_insert(self, stream=None, with_index=None):
+        """The fused step in front of the decode path for this step's tokens:
+        RMSNorm + RoPE of the queries and keys (and index queries / keys unless
+        the layer reuses a selection), K/V/index-key insertion. The queries and
+        keys of the workload are taken as the un-normalised projections; the
+        normalised queries go to separate buffers (``_prologue_state``)."""
+        st = self._prologue_state()
+        with_index = self.has_index if with_index is None else with_index
+        if with_index and self.w.idx_dtype == "f32":
+            raise ValueError("the fused norm/RoPE/insert takes bf16 index projections (FP8 or NVFP4 index cache)")
+        B, Q = len(self.which), self.w.q_len
+        q = self.q.reshape(B * Q, self.w.n_heads, self.w.head_dim)
+        qi = self.q_idx.reshape(B * Q, self.w.n_idx_heads, self.w.head_dim) if with_index else None
+        msa.qk_norm_rope_insert(self.dims, q, self.new_k, self.new_v, qi, self.new_idx if with_index else None,
+                                st["positions"], self.new_slots, st["nr"], st["q_out"],
+                                st["idx_q_out"] if with_index else None, self.cache,
+                                self.idx_cache if with_index else None, self.flags, stream)
+
     def reuse_step(self, selected, stream=None):
         """One decode step of a layer that reuses another layer's selection
         (logical block ids of the same requests): insert this step's K/V only,

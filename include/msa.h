@@ -176,6 +176,45 @@ msa_status_t msa_kv_insert_quant(const msa_dims_t* dims, const void* k_new, cons
                                  const msa_kv_cache_t* cache, const msa_index_cache_t* idx_cache,
                                  uint32_t* dev_flags, void* stream);
 
+/* RMSNorm weights and rotary parameters of msa_qk_norm_rope_insert (host
+ * struct; the weights are device fp32 [D] arrays, 16-byte aligned). */
+typedef struct {
+  const float* q_weight;
+  const float* k_weight;
+  const float* idx_q_weight;   /* may be NULL when the call has no index rows */
+  const float* idx_k_weight;
+  float eps;                   /* >= 0 */
+  float rope_theta;            /* rotary base, > 1 */
+} msa_norm_rope_t;
+
+/*
+ * The step in front of the decode path, fused: per-head RMSNorm of the query,
+ * key, index-query and index-key projections, rotary position embedding, and
+ * insertion of the key, V and index key into the caches ("MiniMax-M3.1-Flash
+ * Day-0 対応", section "最適化と数値": QKV GEMM + norm + RoPE + KV insert;
+ * "MiniMax M3 vLLM サポート：…", section "カーネル融合": QKNorm + RoPE + KV
+ * insertion). The pages give no formulas; implemented (fp32, one CTA per token):
+ *   norm:  y_d = x_d / sqrt(mean_d(x^2) + eps) * w_d (IEEE sqrt and division);
+ *   RoPE:  for i < D/2, phi = position * rope_theta^(-2i/D) (angle in double
+ *          precision), (y_i, y_{i+D/2}) <- (y_i cos - y_{i+D/2} sin,
+ *          y_i sin + y_{i+D/2} cos) — all D dims, the two halves paired;
+ *   the results are rounded to bf16: q_out / idx_q_out receive them, and the
+ *   key and index key go through the cache quantisers of msa_kv_insert_quant
+ *   (as if inserted from those bf16 values); V is inserted unchanged.
+ * q: bf16 [T, H, D]; k, v: bf16 [T, G, D]; idx_q, idx_k: bf16 [T, I, D], both
+ * NULL for a layer that reuses another layer's selection (then idx_q_out,
+ * idx_cache and the index weights may be NULL and no index row is touched:
+ * "vLLM、AMD Instinct MI355X上で…", question 3). positions: int32 [T] (the
+ * token's position in its sequence). slot_mapping: as msa_kv_insert_quant.
+ * q_out: bf16 [T, H, D], idx_q_out: bf16 [T, I, D] (may alias q / idx_q). The
+ * index cache must be FP8 or NVFP4 (MSA_ERR_UNSUPPORTED otherwise).
+ */
+msa_status_t msa_qk_norm_rope_insert(const msa_dims_t* dims, const void* q, const void* k, const void* v,
+                                     const void* idx_q, const void* idx_k, const int32_t* positions,
+                                     const int64_t* slot_mapping, int32_t num_tokens, const msa_norm_rope_t* nr,
+                                     void* q_out, void* idx_q_out, const msa_kv_cache_t* cache,
+                                     const msa_index_cache_t* idx_cache, uint32_t* dev_flags, void* stream);
+
 /*
  * Stage 1, block scoring ("MSA 実行プロセス" step 1). For every request b,
  * position j, index head g and block n < l_j (the query's local block):
