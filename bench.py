@@ -216,26 +216,30 @@ def run_ours(args, world, rank, local):
         kernels launch back to back and overlap through programmatic dependent
         launch; "index": also around the index-score kernel (its duration for
         the roofline; the events cut the overlap on both sides of it); "all":
-        between every kernel (no overlap; the per-kernel breakdown)."""
+        between every kernel (no overlap; the per-kernel breakdown); "fused":
+        step boundaries only, selection and attention in one launch."""
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
         for s in range(n):
             flush(s)
             e = ev[s]
             e[0].record(stream)
             dw.insert_step_tokens()
-            if events != "step":
+            if events in ("index", "all"):
                 e[1].record(stream)
             dw.index_score()
-            if events != "step":
+            if events in ("index", "all"):
                 e[2].record(stream)
-            dw.select()
-            if events == "all":
-                e[3].record(stream)
-            dw.attend()
+            if events == "fused":
+                dw.select_attend()
+            else:
+                dw.select()
+                if events == "all":
+                    e[3].record(stream)
+                dw.attend()
             e[4].record(stream)
         torch.cuda.synchronize(dev)
         step = [ev[s][0].elapsed_time(ev[s][4]) for s in range(n)]
-        idx = [ev[s][1].elapsed_time(ev[s][2]) for s in range(n)] if events != "step" else None
+        idx = [ev[s][1].elapsed_time(ev[s][2]) for s in range(n)] if events in ("index", "all") else None
         per = None
         if events == "all":
             per = {nm: [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(n)] for i, nm in enumerate(names)}
@@ -254,6 +258,8 @@ def run_ours(args, world, rank, local):
     idx_step_ms, idx_launch_ms, _ = timed_steps(args.steps, "index")
     clk = clocks.stop()
     launches = args.steps * 4          # insert, index, select, attention (split-K combine fused)
+    # the same steps with selection and attention in one launch
+    fused_step_ms, _, _ = timed_steps(args.steps, "fused")
     # per-kernel breakdown, outside the timed region, with an event between every kernel
     _, _, per = timed_steps(min(args.steps, 50), "all")
     local_s = sum(step_ms) / 1e3
@@ -310,6 +316,7 @@ def run_ours(args, world, rank, local):
     if w.idx_dtype != "f32":
         # per launch: 20 launches back to back from one captured graph (a launch
         # marshalled from Python takes longer on the host than the kernel on the GPU)
+        dw.qk_norm_rope_insert()          # allocates its buffers outside the capture
         burst = dw.capture(lambda st: [dw.qk_norm_rope_insert(st) for _ in range(20)])
         for _ in range(args.warmup):
             burst.replay()
@@ -362,6 +369,9 @@ def run_ours(args, world, rank, local):
                      "timed_in": f"{args.steps} further steps with events around the kernel "
                                  f"({statistics.mean(idx_step_ms):.4f} ms per step there)"},
         "kernels_ms": {n: statistics.mean(v) for n, v in per.items()},
+        "fused_select_attend": {"value": B * Q / (statistics.mean(fused_step_ms) / 1e3), "unit": "query-tokens/s",
+                                "ms_per_step": statistics.mean(fused_step_ms),
+                                "what": "the step with selection and sparse GQA in one launch"},
         "sparse_gqa_roofline": {"achieved": ab / (att_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                                 "frac": ab / (att_ms / 1e3) / 1e9 / peak, "algorithmic_bytes_per_launch": ab,
                                 "traffic": att_traffic},

@@ -265,10 +265,10 @@ size_t msa_sparse_gqa_workspace_size(const msa_dims_t* dims, msa_dtype_t kv_dtyp
   return gqa_workspace_bytes(dims->batch, dims->q_len, dims->n_kv_heads, dims->topk);
 }
 
-msa_status_t msa_sparse_gqa_decode(const msa_dims_t* dims, const void* q, const msa_kv_cache_t* cache,
-                                   const int32_t* block_table, const int32_t* seq_lens, const int32_t* selected,
-                                   void* out, float* lse, void* workspace, size_t workspace_bytes,
-                                   uint32_t* dev_flags, void* stream) {
+static msa_status_t sparse_gqa_common(const msa_dims_t* dims, const void* q, const msa_kv_cache_t* cache,
+                                      const int32_t* block_table, const int32_t* seq_lens, const int32_t* selected,
+                                      const float* scores, void* out, float* lse, void* workspace,
+                                      size_t workspace_bytes, uint32_t* dev_flags, void* stream) {
   msa_status_t st = check_dims(dims);
   if (st != MSA_OK) return st;
   if (q == nullptr || cache == nullptr || cache->k == nullptr || cache->v == nullptr || block_table == nullptr ||
@@ -304,6 +304,7 @@ msa_status_t msa_sparse_gqa_decode(const msa_dims_t* dims, const void* q, const 
   a.block_table = block_table;
   a.seq_lens = seq_lens;
   a.selected = selected;
+  a.scores = scores;
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
   a.workspace = static_cast<float*>(workspace);
@@ -317,6 +318,23 @@ msa_status_t msa_sparse_gqa_decode(const msa_dims_t* dims, const void* q, const 
   a.K = dims->topk;
   a.softmax_scale = dims->softmax_scale;
   return cuda_status(launch_sparse_gqa(a, static_cast<cudaStream_t>(stream), &g_record));
+}
+
+msa_status_t msa_sparse_gqa_decode(const msa_dims_t* dims, const void* q, const msa_kv_cache_t* cache,
+                                   const int32_t* block_table, const int32_t* seq_lens, const int32_t* selected,
+                                   void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                   uint32_t* dev_flags, void* stream) {
+  return sparse_gqa_common(dims, q, cache, block_table, seq_lens, selected, nullptr, out, lse, workspace,
+                           workspace_bytes, dev_flags, stream);
+}
+
+msa_status_t msa_select_sparse_gqa_decode(const msa_dims_t* dims, const void* q, const msa_kv_cache_t* cache,
+                                          const int32_t* block_table, const int32_t* seq_lens, const float* scores,
+                                          int32_t* selected, void* out, float* lse, void* workspace,
+                                          size_t workspace_bytes, uint32_t* dev_flags, void* stream) {
+  if (scores == nullptr) return MSA_ERR_INVALID_ARG;
+  return sparse_gqa_common(dims, q, cache, block_table, seq_lens, selected, scores, out, lse, workspace,
+                           workspace_bytes, dev_flags, stream);
 }
 
 msa_status_t msa_read_device_flags(const uint32_t* dev_flags, uint32_t* host_flags, void* stream) {

@@ -99,7 +99,8 @@ struct GqaArgs {
   float k_global, v_global;
   const int32_t* block_table;
   const int32_t* seq_lens;
-  const int32_t* selected;  // [B, Q, G, K]
+  const int32_t* selected;  // [B, Q, G, K]; written first when scores is set
+  const float* scores;      // [B, Q, I, NB] or null (fused selection)
   uint16_t* out;            // bf16 [B, Q, H, D]
   float* lse;               // [B, Q, H] or null
   float* workspace;

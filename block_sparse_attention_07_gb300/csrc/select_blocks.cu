@@ -21,6 +21,7 @@
 //      `take` are the chosen blocks.
 //   4. The chosen ids plus the local block are written in ascending order.
 #include "msa_internal.h"
+#include "select_row.cuh"
 
 namespace msa {
 
@@ -37,23 +38,6 @@ struct SelParams {
   uint32_t* flags;
   int B, Q, I, NB, K;
 };
-
-// Monotone map fp32 -> uint32 (NaN is treated as -inf).
-__device__ __forceinline__ uint32_t order_key(float s) {
-  if (s != s) s = -INFINITY;
-  const uint32_t u = __float_as_uint(s);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ uint64_t make_key(float s, int n) {
-  return (static_cast<uint64_t>(order_key(s)) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - n);
-}
-
-__device__ __forceinline__ uint64_t shfl64(uint64_t v, int src) {
-  const uint32_t lo = __shfl_sync(kFullMask, static_cast<uint32_t>(v), src);
-  const uint32_t hi = __shfl_sync(kFullMask, static_cast<uint32_t>(v >> 32), src);
-  return (static_cast<uint64_t>(hi) << 32) | lo;
-}
 
 // Loads this thread's keys of batch `base` (0 where there is no candidate).
 __device__ __forceinline__ void load_batch(const float* row, int ell, int base, uint64_t (&k)[kBatch]) {

@@ -25,6 +25,7 @@
 #include <atomic>
 
 #include "msa_internal.h"
+#include "select_row.cuh"
 
 namespace msa {
 
@@ -57,6 +58,8 @@ struct GqaParams {
   const int32_t* block_table;
   const int32_t* seq_lens;
   const int32_t* selected;
+  const float* scores;          // non-null: the CTAs select their rows' blocks from these first
+  int32_t* sel_out;             // (and write them here; the same buffer as `selected`)
   uint16_t* out;
   float* lse;
   float* ws;
@@ -231,6 +234,27 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     x1 = p.W * (blockIdx.x + 1) / C;
   }
   if (x0 >= x1) return;
+
+  if (p.scores != nullptr) {
+    // Stage 2 inside this launch: every warp selects rows this CTA touches
+    // (rows shared with other CTAs get the same result from each), staging its
+    // survivors in the row-merge buffer, unused until a row ends.
+    uint64_t* surv = reinterpret_cast<uint64_t*>(sm + Ly.comb_o) + warp * (kWarpSurvCap + 8);
+    int* chosen = reinterpret_cast<int*>(surv + kWarpSurvCap);
+    const int64_t r_last = (x1 - 1) / p.K;
+    for (int64_t r = x0 / p.K + warp; r <= r_last; r += blockDim.x >> 5) {
+      const RowPos rp = row_pos(p, r);
+      const int64_t row_off = (static_cast<int64_t>(rp.b) * p.Q + rp.j) * p.G + rp.g;
+      int32_t* out = p.sel_out + row_off * p.K;
+      const int L = p.seq_lens[rp.b];
+      if (L < p.Q || L > p.NB * kBlock || L < 1) {           // (flagged by the item loads below)
+        for (int e = lane; e < p.K; e += 32) out[e] = -1;
+        continue;
+      }
+      warp_select_row(p.scores + row_off * p.NB, (L - p.Q + rp.j) / kBlock, p.K, out, surv, chosen, lane);
+    }
+    __syncthreads();                  // the item loads below read these rows back
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
@@ -822,6 +846,8 @@ cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRec
   p.block_table = a.block_table;
   p.seq_lens = a.seq_lens;
   p.selected = a.selected;
+  p.scores = a.scores;
+  p.sel_out = const_cast<int32_t*>(a.selected);
   p.out = a.out;
   p.lse = a.lse;
   p.ws = a.workspace;
@@ -872,7 +898,8 @@ cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRec
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   err = launch_pdl(kern, dim3(C), dim3(32 * (1 + kCWarps)), smem, stream, tk, tv, p);
-  rec->set("sparse_gqa %s persistent %s grid=%d block=%d smem=%zu stages=%d items=%lld",
+  rec->set("%ssparse_gqa %s persistent %s grid=%d block=%d smem=%zu stages=%d items=%lld",
+           a.scores != nullptr ? "select+" : "",
            a.nvfp4 ? "nvfp4_dequant_f16_mma" : a.fp8 ? "fp8_tma_cvt_f16_mma" : "bf16_tma_mma",
            p.row_aligned ? "whole_rows" : "split_k_fused_combine", C, 32 * (1 + kCWarps), smem,
            a.nvfp4 ? stages_for<kKvNvfp4>() : a.fp8 ? stages_for<kKvFp8>() : stages_for<kKvBf16>(),

@@ -25,7 +25,8 @@ FLAG_BAD_PAGE, FLAG_BAD_BLOCK, FLAG_BAD_SEQLEN, FLAG_BAD_SLOT, FLAG_TIMEOUT, FLA
 # Every function include/msa.h declares.
 EXPORTED = ("msa_abi_version", "msa_status_string", "msa_get_last_dispatch", "msa_kv_insert_quant",
             "msa_index_score", "msa_select_blocks", "msa_sparse_gqa_workspace_size", "msa_sparse_gqa_decode",
-            "msa_sparse_gqa_decode_noalloc", "msa_read_device_flags", "msa_qk_norm_rope_insert")
+            "msa_sparse_gqa_decode_noalloc", "msa_read_device_flags", "msa_qk_norm_rope_insert",
+            "msa_select_sparse_gqa_decode")
 
 
 class Dims(ctypes.Structure):
@@ -77,6 +78,8 @@ def _load():
     lib.msa_sparse_gqa_workspace_size.argtypes = [ctypes.POINTER(Dims), ctypes.c_int]
     lib.msa_sparse_gqa_decode.argtypes = [ctypes.POINTER(Dims), vp, ctypes.POINTER(_KVCache), vp, vp, vp, vp, vp,
                                           vp, sz, vp, vp]
+    lib.msa_select_sparse_gqa_decode.argtypes = [ctypes.POINTER(Dims), vp, ctypes.POINTER(_KVCache), vp, vp, vp,
+                                                 vp, vp, vp, vp, sz, vp, vp]
     lib.msa_sparse_gqa_decode_noalloc.argtypes = [ctypes.POINTER(Dims), vp, ctypes.POINTER(_KVCache), vp, vp, vp,
                                                   vp, vp, vp, vp]
     lib.msa_read_device_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
@@ -189,6 +192,16 @@ def kv_insert_quant(dims: Dims, k_new, v_new, idx_k_new, idx_new_dtype: int, slo
             int(k_new.shape[0]), ctypes.byref(kc), ctypes.byref(ic) if ic is not None else None, _ptr(flags),
             _stream(stream))
     return _call(lib.msa_kv_insert_quant, args, (dims, kc, ic), "msa_kv_insert_quant", prepare)
+
+
+def select_sparse_gqa_decode(dims: Dims, q, cache: KVCache, block_table, seq_lens, scores, selected, out, lse,
+                             workspace, flags, stream=None, prepare=False):
+    """Selection (written to ``selected``) and sparse GQA in one launch."""
+    kc = cache.c()
+    args = (ctypes.byref(dims), _ptr(q), ctypes.byref(kc), _ptr(block_table), _ptr(seq_lens), _ptr(scores),
+            _ptr(selected), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _ptr(flags), _stream(stream))
+    return _call(lib.msa_select_sparse_gqa_decode, args, (dims, kc), "msa_select_sparse_gqa_decode", prepare)
 
 
 def make_norm_rope(q_weight, k_weight, idx_q_weight=None, idx_k_weight=None, eps=1e-6, rope_theta=10000.0):

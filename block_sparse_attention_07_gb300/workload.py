@@ -129,6 +129,10 @@ class DeviceWorkload:
                                              self.selected, self.out, self.lse, self.workspace, self.flags,
                                              prepare=True))
             if self.has_index:
+                self._prep.update(select_attend=msa.select_sparse_gqa_decode(
+                    self.dims, self.q, self.cache, self.block_table_d, self.seq_lens_d, self.scores, self.selected,
+                    self.out, self.lse, self.workspace, self.flags, prepare=True))
+            if self.has_index:
                 self._prep.update(
                     index=msa.index_score(self.dims, self.q_idx, self.q_idx_dtype, self.idx_cache,
                                           self.block_table_d, self.seq_lens_d, self.scores, self.flags, prepare=True),
@@ -160,12 +164,25 @@ class DeviceWorkload:
                               self.selected if selected is None else selected, self.out, self.lse, self.workspace,
                               self.flags, stream)
 
+    def select_attend(self, stream=None):
+        """Selection and sparse GQA in one launch (the selection is written to ``selected``)."""
+        if stream is None:
+            return self.prepared()["select_attend"]()
+        msa.select_sparse_gqa_decode(self.dims, self.q, self.cache, self.block_table_d, self.seq_lens_d, self.scores,
+                                     self.selected, self.out, self.lse, self.workspace, self.flags, stream)
+
     def step(self, stream=None):
         """One decode step: insert this step's tokens, score, select, attend."""
         self.insert_step_tokens(stream)
         self.index_score(stream)
         self.select(stream)
         self.attend(stream)
+
+    def step_fused(self, stream=None):
+        """The same step with selection and attention in one launch."""
+        self.insert_step_tokens(stream)
+        self.index_score(stream)
+        self.select_attend(stream)
 
     # ------------------------------------------- fused norm / RoPE / insert --
     def _prologue_state(self):

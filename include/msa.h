@@ -268,6 +268,20 @@ msa_status_t msa_sparse_gqa_decode(const msa_dims_t* dims, const void* q, const 
                                    size_t workspace_bytes, uint32_t* dev_flags, void* stream);
 
 /*
+ * Stages 2 and 3 in one launch: the selection of msa_select_blocks, computed
+ * by the attention kernel's own CTAs from the block scores (one warp per row
+ * its CTA attends; the result is also written to `selected`, [B, Q, G, K]),
+ * followed by the sparse GQA decode of msa_sparse_gqa_decode over it. Saves
+ * the selection launch and its round trip on the latency path. Arguments as
+ * msa_sparse_gqa_decode, with scores (fp32 [B, Q, I, NB], as written by
+ * msa_index_score) as the input and selected as an output.
+ */
+msa_status_t msa_select_sparse_gqa_decode(const msa_dims_t* dims, const void* q, const msa_kv_cache_t* cache,
+                                          const int32_t* block_table, const int32_t* seq_lens, const float* scores,
+                                          int32_t* selected, void* out, float* lse, void* workspace,
+                                          size_t workspace_bytes, uint32_t* dev_flags, void* stream);
+
+/*
  * Allocation-free variant of msa_sparse_gqa_decode. The pages have no
  * counterpart: it exists for callers that cannot allocate device memory (a
  * process whose allocator owns all device memory, a plugin that receives only

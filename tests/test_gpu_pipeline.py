@@ -78,3 +78,13 @@ def test_full_size_sampled(name):
     dw.step()          # a second step (the benchmark repeats steps) gives the same result
     sample = [0, len(dw.which) - 1]
     parity.verify_workload(dw, w, lens, sample=sample, run_step=False)
+
+
+@pytest.mark.parametrize("name", ["b32_32k", "nvfp4_256k", "spec8", "fp8kv_32k"])
+def test_fused_select_attend_step(name):
+    """The step with selection and attention in one launch (msa_select_sparse_gqa_decode):
+    same checks, including the selection it writes back; NVFP4 rows are split over CTAs."""
+    w = REDUCED[name]
+    dw = parity.build(w)
+    dw.step_fused()
+    parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
