@@ -212,12 +212,14 @@ def run_ours(args, world, rank, local):
     names = ("insert", "index_score", "select", "sparse_gqa")
 
     def timed_steps(n, events):
-        """n steps. events "step": records only at step boundaries, so the four
+        """n steps. events "step": records only at step boundaries, so the
         kernels launch back to back and overlap through programmatic dependent
-        launch; "index": also around the index-score kernel (its duration for
-        the roofline; the events cut the overlap on both sides of it); "all":
-        between every kernel (no overlap; the per-kernel breakdown); "fused":
-        step boundaries only, selection and attention in one launch."""
+        launch (selection inside the attention launch where the workload's
+        step does that, ``dw.fuses_selection``); "index": the same, also around
+        the index-score kernel (its duration for the roofline; the events cut
+        the overlap on both sides of it); "other": step boundaries only, the
+        other composition; "all": four separate launches with events between
+        every kernel (no overlap; the per-kernel breakdown)."""
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
         for s in range(n):
             flush(s)
@@ -229,7 +231,9 @@ def run_ours(args, world, rank, local):
             dw.index_score()
             if events in ("index", "all"):
                 e[2].record(stream)
-            if events == "fused":
+            fused = dw.fuses_selection if events in ("step", "index") else (
+                not dw.fuses_selection if events == "other" else False)
+            if fused:
                 dw.select_attend()
             else:
                 dw.select()
@@ -257,9 +261,10 @@ def run_ours(args, world, rank, local):
     # the index-score kernel's launch duration (roofline), timed live over K more steps
     idx_step_ms, idx_launch_ms, _ = timed_steps(args.steps, "index")
     clk = clocks.stop()
-    launches = args.steps * 4          # insert, index, select, attention (split-K combine fused)
-    # the same steps with selection and attention in one launch
-    fused_step_ms, _, _ = timed_steps(args.steps, "fused")
+    # insert, index, [select,] attention (split-K combine fused)
+    launches = args.steps * (3 if dw.fuses_selection else 4)
+    # the same steps in the other composition (selection fused or separate)
+    other_step_ms, _, _ = timed_steps(args.steps, "other")
     # per-kernel breakdown, outside the timed region, with an event between every kernel
     _, _, per = timed_steps(min(args.steps, 50), "all")
     local_s = sum(step_ms) / 1e3
@@ -325,8 +330,11 @@ def run_ours(args, world, rank, local):
         def pro_step():
             dw.qk_norm_rope_insert()
             dw.index_score()
-            dw.select()
-            dw.attend()
+            if dw.fuses_selection:
+                dw.select_attend()
+            else:
+                dw.select()
+                dw.attend()
         pro_step_ms = event_timed(pro_step, args.steps)
         assert dw.check_flags() == 0, "device flags raised (fused norm/RoPE/insert)"
         dw.insert_step_tokens()           # restore the plain-insert cache contents
@@ -369,9 +377,11 @@ def run_ours(args, world, rank, local):
                      "timed_in": f"{args.steps} further steps with events around the kernel "
                                  f"({statistics.mean(idx_step_ms):.4f} ms per step there)"},
         "kernels_ms": {n: statistics.mean(v) for n, v in per.items()},
-        "fused_select_attend": {"value": B * Q / (statistics.mean(fused_step_ms) / 1e3), "unit": "query-tokens/s",
-                                "ms_per_step": statistics.mean(fused_step_ms),
-                                "what": "the step with selection and sparse GQA in one launch"},
+        "selection_in_attention_launch": dw.fuses_selection,
+        "other_composition": {"value": B * Q / (statistics.mean(other_step_ms) / 1e3), "unit": "query-tokens/s",
+                              "ms_per_step": statistics.mean(other_step_ms),
+                              "what": ("selection as its own launch" if dw.fuses_selection
+                                       else "selection inside the attention launch")},
         "sparse_gqa_roofline": {"achieved": ab / (att_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                                 "frac": ab / (att_ms / 1e3) / 1e9 / peak, "algorithmic_bytes_per_launch": ab,
                                 "traffic": att_traffic},

@@ -32,21 +32,41 @@ __device__ __forceinline__ uint64_t shfl64(uint64_t v, int src) {
 }
 
 constexpr int kWarpSurvCap = 128;   // survivors a warp stages in shared memory
+constexpr int kWarpBatch = 8;       // candidates per lane loaded together (independent loads in flight)
+
+// Keys of candidates base + lane + 32 u, u < kWarpBatch (0 past the row's end).
+__device__ __forceinline__ void warp_load_keys(const float* sr, int ell, int base, int lane,
+                                               uint64_t (&k)[kWarpBatch]) {
+  float v[kWarpBatch];
+#pragma unroll
+  for (int u = 0; u < kWarpBatch; ++u) {
+    const int n = base + lane + 32 * u;
+    v[u] = n < ell ? sr[n] : 0.f;
+  }
+#pragma unroll
+  for (int u = 0; u < kWarpBatch; ++u) {
+    const int n = base + lane + 32 * u;
+    k[u] = n < ell ? make_key(v[u], n) : 0ull;
+  }
+}
 
 // The warp's keys >= t compacted (in candidate order) into surv; returns their
 // number (only the first kWarpSurvCap are stored).
 __device__ __forceinline__ int warp_collect(const float* sr, int ell, uint64_t t, uint64_t* surv, int lane) {
   int s = 0;
-  for (int base = 0; base < ell; base += 32) {
-    const int n = base + lane;
-    const uint64_t k = n < ell ? make_key(sr[n], n) : 0ull;
-    const bool keep = k != 0ull && k >= t;
-    const uint32_t m = __ballot_sync(0xffffffffu, keep);
-    if (keep) {
-      const int at = s + __popc(m & ((1u << lane) - 1u));
-      if (at < kWarpSurvCap) surv[at] = k;
+  for (int base = 0; base < ell; base += 32 * kWarpBatch) {
+    uint64_t k[kWarpBatch];
+    warp_load_keys(sr, ell, base, lane, k);
+#pragma unroll
+    for (int u = 0; u < kWarpBatch; ++u) {
+      const bool keep = k[u] != 0ull && k[u] >= t;
+      const uint32_t m = __ballot_sync(0xffffffffu, keep);
+      if (keep) {
+        const int at = s + __popc(m & ((1u << lane) - 1u));
+        if (at < kWarpSurvCap) surv[at] = k[u];
+      }
+      s += __popc(m);
     }
-    s += __popc(m);
   }
   return s;
 }
@@ -62,9 +82,11 @@ static __device__ void warp_select_row(const float* sr, int ell, int K, int32_t*
     //    hold candidates) has take keys at or above it, so it bounds the row's
     //    take-th largest key from below
     uint64_t tmax = 0ull;
-    for (int n = lane; n < ell; n += 32) {
-      const uint64_t k = make_key(sr[n], n);
-      tmax = k > tmax ? k : tmax;
+    for (int base = 0; base < ell; base += 32 * kWarpBatch) {
+      uint64_t k[kWarpBatch];
+      warp_load_keys(sr, ell, base, lane, k);
+#pragma unroll
+      for (int u = 0; u < kWarpBatch; ++u) tmax = k[u] > tmax ? k[u] : tmax;
     }
     uint64_t t = 0ull;
     if (__popc(__ballot_sync(0xffffffffu, tmax != 0ull)) >= take) {
@@ -81,7 +103,12 @@ static __device__ void warp_select_row(const float* sr, int ell, int K, int32_t*
       for (int bit = 63; bit >= 0; --bit) {
         const uint64_t c = tx | (1ull << bit);
         int cnt = 0;
-        for (int n = lane; n < ell; n += 32) cnt += make_key(sr[n], n) >= c ? 1 : 0;
+        for (int base = 0; base < ell; base += 32 * kWarpBatch) {
+          uint64_t k[kWarpBatch];
+          warp_load_keys(sr, ell, base, lane, k);
+#pragma unroll
+          for (int u = 0; u < kWarpBatch; ++u) cnt += (k[u] != 0ull && k[u] >= c) ? 1 : 0;
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
         if (cnt >= take) tx = c;

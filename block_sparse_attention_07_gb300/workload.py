@@ -171,8 +171,23 @@ class DeviceWorkload:
         msa.select_sparse_gqa_decode(self.dims, self.q, self.cache, self.block_table_d, self.seq_lens_d, self.scores,
                                      self.selected, self.out, self.lse, self.workspace, self.flags, stream)
 
+    @property
+    def fuses_selection(self) -> bool:
+        """Whether ``step`` selects inside the attention launch: faster where the
+        attention CTAs own whole rows (bf16 and FP8 K/V); with NVFP4 K/V the
+        rows are split over CTAs and the separate selection launch is faster."""
+        return self.w.kv_dtype != "nvfp4"
+
     def step(self, stream=None):
-        """One decode step: insert this step's tokens, score, select, attend."""
+        """One decode step: insert this step's tokens, score, select, attend
+        (selection and attention in one launch where that is faster)."""
+        if self.fuses_selection:
+            self.step_fused(stream)
+        else:
+            self.step_separate(stream)
+
+    def step_separate(self, stream=None):
+        """The step with the selection as its own launch."""
         self.insert_step_tokens(stream)
         self.index_score(stream)
         self.select(stream)

@@ -98,3 +98,24 @@ def test_dispatch_record_names_the_variant():
     dwt = parity.build(wt)
     dwt.index_score()
     assert "index_score f32_fma" in msa.last_dispatch()
+
+
+def test_fused_selection_flags_bad_pages_and_lengths():
+    """The selection inside the attention launch meets the same invalid inputs:
+    a page id outside the cache and a request with an impossible length."""
+    w, dw = _small()
+    dw.step_fused()
+    assert dw.check_flags() == 0
+    dw.block_table_d[0, 3] = dw.num_pages + 7
+    dw.index_score()
+    dw.select_attend()
+    assert dw.check_flags() & msa.FLAG_BAD_PAGE
+    assert torch.isfinite(dw.out.float()).all()
+    dw.flags.zero_()
+    dw.block_table_d.copy_(torch.from_numpy(dw.block_table))
+    dw.seq_lens_d[1] = 0
+    dw.index_score()
+    dw.select_attend()
+    assert dw.check_flags() & msa.FLAG_BAD_SEQLEN
+    assert (dw.selected[1] == -1).all()
+    assert torch.isfinite(dw.out.float()).all()
