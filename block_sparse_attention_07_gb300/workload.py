@@ -103,10 +103,30 @@ class DeviceWorkload:
         self.selected = torch.empty((B, Q, I, w.topk), dtype=torch.int32, device=dev)
         self.out = torch.empty((B, Q, H, D), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((B, Q, H), dtype=torch.float32, device=dev)
+        self._pack_step_inputs()
         self._prep = None
         ws = msa.sparse_gqa_workspace_size(self.dims, self.cache.dtype)
         self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
         torch.cuda.synchronize(dev)
+
+    # Per-step inputs: what changes from one decode step to the next.
+    STEP_INPUTS = ("q", "q_idx", "new_k", "new_v", "new_idx", "new_slots", "block_table_d", "seq_lens_d")
+
+    def _pack_step_inputs(self):
+        """Places the per-step input tensors in one device buffer (256-byte
+        aligned views), so that a step's inputs arrive in one host-to-device copy
+        of ``step_inputs``."""
+        parts = [(n, getattr(self, n)) for n in self.STEP_INPUTS if getattr(self, n) is not None]
+        offs, total = [], 0
+        for _, t in parts:
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        buf = torch.empty(total, dtype=torch.uint8, device=self.device)
+        for (n, t), o in zip(parts, offs):
+            view = buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+            view.copy_(t)
+            setattr(self, n, view)
+        self.step_inputs = buf
 
     def _insert(self, k, v, idx, slots):
         dev = self.device
