@@ -421,74 +421,79 @@ __global__ void __launch_bounds__(kIdxThreads, kFp4Keys ? kFp4CtasPerSm : 1) ind
   }
 }
 
-// fp32 keys and queries (small workloads): one warp per (request, block, head);
-// each lane scores 4 tokens with plain fp32 FMAs.
-__global__ void __launch_bounds__(128) index_score_f32_kernel(IdxParams p) {
+// fp32 keys and queries (small workloads): one 128-thread CTA per (request,
+// block, index head). Thread t scores token t of the block against the Q
+// positions' index queries (in shared memory) with plain fp32 FMAs, eight
+// 16-byte loads of its key row in flight at a time; the block's maximum per
+// position is taken over the CTA by shuffles and shared memory.
+__global__ void __launch_bounds__(kBlock) index_score_f32_kernel(IdxParams p) {
   extern __shared__ __align__(16) uint8_t smem_f32[];
   uint8_t* smem = smem_f32;
   int* pref = reinterpret_cast<int*>(smem);
   float* qsh = reinterpret_cast<float*>(smem + ((static_cast<size_t>(p.B) + 1) * 4 + 15) / 16 * 16);
+  float* red = qsh + 8 * kDim;                      // [4 warps][8 positions]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_launch_dependents();
   griddep_wait();
   if (warp == 0) build_prefix(p, pref, blockIdx.x == 0);
   __syncthreads();
   fill_tails(p, pref);
-  float* qw = qsh + warp * 8 * kDim;
   const int64_t total = static_cast<int64_t>(pref[p.B]) * p.I;
-  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const float* qg = static_cast<const float*>(p.q);
   const float* keys = static_cast<const float*>(p.keys);
-  for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp; w < total; w += nwarps) {
-    const int64_t v = w / p.I;
-    const int g = static_cast<int>(w % p.I);
+  for (int64_t task = blockIdx.x; task < total; task += gridDim.x) {
+    const int64_t v = task / p.I;
+    const int g = static_cast<int>(task % p.I);
     const int b = find_request(pref, p.B, v);
     const int n = static_cast<int>(v - pref[b]);
     const int L = p.seq_lens[b];
-    __syncwarp();
-    for (int x = lane; x < p.Q * kDim; x += 32) {
+    __syncthreads();                                // previous task done with qsh / red
+    for (int x = threadIdx.x; x < p.Q * kDim; x += blockDim.x) {
       const int j = x / kDim, d = x % kDim;
-      qw[x] = qg[((static_cast<int64_t>(b) * p.Q + j) * p.I + g) * kDim + d];
+      qsh[x] = qg[((static_cast<int64_t>(b) * p.Q + j) * p.I + g) * kDim + d];
     }
-    __syncwarp();
+    __syncthreads();
     const int page = p.block_table[static_cast<int64_t>(b) * p.NB + n];
-    float best[8];
+    float dot[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) best[j] = -INFINITY;
-    if (page < 0 || page >= p.P) {
-      if (lane == 0) set_flag(p.flags, MSA_FLAG_BAD_PAGE);
+    for (int j = 0; j < 8; ++j) dot[j] = 0.f;
+    const bool ok = page >= 0 && page < p.P;
+    if (!ok) {
+      if (threadIdx.x == 0) set_flag(p.flags, MSA_FLAG_BAD_PAGE);
     } else {
-      for (int k = 0; k < 4; ++k) {
-        const float4* row = reinterpret_cast<const float4*>(
-            keys + ((static_cast<int64_t>(page) * p.I + g) * kBlock + lane + 32 * k) * kDim);
-        float dot[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int d4 = 0; d4 < kDim / 4; ++d4) {
-          const float4 kv = row[d4];
+      const float4* row = reinterpret_cast<const float4*>(
+          keys + ((static_cast<int64_t>(page) * p.I + g) * kBlock + threadIdx.x) * kDim);
+      for (int d8 = 0; d8 < kDim / 4; d8 += 8) {
+        float4 kv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) kv[u] = row[d8 + u];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             if (j < p.Q) {
-              const float* qj = qw + j * kDim + 4 * d4;
-              dot[j] = fmaf(kv.x, qj[0], dot[j]);
-              dot[j] = fmaf(kv.y, qj[1], dot[j]);
-              dot[j] = fmaf(kv.z, qj[2], dot[j]);
-              dot[j] = fmaf(kv.w, qj[3], dot[j]);
+              const float4 qj = *reinterpret_cast<const float4*>(qsh + j * kDim + 4 * (d8 + u));
+              dot[j] = fmaf(kv[u].x, qj.x, dot[j]);
+              dot[j] = fmaf(kv[u].y, qj.y, dot[j]);
+              dot[j] = fmaf(kv[u].z, qj.z, dot[j]);
+              dot[j] = fmaf(kv[u].w, qj.w, dot[j]);
             }
           }
         }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) best[j] = fmaxf(best[j], dot[j]);
       }
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      for (int o = 16; o > 0; o >>= 1) best[j] = fmaxf(best[j], __shfl_xor_sync(kFull, best[j], o));
-    if (lane < p.Q) {
-      float val = best[0];
-#pragma unroll
-      for (int j = 1; j < 8; ++j)
-        if (lane == j) val = best[j];
-      const int ell = (L - p.Q + lane) / kBlock;
-      p.scores[((static_cast<int64_t>(b) * p.Q + lane) * p.I + g) * p.NB + n] = n < ell ? val : -INFINITY;
+    for (int j = 0; j < 8; ++j) {
+      float m = ok ? dot[j] : -INFINITY;
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+      if (lane == 0) red[warp * 8 + j] = m;
+    }
+    __syncthreads();
+    if (threadIdx.x < p.Q) {
+      const int j = threadIdx.x;
+      const float val = fmaxf(fmaxf(red[j], red[8 + j]), fmaxf(red[16 + j], red[24 + j]));
+      const int ell = (L - p.Q + j) / kBlock;
+      p.scores[((static_cast<int64_t>(b) * p.Q + j) * p.I + g) * p.NB + n] = n < ell ? val : -INFINITY;
     }
   }
 }
@@ -517,14 +522,14 @@ cudaError_t launch_index_score(const IndexArgs& a, cudaStream_t stream, Dispatch
              !a.fp4 ? "fp8_mma_f16" : a.Q == 1 ? "nvfp4_group_cols_mma_f16" : "nvfp4_mma_f16", grid, block, smem,
              stages, a.Q, a.I);
   } else {
-    const size_t smem = ((static_cast<size_t>(a.B) + 1) * 4 + 15) / 16 * 16 + 4 * 8 * kDim * 4;
+    const size_t smem = ((static_cast<size_t>(a.B) + 1) * 4 + 15) / 16 * 16 + 8 * kDim * 4 + 4 * 8 * 4;
     err = cudaFuncSetAttribute(index_score_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    const int grid = sms * 4;
-    err = launch_pdl(index_score_f32_kernel, dim3(grid), dim3(128), smem, stream, p);
+    const int grid = sms * 8;                   // grid-stride over (request, block, head) tasks
+    err = launch_pdl(index_score_f32_kernel, dim3(grid), dim3(kBlock), smem, stream, p);
     if (err != cudaSuccess) return err;
-    rec->set("index_score f32_fma grid=%d block=128 smem=%zu q_len=%d idx_heads=%d", grid, smem, a.Q, a.I);
+    rec->set("index_score f32_fma grid=%d block=%d smem=%zu q_len=%d idx_heads=%d", grid, kBlock, smem, a.Q, a.I);
   }
   return cudaGetLastError();
 }
