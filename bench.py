@@ -46,8 +46,8 @@ FALLBACK_HBM_GBS = 6800.0
 # workload, keyed by the hash of the kernel's sources when it was measured (a
 # changed kernel reports null until it is measured again). Summaries: profiles/.
 NCU_TRAFFIC = {
-    ("index_score", "66e3ad521ee48e05"): 551617792 + 3014400,
-    ("sparse_gqa", "873f8d93a1275b31"): 134884096 + 58112,
+    ("index_score", "476114e664ac61d2"): 551623936 + 3188736,
+    ("sparse_gqa", "873f8d93a1275b31"): 135006976 + 123648,
 }
 
 
