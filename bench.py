@@ -378,7 +378,7 @@ def run_ours(args, world, rank, local):
     ab = attention_bytes(dw, sel)
     att_ms = statistics.mean(per["sparse_gqa"])
     traffic = NCU_TRAFFIC.get(("index_score", _src_hash("index_score.cu", "msa_device.cuh")))
-    att_traffic = NCU_TRAFFIC.get(("sparse_gqa", _src_hash("sparse_gqa.cu", "msa_device.cuh")))
+    att_traffic = NCU_TRAFFIC.get(("sparse_gqa", _src_hash("sparse_gqa.cu", "select_row.cuh", "msa_device.cuh")))
     if args.workload != "b32_32k" or args.batch:
         traffic = att_traffic = None          # the counters were taken on the default workload
     line = {
@@ -451,9 +451,69 @@ def cpu_baseline(w, n_requests, budget_s=20.0):
         done += 1
         if spent > budget_s:
             break
-    return {"value": done * w.q_len / spent, "unit": "query-tokens/s", "cores": 1, "kind": "oracle",
+    line = {"value": done * w.q_len / spent, "unit": "query-tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{done} of {w.batch} requests of the same workload, all stages, fp64 numpy, 1 thread",
             "seconds": spent}
+    try:
+        line["all_cores"] = cpu_all_cores(w)
+    except Exception as e:                     # reported, never fatal to the GPU figures
+        line["all_cores"] = {"error": f"{type(e).__name__}: {e}"}
+    return line
+
+
+def _oracle_worker(w, bs, barrier, out_q):
+    """One spawned process: builds its requests, waits for the others, then
+    runs them through the oracle (numpy with one BLAS thread)."""
+    from block_sparse_attention_07_gb300 import synth
+    from oracle import run as orun
+    lens = synth.seq_lens(w)
+    kg = synth.kv_scale(w)
+    idx_g = float(np.float32(synth.NVFP4_IDX_SYNTH_GLOBAL)) if w.idx_dtype == "nvfp4" else 1.0
+    reqs = [(b, synth.request(w, b, int(lens[b]))) for b in bs]
+    barrier.wait(timeout=900)
+    t0 = time.monotonic()
+    for b, req in reqs:
+        orun.run_request(req, int(lens[b]), w.topk, w.softmax_scale, w.block_size, w.idx_dtype, w.kv_dtype, kg, kg,
+                         idx_global=idx_g)
+    out_q.put((t0, time.monotonic(), len(reqs)))
+
+
+def cpu_all_cores(w, mem_budget=32 << 30):
+    """The same oracle on every host core: one spawned process per request (at
+    most one per core, and few enough that their fp64 working sets, about 32 KB
+    per context token, fit in mem_budget); wall clock from the first start to
+    the last finish, request generation excluded."""
+    import multiprocessing as mp
+    from block_sparse_attention_07_gb300 import synth
+    ctx = mp.get_context("spawn")
+    max_ctx = int(synth.seq_lens(w).max())
+    C = max(1, min(os.cpu_count() or 1, w.batch, mem_budget // max(1, max_ctx * 32 * 1024)))
+    barrier = ctx.Barrier(C)
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(w, [k], barrier, q), daemon=True) for k in range(C)]
+    for pr in procs:
+        pr.start()
+    import queue as _queue
+    res = []
+    deadline = time.monotonic() + 1800
+    try:
+        while len(res) < C:
+            try:
+                res.append(q.get(timeout=2))
+            except _queue.Empty:
+                if any(pr.exitcode not in (None, 0) for pr in procs) or time.monotonic() > deadline:
+                    raise RuntimeError("an oracle process failed or ran out of time")
+    finally:
+        for pr in procs:
+            pr.join(timeout=60)
+            if pr.is_alive():
+                pr.terminate()
+    wall = max(r[1] for r in res) - min(r[0] for r in res)
+    n = sum(r[2] for r in res)
+    return {"value": n * w.q_len / wall, "unit": "query-tokens/s", "cores": C, "kind": "oracle",
+            "sample": f"{n} of {w.batch} requests, one spawned process each (fp64 numpy, 1 BLAS thread per "
+                      f"process) on {os.cpu_count()} host cores",
+            "wall_s": wall}
 
 
 def run_reference(args, world, rank):

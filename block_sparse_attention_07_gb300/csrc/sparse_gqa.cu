@@ -181,6 +181,16 @@ __device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, int la
   return ok;
 }
 
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (bulk copy) writes to the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+
 __device__ __forceinline__ uint32_t swz(uint32_t box, int row, int chunk) {
   return box + row * 128 + ((chunk ^ (row & 7)) << 4);
 }
@@ -751,6 +761,33 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     return tile;
   };
 
+  // Zeroes the V rows of this warp's tokens that lie past the causal limit in
+  // the local block. Their probabilities are exactly 0, but a cache slot that
+  // has not been written yet may hold a NaN or infinity bit pattern, and
+  // 0 x NaN would reach the output through the P V product. kt: the tile
+  // (bf16 or expanded NVFP4: V in two 64-dim boxes; FP8: one 128-code box);
+  // async_tile: the tile is a stage that the next bulk copy overwrites.
+  auto clear_masked_v = [&](uint32_t kt, int it_blk, bool async_tile) {
+    if (it_blk != seg_ell) return;               // uniform over the warp
+    const int t = kTokPerWarp * w + lane;        // this lane's token row
+    if (it_blk * kBlock + t > seg_p) {
+      if (kFp8) {
+        const uint32_t row = kt + kFp8BoxBytes + static_cast<uint32_t>(t) * 128u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) st_shared_zero16(row + 16u * i);
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t row = kt + (2 + h) * kBoxBytes + static_cast<uint32_t>(t) * 128u;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) st_shared_zero16(row + 16u * i);
+        }
+      }
+      if (async_tile) fence_proxy_async_smem();
+    }
+    __syncwarp();
+  };
+
   // Item cursor: `cur` holds the infos of items base .. base + 31, `nxt` of the
   // 32 after them (loaded one chunk ahead).
   ItemInfo cur = load_item(p, x0 + lane, x1, false);
@@ -783,11 +820,13 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
       kt = expand(s);
       qk(kt, sc);
       softmax_prep(sc, it_blk);
+      clear_masked_v(kt, it_blk, false);
       softmax_pv(kt, sc);
     } else {
       if (!mbar_wait(smem_addr(&full[s]), phase)) { ok = false; break; }
       qk(kt, sc);
       softmax_prep(sc, it_blk);
+      clear_masked_v(kt, it_blk, true);
       softmax_pv(kt, sc);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&empty[s]));

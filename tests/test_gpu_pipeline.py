@@ -88,3 +88,61 @@ def test_fused_select_attend_step(name):
     dw = parity.build(w)
     dw.step_fused()
     parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
+
+
+def _poison_unwritten_slots(dw):
+    """Fills every cache slot past each request's length (the tail of its last
+    page, which no step has written) with NaN bit patterns: bf16 0xFFFF, E4M3
+    0xFF, NVFP4 block scales 0x7F (E4M3 NaN), fp32 NaN. The method reads none of
+    them: the indexer scores only whole blocks before the local one, and the
+    attention gives tokens past the causal limit probability 0."""
+    import torch
+    c, ic = dw.cache, dw.idx_cache
+    for bi, L in enumerate(dw.lens):
+        off = int(L) % 128
+        if off == 0:
+            continue
+        page = int(dw.block_table[bi, (int(L) - 1) // 128])
+        if c.k.dtype == torch.bfloat16:
+            c.k.view(torch.int16)[page, :, off:] = -1
+            c.v.view(torch.int16)[page, :, off:] = -1
+        else:
+            c.k[page, :, off:] = 0xFF
+            c.v[page, :, off:] = 0xFF
+            if c.k_scale is not None:
+                c.k_scale[page, :, off:] = 0x7F
+                c.v_scale[page, :, off:] = 0x7F
+        if ic.keys.dtype == torch.float32:
+            ic.keys[page, :, off:] = float("nan")
+        else:
+            ic.keys[page, :, off:] = 0xFF
+            if ic.scale is not None:
+                ic.scale[page, :, off:] = float("nan")
+            if ic.block_scale is not None:
+                ic.block_scale[page, :, off:] = 0x7F
+    torch.cuda.synchronize()
+
+
+NAN_TAIL = {
+    # (workload, selection inside the attention launch); no length is a multiple of 128
+    "bf16": (REDUCED["b32_32k"], False),
+    "bf16_fused": (REDUCED["b32_32k"], True),
+    "fp8kv_fused": (REDUCED["fp8kv_32k"], True),
+    "nvfp4": (REDUCED["nvfp4_256k"], False),
+    "spec8": (REDUCED["spec8"], True),
+    "spec8_fp8kv": (REDUCED["spec8_fp8kv"], False),
+    "tiny_f32": (synth.scaled(W["tiny"], ctx=3950), False),
+    "fp4idx": (REDUCED["b32_32k_fp4idx"], False),
+}
+
+
+@pytest.mark.parametrize("case", list(NAN_TAIL))
+def test_unwritten_slots_hold_nan(case):
+    """Outputs stay finite and match the oracle when the never-written slots of
+    the local page hold NaN patterns (a cache in reused memory)."""
+    w, fused = NAN_TAIL[case]
+    assert (synth.seq_lens(w) % 128 != 0).all()
+    dw = parity.build(w)
+    _poison_unwritten_slots(dw)
+    dw.step_fused() if fused else dw.step_separate()
+    parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
