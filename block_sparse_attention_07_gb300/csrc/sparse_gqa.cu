@@ -9,9 +9,7 @@
 //
 // Work items are (row, selection slot) pairs, row = (request, KV head,
 // position) with the positions of one (request, KV head) adjacent so that
-// shared pages are still in L2; a row's last slot (the local block of a full
-// selection) is processed first, so that when the selection runs inside the
-// launch the local block's copy overlaps it. A persistent grid gives each CTA a contiguous
+// shared pages are still in L2. A persistent grid gives each CTA a contiguous
 // item range; whenever the row changes inside the range the CTA merges its
 // four warps' online-softmax states and writes either the final output (the
 // CTA covered the whole row) or a partial (o, m, l) that the combine kernel
@@ -121,18 +119,13 @@ struct ItemInfo {
   int blk, page, valid, g;
 };
 
-// Selection slot of position e of a row: the last slot first (it holds the
-// local block whenever the selection is full, so its copy can start before the
-// selection is known), then slots 0 .. K - 2.
-__device__ __forceinline__ int slot_of(int e, int K) { return e == 0 ? K - 1 : e - 1; }
-
 // Selected block, page and validity of item x (x >= x1: an empty slot). Checks
 // the device-side invariants; only the producer reports problems.
 __device__ __forceinline__ ItemInfo load_item(const GqaParams& p, int64_t x, int64_t x1, bool report) {
   ItemInfo it{-1, -1, 0, 0};
   if (x >= x1) return it;
   const uint32_t r = static_cast<uint32_t>(x) / static_cast<uint32_t>(p.K);
-  const int e = slot_of(static_cast<int>(static_cast<uint32_t>(x) - r * static_cast<uint32_t>(p.K)), p.K);
+  const int e = static_cast<int>(static_cast<uint32_t>(x) - r * static_cast<uint32_t>(p.K));
   const RowPos rp = row_pos(p, r);
   it.g = rp.g;
   it.blk = p.selected[((static_cast<int64_t>(rp.b) * p.Q + rp.j) * p.G + rp.g) * p.K + e];
@@ -252,58 +245,14 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
   }
   if (x0 >= x1) return;
 
-  // Copies block page (KV head g) into stage s; lane 0 of the producer only.
-  const uint64_t pol = l2_evict_first_policy();
-  auto issue = [&](int s, int page, int g) {
-    const uint32_t fb = smem_addr(&full[s]);
-    const uint32_t dst = base_addr + Ly.stages + s * kStageBytes;
-    const int64_t ph = static_cast<int64_t>(page) * p.G + g;   // (page, kv head) slab
-    mbar_arrive_expect_tx(fb, kStageBytes);
-    if (kFp8) {
-      const int y = static_cast<int>(ph * kBlock);
-      tma_load_2d(dst, &tk, 0, y, fb);
-      tma_load_2d(dst + kFp8BoxBytes, &tv, 0, y, fb);
-    } else if (!kFp4) {
-      const int y = static_cast<int>(ph * kBlock);
-      tma_load_2d(dst, &tk, 0, y, fb);
-      tma_load_2d(dst + kBoxBytes, &tk, 64, y, fb);
-      tma_load_2d(dst + 2 * kBoxBytes, &tv, 0, y, fb);
-      tma_load_2d(dst + 3 * kBoxBytes, &tv, 64, y, fb);
-    } else {
-      constexpr uint32_t cb = kBlock * kDim / 2, sb = kBlock * kDim / 16;
-      bulk_g2s(dst, p.k4 + ph * cb, cb, fb, pol);
-      bulk_g2s(dst + cb, p.ks + ph * sb, sb, fb, pol);
-      bulk_g2s(dst + cb + sb, p.v4 + ph * cb, cb, fb, pol);
-      bulk_g2s(dst + 2 * cb + sb, p.vs + ph * sb, sb, fb, pol);
-    }
-  };
-
-  bool pre = false;   // producer: the first item's copy is already in stage 0
   if (p.scores != nullptr) {
-    // Stage 2 inside this launch: the consumer warps select the rows this CTA
-    // touches (rows shared with other CTAs get the same result from each),
-    // staging survivors in the row-merge buffer, unused until a row ends.
-    // Meanwhile the producer copies the first row's local block: when that
-    // row's selection is full (ell >= K - 1) its last slot, the first one
-    // processed, is the local block ell, whatever the scores.
-    if (warp == 0) {
-      if (x0 % p.K == 0) {
-        const RowPos rp = row_pos(p, x0 / p.K);
-        const int L = p.seq_lens[rp.b];
-        const int ell = (L - p.Q + rp.j) / kBlock;
-        if (!(L < p.Q || L > p.NB * kBlock || L < 1) && ell >= p.K - 1) {
-          const int page = p.block_table[static_cast<int64_t>(rp.b) * p.NB + ell];
-          if (page >= 0 && page < p.P) {
-            pre = true;
-            if (lane == 0) issue(0, page, rp.g);     // stage 0 is free: no wait
-          }
-        }
-      }
-    }
+    // Stage 2 inside this launch: every warp selects rows this CTA touches
+    // (rows shared with other CTAs get the same result from each), staging its
+    // survivors in the row-merge buffer, unused until a row ends.
     uint64_t* surv = reinterpret_cast<uint64_t*>(sm + Ly.comb_o) + warp * (kWarpSurvCap + 8);
     int* chosen = reinterpret_cast<int*>(surv + kWarpSurvCap);
     const int64_t r_last = (x1 - 1) / p.K;
-    for (int64_t r = x0 / p.K + warp - 1; warp > 0 && r <= r_last; r += kCWarps) {
+    for (int64_t r = x0 / p.K + warp; r <= r_last; r += blockDim.x >> 5) {
       const RowPos rp = row_pos(p, r);
       const int64_t row_off = (static_cast<int64_t>(rp.b) * p.Q + rp.j) * p.G + rp.g;
       int32_t* out = p.sel_out + row_off * p.K;
@@ -320,9 +269,8 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
     // The warp fetches the next 32 items' block, page and validity at once
-    // (one chunk ahead); lane 0 issues the copies. The consumers see the same
-    // validity for the pre-copied first item: the selection wrote ell into its
-    // slot, and the length and page checks are the ones made above.
+    // (one chunk ahead); lane 0 issues the copies.
+    const uint64_t pol = l2_evict_first_policy();
     ItemInfo cur = load_item(p, x0 + lane, x1, true);
     int64_t i = 0;
     int s = 0;
@@ -335,14 +283,32 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
         if (!__shfl_sync(kAll, cur.valid, k)) continue;
         const int page = __shfl_sync(kAll, cur.page, k);
         const int g = __shfl_sync(kAll, cur.g, k);
-        if (pre && base == x0 && k == 0) {
-          // copied before the selection
-        } else if (lane == 0) {
+        if (lane == 0) {
           if (!mbar_wait(smem_addr(&empty[s]), phase ^ 1u)) {
             set_flag(p.flags, MSA_FLAG_TIMEOUT);
             ok = false;
           } else {
-            issue(s, page, g);
+            const uint32_t fb = smem_addr(&full[s]);
+            const uint32_t dst = base_addr + Ly.stages + s * kStageBytes;
+            const int64_t ph = static_cast<int64_t>(page) * p.G + g;   // (page, kv head) slab
+            mbar_arrive_expect_tx(fb, kStageBytes);
+            if (kFp8) {
+              const int y = static_cast<int>(ph * kBlock);
+              tma_load_2d(dst, &tk, 0, y, fb);
+              tma_load_2d(dst + kFp8BoxBytes, &tv, 0, y, fb);
+            } else if (!kFp4) {
+              const int y = static_cast<int>(ph * kBlock);
+              tma_load_2d(dst, &tk, 0, y, fb);
+              tma_load_2d(dst + kBoxBytes, &tk, 64, y, fb);
+              tma_load_2d(dst + 2 * kBoxBytes, &tv, 0, y, fb);
+              tma_load_2d(dst + 3 * kBoxBytes, &tv, 64, y, fb);
+            } else {
+              constexpr uint32_t cb = kBlock * kDim / 2, sb = kBlock * kDim / 16;
+              bulk_g2s(dst, p.k4 + ph * cb, cb, fb, pol);
+              bulk_g2s(dst + cb, p.ks + ph * sb, sb, fb, pol);
+              bulk_g2s(dst + cb + sb, p.v4 + ph * cb, cb, fb, pol);
+              bulk_g2s(dst + 2 * cb + sb, p.vs + ph * sb, sb, fb, pol);
+            }
           }
         }
         ok = __shfl_sync(kAll, ok ? 1 : 0, 0) != 0;
