@@ -146,3 +146,28 @@ def test_unwritten_slots_hold_nan(case):
     _poison_unwritten_slots(dw)
     dw.step_fused() if fused else dw.step_separate()
     parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
+
+
+@pytest.mark.parametrize("name,fused", [("b32_32k", True), ("tiny", False), ("b32_32k_fp4idx", False),
+                                        ("spec8", True), ("spec8_fp4idx", False)])
+def test_scores_scale_exactly_with_index_queries(name, fused):
+    """Multiplying every index query by 2^k multiplies every block score by
+    exactly 2^k (products, fp32 sums and scale multiplies all commute with a
+    power of two) and so leaves every selection unchanged."""
+    import torch
+    w = REDUCED[name]
+    dw = parity.build(w)
+    run = dw.step_fused if fused else dw.step_separate
+    run()
+    torch.cuda.synchronize()
+    S0, sel0 = dw.scores.cpu().numpy().copy(), dw.selected.cpu().numpy().copy()
+    scale = 1.0
+    for k in (5, -3, -4):
+        dw.q_idx.mul_(2.0 ** k)
+        scale *= 2.0 ** k
+        run()
+        torch.cuda.synchronize()
+        assert dw.check_flags() == 0
+        assert np.array_equal(dw.selected.cpu().numpy(), sel0), f"selection changed at 2^{k}"
+        S = dw.scores.cpu().numpy()
+        assert np.array_equal(S, (S0 * np.float32(scale)).astype(np.float32)), f"scores not scaled exactly at 2^{k}"
