@@ -254,8 +254,11 @@ size_t msa_sparse_gqa_workspace_size(const msa_dims_t* dims, msa_dtype_t kv_dtyp
  *   out[b, j, h] = sum_t softmax_t(softmax_scale * q . k_t) * v_t
  *   lse[b, j, h] = log sum_t exp(softmax_scale * q . k_t)
  * The work is split over the selected blocks and the partial results merged
- * with a log-sum-exp combine. K/V are read from bf16 or NVFP4 pages and
- * dequantised in the kernel.
+ * with a log-sum-exp combine. K/V are read from bf16, FP8 E4M3 or NVFP4 pages
+ * and dequantised in the kernel. Cache slots past a position's causal limit
+ * never reach its result: their logits are masked and their V rows are zeroed
+ * before the P.V product. So slots that were never written, such as the tail
+ * of a request's last page, may hold any bytes, NaN patterns included.
  * q: bf16 [B, Q, H, D]. out: bf16 [B, Q, H, D]. lse: fp32 [B, Q, H] or NULL.
  * workspace: device scratch of at least msa_sparse_gqa_workspace_size bytes
  * (B * Q * G * (topk * 8,320 + 8)), 256-byte aligned: split-K partials and one
