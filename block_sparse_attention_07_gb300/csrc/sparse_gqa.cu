@@ -23,6 +23,8 @@
 #include <cuda.h>
 
 #include <atomic>
+#include <cstdlib>
+#include <cstring>
 
 #include "msa_internal.h"
 #include "select_row.cuh"
@@ -837,6 +839,483 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
   if (!ok && lane == 0) set_flag(p.flags, MSA_FLAG_TIMEOUT);
 }
 
+// ---------------------------------------------------------------------------
+// bf16 K/V on the fifth-generation tensor cores. The 16-head tile is below
+// tcgen05's minimum M, so both products run transposed:
+//   S^T = K Q^T   (M = 128 tokens, N = 16 heads, K = 128 dims)
+//   O^T = V^T P^T (M = 128 dims,   N = 16 heads, K = 128 tokens)
+// A is the TMA-loaded, 128-byte-swizzled K tile (K-major) or V tile (read
+// MN-major); B is the row's query or the block's probabilities, staged in
+// shared memory in the same swizzled K-major form. S (double-buffered) and O
+// accumulate in TMEM. One thread of the MMA warp issues the MMAs; its commits
+// release the K/V stage and the P buffer. The four softmax warps own one token
+// each of S (TMEM lane = token) and one head dim each of O (lane = dim).
+// Whole rows per CTA; every wait is bounded.
+
+constexpr int kTcWarps = 6;                      // producer, 4 softmax warps, MMA warp
+constexpr int kTcMmaWarp = 5;
+constexpr uint32_t kTcCols = 64;                 // TMEM columns: S[2] (16 each) + O (16)
+constexpr uint32_t kTcO = 32;                    // O's first column
+constexpr int kTcStages = 3;
+
+struct TcLayout {
+  uint32_t stages, q, p, red, vote, lsum, bars, tslot, total;
+};
+__host__ __device__ constexpr TcLayout tc_layout() {
+  TcLayout s{};
+  s.stages = 0;                                  // kTcStages x 64 KB (K lo, K hi, V lo, V hi)
+  s.q = s.stages + kTcStages * kTileBytes;       // 2 x 4 KB: query of the row, 16 heads x 128 dims
+  s.p = s.q + 2 * 4096;                          // 2 x 4 KB: P of the block, 16 heads x 128 tokens
+  s.red = s.p + 2 * 4096;                        // [2][4 warps][16] block maxima
+  s.vote = s.red + 2 * 4 * 16 * 4;               // [2][4] raise votes
+  s.lsum = s.vote + 2 * 4 * 4;                   // [4 warps][16] row sums
+  s.bars = s.lsum + 4 * 16 * 4;                  // 20 mbarriers
+  s.tslot = s.bars + 20 * 8;                     // TMEM base address
+  s.total = s.tslot + 16;
+  return s;
+}
+
+// Shared-memory matrix descriptor of a 128-byte-swizzled operand (the layout
+// the TMA boxes have: 16-byte chunk c of row r at ((c ^ (r & 7)) << 4), rows
+// 128 B apart, 8-row groups 1024 B apart): start address, leading and stride
+// byte offsets (16-byte units), descriptor version 1, swizzle mode 2.
+__device__ __forceinline__ uint64_t tc_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A/B
+// major-ness (0: K-major, 1: MN-major), N / 8, M / 16.
+__host__ __device__ constexpr uint32_t tc_idesc_bf16(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc ? 1 : 0) : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                 "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+               ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+                 "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+               : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_u16(uint32_t a, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+__global__ void __launch_bounds__(32 * kTcWarps, 1)
+    sparse_gqa_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, GqaParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  constexpr TcLayout Ly = tc_layout();
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base_addr = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base_addr - raw);
+  const uint32_t bars = base_addr + Ly.bars;
+  // mbarriers: full[3], empty[3], s_full[2], s_free[2], p_full[2], p_free[2], q_full[2], o_full, o_free, done
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (3 + s); };
+  auto s_full = [&](int b) { return bars + 8u * (6 + b); };
+  auto s_free = [&](int b) { return bars + 8u * (8 + b); };
+  auto p_full = [&](int b) { return bars + 8u * (10 + b); };
+  auto p_free = [&](int b) { return bars + 8u * (12 + b); };
+  auto q_full = [&](int b) { return bars + 8u * (14 + b); };
+  const uint32_t o_full = bars + 8u * 16, o_free = bars + 8u * 17, done_bar = bars + 8u * 18;
+  const uint32_t gbar = bars + 8u * 19;      // softmax-warp group sync (bounded, unlike bar.sync)
+  float* red = reinterpret_cast<float*>(sm + Ly.red);
+  volatile int* vote = reinterpret_cast<volatile int*>(sm + Ly.vote);
+  float* lsum = reinterpret_cast<float*>(sm + Ly.lsum);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);               // a commit after the block's P.V
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(s_free(b), kCWarps);
+      mbar_init(p_full(b), kCWarps);
+      mbar_init(p_free(b), 1);
+      mbar_init(q_full(b), kCWarps);
+    }
+    mbar_init(o_full, 1);
+    mbar_init(o_free, kCWarps);
+    mbar_init(done_bar, 1);
+    mbar_init(gbar, kCWarps);
+    fence_mbar_init();
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
+  }
+  if (warp == kTcMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(base_addr + Ly.tslot), "r"(kTcCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + Ly.tslot);
+  griddep_wait();
+
+  const int C = gridDim.x;
+  const int64_t rows_all = p.W / p.K;
+  const int64_t x0 = rows_all * blockIdx.x / C * p.K;
+  const int64_t x1 = rows_all * (blockIdx.x + 1) / C * p.K;
+  const int64_t r0 = x0 / p.K;
+
+  if (x0 < x1 && p.scores != nullptr) {
+    // Stage 2 inside this launch (as in the mma.sync kernel); the survivors go
+    // to the third stage, which no copy has been issued to yet.
+    uint64_t* surv = reinterpret_cast<uint64_t*>(sm + Ly.stages + 2 * kTileBytes) + warp * (kWarpSurvCap + 8);
+    int* chosen = reinterpret_cast<int*>(surv + kWarpSurvCap);
+    for (int64_t r = r0 + warp; r * p.K < x1; r += kTcWarps) {
+      const RowPos rp = row_pos(p, r);
+      const int64_t row_off = (static_cast<int64_t>(rp.b) * p.Q + rp.j) * p.G + rp.g;
+      int32_t* out = p.sel_out + row_off * p.K;
+      const int L = p.seq_lens[rp.b];
+      if (L < p.Q || L > p.NB * kBlock || L < 1) {
+        for (int e = lane; e < p.K; e += 32) out[e] = -1;
+        continue;
+      }
+      warp_select_row(p.scores + row_off * p.NB, (L - p.Q + rp.j) / kBlock, p.K, out, surv, chosen, lane);
+    }
+    __syncthreads();
+  }
+
+  bool ok = true;
+  if (x0 < x1 && warp == 0) {
+    // ------------------------------------------------------------ producer --
+    ItemInfo cur = load_item(p, x0 + lane, x1, true);
+    int64_t i = 0;
+    int s = 0;
+    uint32_t phase = 0;
+    for (int64_t base = x0; base < x1 && ok; base += 32) {
+      const ItemInfo nxt = load_item(p, base + 32 + lane, x1, true);
+      const int n = static_cast<int>(x1 - base < 32 ? x1 - base : 32);
+      for (int k = 0; k < n; ++k) {
+        if (!__shfl_sync(kAll, cur.valid, k)) continue;
+        const int page = __shfl_sync(kAll, cur.page, k);
+        const int g = __shfl_sync(kAll, cur.g, k);
+        if (lane == 0) {
+          if (!mbar_wait(empty(s), phase ^ 1u)) {
+            set_flag(p.flags, MSA_FLAG_TIMEOUT);
+            ok = false;
+          } else {
+            const uint32_t fb = full(s);
+            const uint32_t dst = base_addr + Ly.stages + s * kTileBytes;
+            const int y = static_cast<int>((static_cast<int64_t>(page) * p.G + g) * kBlock);
+            mbar_arrive_expect_tx(fb, kTileBytes);
+            tma_load_2d(dst, &tk, 0, y, fb);
+            tma_load_2d(dst + kBoxBytes, &tk, 64, y, fb);
+            tma_load_2d(dst + 2 * kBoxBytes, &tv, 0, y, fb);
+            tma_load_2d(dst + 3 * kBoxBytes, &tv, 64, y, fb);
+          }
+        }
+        ok = __shfl_sync(kAll, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        ++i;
+        if (++s == kTcStages) { s = 0; phase ^= 1u; }
+      }
+      cur = nxt;
+    }
+    if (lane == 0) {          // the last copies land before the CTA's teardown
+      const int64_t first = i > kTcStages ? i - kTcStages : 0;
+      for (int64_t k = first; k < i; ++k)
+        if (!mbar_wait(full(static_cast<int>(k % kTcStages)), static_cast<uint32_t>((k / kTcStages) & 1))) break;
+    }
+  } else if (x0 < x1 && warp == kTcMmaWarp) {
+    // ----------------------------------------------------------- MMA warp --
+    constexpr uint32_t id_qk = tc_idesc_bf16(128, 16, 0, 0);
+    constexpr uint32_t id_pv = tc_idesc_bf16(128, 16, 1, 0);
+    const bool leader = lane == 0;
+    ItemInfo cur = load_item(p, x0 + lane, x1, false);
+    ItemInfo nxt = load_item(p, x0 + 32 + lane, x1, false);
+    int64_t base = x0;
+    int kx = 0;
+    int64_t n = 0;                 // valid items so far
+    int64_t rv = 0;                // rows with a valid item so far
+    int64_t cur_row = -1;
+    bool row_first = true;
+    bool pend = false, pend_first = false;
+    int64_t pend_n = 0, pend_rv = 0;
+    auto issue_pv = [&](int64_t m, bool first, bool last, int64_t mrv) -> bool {
+      if (first && mrv >= 1 && !mbar_wait(o_free, static_cast<uint32_t>((mrv - 1) & 1))) return false;
+      if (!mbar_wait(p_full(static_cast<int>(m & 1)), static_cast<uint32_t>((m >> 1) & 1))) return false;
+      tc_fence_after();
+      if (leader) {
+        const uint32_t vt = base_addr + Ly.stages + static_cast<uint32_t>(m % kTcStages) * kTileBytes + 2 * kBoxBytes;
+        const uint32_t pt = base_addr + Ly.p + static_cast<uint32_t>(m & 1) * 4096u;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma(tmem + kTcO, tc_desc(vt + kk * 2048u, kBoxBytes, 1024), tc_desc(pt + (kk >> 2) * 2048u + (kk & 3) * 32u, 16, 1024),
+                 id_pv, !(first && kk == 0));
+        tc_commit(empty(static_cast<int>(m % kTcStages)));
+        tc_commit(p_free(static_cast<int>(m & 1)));
+        if (last) tc_commit(o_full);
+      }
+      __syncwarp();
+      return true;
+    };
+    while (ok && base + kx < x1) {
+      const int64_t x = base + kx;
+      const int valid = __shfl_sync(kAll, cur.valid, kx);
+      if (++kx == 32) {
+        kx = 0;
+        base += 32;
+        cur = nxt;
+        nxt = load_item(p, base + 32 + lane, x1, false);
+      }
+      const int64_t row = x / p.K;
+      if (row != cur_row) {
+        if (pend) { ok = issue_pv(pend_n, pend_first, true, pend_rv); pend = false; if (!ok) break; }
+        cur_row = row;
+        row_first = true;
+      }
+      if (!valid) continue;
+      const int64_t krow = row - r0;
+      const int s = static_cast<int>(n % kTcStages);
+      if (!mbar_wait(full(s), static_cast<uint32_t>((n / kTcStages) & 1))) { ok = false; break; }
+      if (row_first && !mbar_wait(q_full(static_cast<int>(krow & 1)), static_cast<uint32_t>((krow >> 1) & 1))) { ok = false; break; }
+      if (n >= 2 && !mbar_wait(s_free(static_cast<int>(n & 1)), static_cast<uint32_t>(((n - 2) >> 1) & 1))) { ok = false; break; }
+      tc_fence_after();
+      if (leader) {
+        const uint32_t kt = base_addr + Ly.stages + static_cast<uint32_t>(s) * kTileBytes;
+        const uint32_t qt = base_addr + Ly.q + static_cast<uint32_t>(krow & 1) * 4096u;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma(tmem + static_cast<uint32_t>(n & 1) * 16u,
+                 tc_desc(kt + (kk >> 2) * kBoxBytes + (kk & 3) * 32u, 16, 1024),
+                 tc_desc(qt + (kk >> 2) * 2048u + (kk & 3) * 32u, 16, 1024), id_qk, kk > 0);
+        tc_commit(s_full(static_cast<int>(n & 1)));
+      }
+      __syncwarp();
+      if (pend) { ok = issue_pv(pend_n, pend_first, false, pend_rv); if (!ok) break; }
+      if (row_first) ++rv;
+      pend = true; pend_n = n; pend_first = row_first; pend_rv = rv - 1;
+      row_first = false;
+      ++n;
+    }
+    if (ok && pend) ok = issue_pv(pend_n, pend_first, true, pend_rv);
+    if (leader) {             // every MMA has finished before TMEM is freed
+      tc_commit(done_bar);
+      mbar_wait(done_bar, 0);
+    }
+    __syncwarp();
+  } else if (x0 < x1) {
+    // ------------------------------------------------------- softmax warps --
+    const int sw = warp - 1;                 // 0 .. 3
+    const int ct = threadIdx.x - 32;         // 0 .. 127
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int t = 32 * (warp & 3) + lane;    // token of S / dim of O this thread owns
+    const float mul = p.scale_log2;
+    float m_ref[16], l_part[16];
+    int64_t seg_row = -1;
+    int seg_b = 0, seg_g = 0, seg_j = 0, seg_p = 0, seg_ell = 0;
+    bool seg_valid = false;
+    int64_t n = 0, rv = 0;
+    uint32_t gph = 0;
+    auto gsync = [&]() -> bool { return group_sync(gbar, gph, lane); };
+
+    auto begin_row = [&](int64_t r) {
+      const RowPos rp = row_pos(p, r);
+      seg_row = r;
+      seg_b = rp.b; seg_g = rp.g; seg_j = rp.j;
+      seg_p = p.seq_lens[rp.b] - p.Q + rp.j;
+      seg_ell = seg_p / kBlock;
+      seg_valid = false;
+#pragma unroll
+      for (int h = 0; h < 16; ++h) { m_ref[h] = -INFINITY; l_part[h] = 0.f; }
+      // the row's query, 16 heads x 128 dims, as the swizzled K-major B operand
+      const int64_t krow = r - r0;
+      const uint16_t* qh = p.q + ((static_cast<int64_t>(rp.b) * p.Q + rp.j) * p.H + static_cast<int64_t>(rp.g) * kGroup) * kDim;
+      const uint32_t qt = base_addr + Ly.q + static_cast<uint32_t>(krow & 1) * 4096u;
+      for (int i = ct; i < 256; i += 128) {
+        const int h = i >> 4, c = i & 15;
+        st_shared_v4(qt + (c >> 3) * 2048u + h * 128u + ((((c & 7) ^ (h & 7))) << 4),
+                     reinterpret_cast<const uint4*>(qh)[h * 16 + c]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_full(static_cast<int>(krow & 1)));
+    };
+    auto end_row = [&]() -> bool {
+      const int64_t head0 = (static_cast<int64_t>(seg_b) * p.Q + seg_j) * p.H + static_cast<int64_t>(seg_g) * kGroup;
+      float Lt[16];
+      uint32_t o[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) { Lt[h] = 0.f; o[h] = 0u; }
+      if (seg_valid) {
+        if (!mbar_wait(o_full, static_cast<uint32_t>((rv - 1) & 1))) return false;
+        tc_fence_after();
+        tc_ld16(tmem + kTcO + lane_base, o);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free);
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          float v = l_part[h];
+#pragma unroll
+          for (int s = 16; s > 0; s >>= 1) v += __shfl_xor_sync(kAll, v, s);
+          if (lane == 0) lsum[sw * 16 + h] = v;
+        }
+        if (!gsync()) return false;
+#pragma unroll
+        for (int h = 0; h < 16; ++h) Lt[h] = lsum[h] + lsum[16 + h] + lsum[32 + h] + lsum[48 + h];
+        if (!gsync()) return false;   // lsum is rewritten at the next row end
+      }
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        const float ll = seg_valid ? Lt[h] : 0.f;
+        const float v = ll > 0.f ? __uint_as_float(o[h]) / ll : 0.f;
+        p.out[(head0 + h) * kDim + t] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFF);
+        if (p.lse != nullptr && ct == h) p.lse[head0 + h] = ll > 0.f ? (m_ref[h] + log2f(ll)) * kLn2 : -INFINITY;
+      }
+      return true;
+    };
+
+    ItemInfo cur = load_item(p, x0 + lane, x1, false);
+    ItemInfo nxt = load_item(p, x0 + 32 + lane, x1, false);
+    int64_t base = x0;
+    int kx = 0;
+    bool row_first = true;
+    while (ok && base + kx < x1) {
+      const int64_t x = base + kx;
+      const int valid = __shfl_sync(kAll, cur.valid, kx);
+      const int it_blk = __shfl_sync(kAll, cur.blk, kx);
+      if (++kx == 32) {
+        kx = 0;
+        base += 32;
+        cur = nxt;
+        nxt = load_item(p, base + 32 + lane, x1, false);
+      }
+      const int64_t row = x / p.K;
+      if (row != seg_row) {
+        if (seg_row >= 0 && !end_row()) { ok = false; break; }
+        begin_row(row);
+        row_first = true;
+      }
+      if (!valid) continue;
+      if (!seg_valid) { seg_valid = true; ++rv; }
+      const int b2 = static_cast<int>(n & 1);
+      // S of this block: 16 heads of token t
+      if (!mbar_wait(s_full(b2), static_cast<uint32_t>((n >> 1) & 1))) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[16];
+      tc_ld16(tmem + static_cast<uint32_t>(b2) * 16u + lane_base, sr);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free(b2));
+      const bool masked = it_blk == seg_ell && it_blk * kBlock + t > seg_p;
+      float xs[16];
+      bool raise = false;
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        xs[h] = masked ? -INFINITY : __uint_as_float(sr[h]) * mul;
+        raise = raise || xs[h] > m_ref[h] + kRescaleSlack;
+      }
+      const uint32_t wv = __ballot_sync(kAll, raise);
+      if (lane == 0) vote[b2 * 4 + sw] = wv != 0u;
+      if (!gsync()) { ok = false; break; }
+      if (vote[b2 * 4] | vote[b2 * 4 + 1] | vote[b2 * 4 + 2] | vote[b2 * 4 + 3]) {
+        // exact block maxima per head, then a raised reference where they
+        // exceed it by more than the slack (uniform over the CTA)
+        float bm[16];
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          float v = xs[h];
+#pragma unroll
+          for (int s = 16; s > 0; s >>= 1) v = fmaxf(v, __shfl_xor_sync(kAll, v, s));
+          bm[h] = v;
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int h = 0; h < 16; ++h) red[(b2 * 4 + sw) * 16 + h] = bm[h];
+        }
+        if (!gsync()) { ok = false; break; }
+        float alpha[16];
+        bool any_alpha = false;
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          const float* rh = red + b2 * 64 + h;
+          const float M = fmaxf(fmaxf(rh[0], rh[16]), fmaxf(rh[32], rh[48]));
+          const float mn = M > m_ref[h] + kRescaleSlack ? M : m_ref[h];
+          alpha[h] = m_ref[h] == -INFINITY ? 0.f : ex2_approx(m_ref[h] - mn);
+          any_alpha = any_alpha || mn != m_ref[h];
+          m_ref[h] = mn;
+          l_part[h] *= alpha[h];
+        }
+        if (any_alpha && !row_first) {
+          // O *= alpha once the previous block's P.V has landed
+          if (!mbar_wait(p_free(static_cast<int>((n - 1) & 1)), static_cast<uint32_t>(((n - 1) >> 1) & 1))) { ok = false; break; }
+          tc_fence_after();
+          uint32_t o[16];
+          tc_ld16(tmem + kTcO + lane_base, o);
+#pragma unroll
+          for (int h = 0; h < 16; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+          tc_st16(tmem + kTcO + lane_base, o);
+          tc_fence_before();
+        }
+      }
+      // P of this block into the free P buffer (the P.V two blocks back has read it)
+      if (n >= 2 && !mbar_wait(p_free(b2), static_cast<uint32_t>(((n - 2) >> 1) & 1))) { ok = false; break; }
+      const uint32_t pt = base_addr + Ly.p + static_cast<uint32_t>(b2) * 4096u + static_cast<uint32_t>(t >> 6) * 2048u;
+      const int chunk = (t & 63) >> 3;
+      const uint32_t within = static_cast<uint32_t>(t & 7) * 2u;
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        const float pv = ex2_approx(xs[h] - m_ref[h]);
+        l_part[h] += pv;
+        st_shared_u16(pt + h * 128u + ((chunk ^ (h & 7)) << 4) + within,
+                      static_cast<uint16_t>(pack_bf16x2(pv, 0.f) & 0xFFFF));
+      }
+      if (masked) {
+        // a never-written slot may hold NaN: zero this token's V row, since
+        // 0 x NaN would reach O through the product
+        const uint32_t vrow = base_addr + Ly.stages + static_cast<uint32_t>(n % kTcStages) * kTileBytes +
+                              2 * kBoxBytes + static_cast<uint32_t>(t) * 128u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          st_shared_zero16(vrow + 16u * i);
+          st_shared_zero16(vrow + kBoxBytes + 16u * i);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full(b2));
+      row_first = false;
+      ++n;
+    }
+    if (ok && seg_row >= 0) ok = end_row();
+  }
+  if (!ok && lane == 0) set_flag(p.flags, MSA_FLAG_TIMEOUT);
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kTcMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcCols) : "memory");
+  }
+}
+
 size_t gqa_workspace_bytes(int B, int Q, int G, int K) {
   const size_t rows = static_cast<size_t>(B) * Q * G;
   return rows * K * kPartialFloats * sizeof(float) + rows * sizeof(unsigned long long);
@@ -877,6 +1356,17 @@ static cudaError_t make_kv_map(CUtensorMap* map, const void* base, int64_t rows,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The tcgen05 form of the bf16 tile is opt-in: MSA_BF16_ATTENTION=tcgen05 in
+// the environment when the call is made (read on every call, so a captured
+// graph keeps the kernel chosen at capture). With 16 heads per KV head its
+// per-block hand-offs (S in TMEM, a CTA-wide rescale vote, P through shared
+// memory) cost more than the register-resident mma.sync tile saves: on the
+// 32 x 32K bf16 workload the launch takes 46.7 us against 31.2.
+static bool bf16_tcgen05_selected() {
+  const char* e = getenv("MSA_BF16_ATTENTION");
+  return e != nullptr && strcmp(e, "tcgen05") == 0;
 }
 
 cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRecord* rec) {
@@ -933,6 +1423,16 @@ cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRec
   p.epoch = epoch.fetch_add(1);
   if (p.epoch == 0) p.epoch = epoch.fetch_add(1);    // 0 never tags a ticket
   p.tickets = reinterpret_cast<unsigned long long*>(a.workspace + (p.W / p.K) * p.K * kPartialFloats);
+  if (!a.nvfp4 && !a.fp8 && bf16_tcgen05_selected()) {
+    // bf16 K/V on the tcgen05 kernel, when selected (whole rows)
+    const size_t tsmem = tc_layout().total + 1024;
+    err = cudaFuncSetAttribute(sparse_gqa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(tsmem));
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(sparse_gqa_tc_kernel, dim3(C), dim3(32 * kTcWarps), tsmem, stream, tk, tv, p);
+    rec->set("%ssparse_gqa bf16_tma_tcgen05 persistent whole_rows grid=%d block=%d smem=%zu stages=%d items=%lld",
+             a.scores != nullptr ? "select+" : "", C, 32 * kTcWarps, tsmem, kTcStages, static_cast<long long>(p.W));
+    return err != cudaSuccess ? err : cudaGetLastError();
+  }
   auto kern = a.nvfp4 ? sparse_gqa_kernel<kKvNvfp4> : a.fp8 ? sparse_gqa_kernel<kKvFp8> : sparse_gqa_kernel<kKvBf16>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;

@@ -259,6 +259,11 @@ size_t msa_sparse_gqa_workspace_size(const msa_dims_t* dims, msa_dtype_t kv_dtyp
  * never reach its result: their logits are masked and their V rows are zeroed
  * before the P.V product. So slots that were never written, such as the tail
  * of a request's last page, may hold any bytes, NaN patterns included.
+ * For bf16 K/V the environment variable MSA_BF16_ATTENTION=tcgen05, read on
+ * every call, selects a tcgen05 form of the tile. It computes S^T = K.Q^T and
+ * O^T = V^T.P^T with S and O in tensor memory and gives the same results
+ * within the same tolerances, but it is slower at 16 heads per KV head. The
+ * default is the mma.sync tile.
  * q: bf16 [B, Q, H, D]. out: bf16 [B, Q, H, D]. lse: fp32 [B, Q, H] or NULL.
  * workspace: device scratch of at least msa_sparse_gqa_workspace_size bytes
  * (B * Q * G * (topk * 8,320 + 8)), 256-byte aligned: split-K partials and one

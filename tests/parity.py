@@ -136,3 +136,36 @@ def verify_workload(dw, w, full_lens, sample=None, heads=None, run_step=True):
         assert np.isneginf(S[bi, :, :, nb:]).all(), f"{where}: scores beyond the request not -inf"
         check_selection(sel[bi], ora["S"], L, w, gpu_S=S[bi, :, :, :nb], where=where)
         check_attention(out[bi], lse[bi], ora["out"], ora["lse"], where, heads=heads)
+
+
+def poison_unwritten_slots(dw):
+    """Fills every cache slot past each request's length (the tail of its last
+    page, which no step has written) with NaN bit patterns: bf16 0xFFFF, E4M3
+    0xFF, NVFP4 block scales 0x7F (E4M3 NaN), fp32 NaN. The method reads none of
+    them: the indexer scores only whole blocks before the local one, and the
+    attention gives tokens past the causal limit probability 0."""
+    import torch
+    c, ic = dw.cache, dw.idx_cache
+    for bi, L in enumerate(dw.lens):
+        off = int(L) % 128
+        if off == 0:
+            continue
+        page = int(dw.block_table[bi, (int(L) - 1) // 128])
+        if c.k.dtype == torch.bfloat16:
+            c.k.view(torch.int16)[page, :, off:] = -1
+            c.v.view(torch.int16)[page, :, off:] = -1
+        else:
+            c.k[page, :, off:] = 0xFF
+            c.v[page, :, off:] = 0xFF
+            if c.k_scale is not None:
+                c.k_scale[page, :, off:] = 0x7F
+                c.v_scale[page, :, off:] = 0x7F
+        if ic.keys.dtype == torch.float32:
+            ic.keys[page, :, off:] = float("nan")
+        else:
+            ic.keys[page, :, off:] = 0xFF
+            if ic.scale is not None:
+                ic.scale[page, :, off:] = float("nan")
+            if ic.block_scale is not None:
+                ic.block_scale[page, :, off:] = 0x7F
+    torch.cuda.synchronize()

@@ -90,39 +90,6 @@ def test_fused_select_attend_step(name):
     parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
 
 
-def _poison_unwritten_slots(dw):
-    """Fills every cache slot past each request's length (the tail of its last
-    page, which no step has written) with NaN bit patterns: bf16 0xFFFF, E4M3
-    0xFF, NVFP4 block scales 0x7F (E4M3 NaN), fp32 NaN. The method reads none of
-    them: the indexer scores only whole blocks before the local one, and the
-    attention gives tokens past the causal limit probability 0."""
-    import torch
-    c, ic = dw.cache, dw.idx_cache
-    for bi, L in enumerate(dw.lens):
-        off = int(L) % 128
-        if off == 0:
-            continue
-        page = int(dw.block_table[bi, (int(L) - 1) // 128])
-        if c.k.dtype == torch.bfloat16:
-            c.k.view(torch.int16)[page, :, off:] = -1
-            c.v.view(torch.int16)[page, :, off:] = -1
-        else:
-            c.k[page, :, off:] = 0xFF
-            c.v[page, :, off:] = 0xFF
-            if c.k_scale is not None:
-                c.k_scale[page, :, off:] = 0x7F
-                c.v_scale[page, :, off:] = 0x7F
-        if ic.keys.dtype == torch.float32:
-            ic.keys[page, :, off:] = float("nan")
-        else:
-            ic.keys[page, :, off:] = 0xFF
-            if ic.scale is not None:
-                ic.scale[page, :, off:] = float("nan")
-            if ic.block_scale is not None:
-                ic.block_scale[page, :, off:] = 0x7F
-    torch.cuda.synchronize()
-
-
 NAN_TAIL = {
     # (workload, selection inside the attention launch); no length is a multiple of 128
     "bf16": (REDUCED["b32_32k"], False),
@@ -143,7 +110,7 @@ def test_unwritten_slots_hold_nan(case):
     w, fused = NAN_TAIL[case]
     assert (synth.seq_lens(w) % 128 != 0).all()
     dw = parity.build(w)
-    _poison_unwritten_slots(dw)
+    parity.poison_unwritten_slots(dw)
     dw.step_fused() if fused else dw.step_separate()
     parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
 
