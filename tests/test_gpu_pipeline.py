@@ -138,3 +138,46 @@ def test_scores_scale_exactly_with_index_queries(name, fused):
         assert np.array_equal(dw.selected.cpu().numpy(), sel0), f"selection changed at 2^{k}"
         S = dw.scores.cpu().numpy()
         assert np.array_equal(S, (S0 * np.float32(scale)).astype(np.float32)), f"scores not scaled exactly at 2^{k}"
+
+
+QLENS = {
+    # query positions between 1 and 8: the index kernel's unused mma columns,
+    # per-position causal limits (some straddling a block boundary), and the
+    # per-position selections and attention rows
+    "q2_bf16": synth.scaled(W["spec8"], batch=3, ctx=2946, q_len=2),
+    "q3_bf16": synth.scaled(W["spec8"], batch=3, ctx=2947, q_len=3),
+    "q5_fp8kv": synth.scaled(W["spec8"], batch=2, ctx=2693, q_len=5, kv_dtype="fp8"),
+    "q7_bf16": synth.scaled(W["spec8"], batch=2, ctx=2950, q_len=7),
+    "q3_fp4idx": synth.scaled(W["spec8"], batch=3, ctx=2305, q_len=3, idx_dtype="nvfp4"),
+    "q2_nvfp4kv": synth.scaled(W["nvfp4_256k"], batch=2, ctx=3001, q_len=2),
+}
+
+
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("case", list(QLENS))
+def test_query_lengths(case, fused):
+    w = QLENS[case]
+    dw = parity.build(w)
+    dw.step_fused() if fused else dw.step_separate()
+    parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
+
+
+HEADS = {
+    # 1 to 3 KV heads (index heads = KV heads, 16 query heads each): the index
+    # kernel's consumer warps, page strides and every row enumeration follow G
+    "g1": synth.scaled(W["b32_32k"], batch=3, ctx=2100, n_heads=16, n_kv_heads=1, n_idx_heads=1),
+    "g2_spec": synth.scaled(W["spec8"], batch=2, ctx=2951, n_heads=32, n_kv_heads=2, n_idx_heads=2),
+    "g3_fp4idx": synth.scaled(W["b32_32k_fp4idx"], batch=2, ctx=2400, n_heads=48, n_kv_heads=3, n_idx_heads=3),
+    "g2_nvfp4kv": synth.scaled(W["nvfp4_256k"], batch=2, ctx=2700, n_heads=32, n_kv_heads=2, n_idx_heads=2),
+    "g3_fp8kv": synth.scaled(W["fp8kv_32k"], batch=2, ctx=2300, n_heads=48, n_kv_heads=3, n_idx_heads=3),
+    "g1_tiny_f32": synth.scaled(W["tiny"], ctx=1500, n_heads=16, n_kv_heads=1, n_idx_heads=1),
+}
+
+
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("case", list(HEADS))
+def test_head_counts(case, fused):
+    w = HEADS[case]
+    dw = parity.build(w)
+    dw.step_fused() if fused else dw.step_separate()
+    parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)

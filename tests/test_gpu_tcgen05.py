@@ -39,6 +39,14 @@ def test_edge_lengths(tcgen05):
     parity.verify_workload(dw, w, lens, run_step=False)
 
 
+def test_two_kv_heads_three_positions(tcgen05):
+    w = synth.scaled(W["spec8"], batch=2, ctx=2947, q_len=3, n_heads=32, n_kv_heads=2, n_idx_heads=2)
+    dw = parity.build(w)
+    dw.step_fused()
+    assert "bf16_tma_tcgen05" in msa.last_dispatch()
+    parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
+
+
 def test_unwritten_slots_hold_nan(tcgen05):
     w = REDUCED["spec8"]
     dw = parity.build(w)
