@@ -86,8 +86,8 @@ def _load():
     lib.msa_qk_norm_rope_insert.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, vp, vp, vp, vp, i32,
                                             ctypes.POINTER(NormRope), vp, vp, ctypes.POINTER(_KVCache),
                                             ctypes.POINTER(_IndexCache), vp, vp]
-    for name in EXPORTED:
-        if name != "msa_abi_version" and name != "msa_status_string":
+    for name in EXPORTED:       # every other entry point returns msa_status_t
+        if name not in ("msa_abi_version", "msa_status_string", "msa_sparse_gqa_workspace_size"):
             getattr(lib, name).restype = ctypes.c_int
     return lib
 

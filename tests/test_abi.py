@@ -106,3 +106,27 @@ def test_dtype_combinations_rejected(m):
 
 def test_dispatch_record_before_any_launch(m):
     assert isinstance(m.last_dispatch(), str)
+
+
+def test_empty_inserts_launch_nothing(m):
+    """Zero new tokens is a valid call that launches nothing (checked before any
+    device pointer is touched, so it runs here without a GPU)."""
+    lib = m.lib
+    d = m.make_dims(2, 1, max_blocks_per_seq=4, num_pages=8)
+    fake = ctypes.c_void_p(0x10000)
+    kc = m._KVCache(m.BF16, fake, fake, None, None, 1.0, 1.0)
+    assert lib.msa_kv_insert_quant(ctypes.byref(d), None, None, None, m.BF16, None, 0, ctypes.byref(kc), None,
+                                   fake, None) == m.OK
+    assert m.last_dispatch() == "kv_insert empty"
+    assert lib.msa_kv_insert_quant(ctypes.byref(d), None, None, None, m.BF16, None, -1, ctypes.byref(kc), None,
+                                   fake, None) == m.ERR_INVALID_ARG
+
+
+def test_workspace_size_above_4_gib(m):
+    """The workspace size is a size_t all the way to Python: the largest shapes
+    the API takes need more than 2^32 bytes."""
+    d = m.make_dims(4096, 8, max_blocks_per_seq=4, num_pages=8)
+    rows = 4096 * 8 * 4
+    assert m.sparse_gqa_workspace_size(d, m.BF16) == rows * (16 * (16 * 128 + 32) * 4 + 8)
+    assert m.sparse_gqa_workspace_size(d, m.BF16) > 2 ** 32
+

@@ -181,3 +181,15 @@ def test_head_counts(case, fused):
     dw = parity.build(w)
     dw.step_fused() if fused else dw.step_separate()
     parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
+
+
+@pytest.mark.parametrize("base", ["b32_32k", "b32_32k_fp4idx"])
+def test_max_batch(base):
+    """The largest batch the API takes (4,096 requests) with short contexts. This
+    exercises the index kernel's per-request prefix (16 KB of shared memory at
+    this batch), every row enumeration and the selection padding (2 candidates
+    for 15 slots). Sampled requests are checked."""
+    w = synth.scaled(W[base], batch=4096, ctx=260)
+    dw = parity.build(w)
+    dw.step()
+    parity.verify_workload(dw, w, synth.seq_lens(w), sample=[0, 1, 2047, 4095], run_step=False)
