@@ -183,12 +183,13 @@ def test_head_counts(case, fused):
     parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
 
 
-@pytest.mark.parametrize("base", ["b32_32k", "b32_32k_fp4idx"])
+@pytest.mark.parametrize("base", ["b32_32k", "b32_32k_fp4idx", "spec8", "nvfp4_256k"])
 def test_max_batch(base):
     """The largest batch the API takes (4,096 requests) with short contexts. This
     exercises the index kernel's per-request prefix (16 KB of shared memory at
     this batch), every row enumeration and the selection padding (2 candidates
-    for 15 slots). Sampled requests are checked."""
+    for 15 slots). With 8 positions there are 131,072 attention rows and the
+    split-K workspace is over 4 GiB. Sampled requests are checked."""
     w = synth.scaled(W[base], batch=4096, ctx=260)
     dw = parity.build(w)
     dw.step()
