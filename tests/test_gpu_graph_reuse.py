@@ -87,3 +87,30 @@ def test_layer_reusing_selection(name, graph):
         parity.check_attention(out[bi], lse[bi], ora["out"], ora["lse"], f"{w.name} layer 1 b={b}")
     # a different layer really attends over different data
     assert not torch.equal(layer.out, src.out)
+
+
+def test_two_streams_at_once():
+    """Two independent decode steps in flight on two streams at once: an NVFP4
+    one whose rows are merged through tickets, and a bf16 one. Each has its own
+    workspace and caches, and both must still match the oracle and repeat
+    bit for bit."""
+    wa = synth.scaled(W["nvfp4_256k"], batch=2, ctx=3000)
+    wb = synth.scaled(W["b32_32k"], batch=3, ctx=2000)
+    da, db = parity.build(wa), parity.build(wb)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    firsts = None
+    for it in range(4):
+        with torch.cuda.stream(sa):
+            da.step_separate(sa)
+        with torch.cuda.stream(sb):
+            db.step_fused(sb)
+        torch.cuda.synchronize()
+        now = [t.clone() for t in (da.out, da.lse, db.out, db.lse)]
+        if firsts is None:
+            firsts = now
+        else:
+            for x, y in zip(firsts, now):
+                assert torch.equal(x, y)
+    parity.verify_workload(da, wa, synth.seq_lens(wa), run_step=False)
+    parity.verify_workload(db, wb, synth.seq_lens(wb), run_step=False)
