@@ -194,3 +194,23 @@ def test_max_batch(base):
     dw = parity.build(w)
     dw.step()
     parity.verify_workload(dw, w, synth.seq_lens(w), sample=[0, 1, 2047, 4095], run_step=False)
+
+
+@pytest.mark.parametrize("name", ["b32_32k", "fp8kv_32k", "nvfp4_256k", "spec8"])
+def test_large_logits(name, monkeypatch):
+    """Attention queries scaled by 2^6 (exact in bf16) on both sides. Logits reach a
+    few hundred, the softmax is nearly one-hot, and the running maximum rises by
+    more than the rescale slack on most blocks. So the output rescale path runs far
+    more often than on unit-scale data."""
+    plain = synth.request
+
+    def scaled_request(w, b, length):
+        r = dict(plain(w, b, length))
+        r["q"] = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(r["q"]) * np.float32(64.0))
+        return r
+
+    monkeypatch.setattr(synth, "request", scaled_request)
+    w = REDUCED[name]
+    dw = parity.build(w)
+    dw.step()
+    parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
