@@ -46,7 +46,7 @@ FALLBACK_HBM_GBS = 6800.0
 # workload, keyed by the hash of the kernel's sources when it was measured (a
 # changed kernel reports null until it is measured again). Summaries: profiles/.
 NCU_TRAFFIC = {
-    ("index_score", "476114e664ac61d2"): 551623936 + 3188736,
+    ("index_score", "0b53ac867cdc1428"): 551638016 + 157440,
     ("sparse_gqa", "a1d657ef6852a159"): 134992128 + 123648,
 }
 
@@ -214,24 +214,30 @@ def run_ours(args, world, rank, local):
     def timed_steps(n, events):
         """n steps. events "step": records only at step boundaries, so the
         kernels launch back to back and overlap through programmatic dependent
-        launch (selection inside the attention launch where the workload's
-        step does that, ``dw.fuses_selection``); "index": the same, also around
-        the index-score kernel (its duration for the roofline; the events cut
-        the overlap on both sides of it); "other": step boundaries only, the
-        other composition; "all": four separate launches with events between
-        every kernel (no overlap; the per-kernel breakdown)."""
+        launch (the insert inside the index launch and the selection inside the
+        attention launch where the workload's step does that,
+        ``dw.merges_insert`` / ``dw.fuses_selection``); "index": the insert as
+        its own launch, with events around the index-score kernel (its duration
+        for the roofline; the events cut the overlap on both sides of it);
+        "other": step boundaries only, the other selection composition;
+        "unmerged": step boundaries only, the insert as its own launch; "all":
+        four separate launches with events between every kernel (no overlap;
+        the per-kernel breakdown)."""
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
         for s in range(n):
             flush(s)
             e = ev[s]
             e[0].record(stream)
-            dw.insert_step_tokens()
-            if events in ("index", "all"):
-                e[1].record(stream)
-            dw.index_score()
-            if events in ("index", "all"):
-                e[2].record(stream)
-            fused = dw.fuses_selection if events in ("step", "index") else (
+            if dw.merges_insert and events in ("step", "other"):
+                dw.insert_index_score()
+            else:
+                dw.insert_step_tokens()
+                if events in ("index", "all"):
+                    e[1].record(stream)
+                dw.index_score()
+                if events in ("index", "all"):
+                    e[2].record(stream)
+            fused = dw.fuses_selection if events in ("step", "index", "unmerged") else (
                 not dw.fuses_selection if events == "other" else False)
             if fused:
                 dw.select_attend()
@@ -261,10 +267,12 @@ def run_ours(args, world, rank, local):
     # the index-score kernel's launch duration (roofline), timed live over K more steps
     idx_step_ms, idx_launch_ms, _ = timed_steps(args.steps, "index")
     clk = clocks.stop()
-    # insert, index, [select,] attention (split-K combine fused)
-    launches = args.steps * (3 if dw.fuses_selection else 4)
+    # [insert,] index, [select,] attention (split-K combine fused)
+    launches = args.steps * ((1 if dw.merges_insert else 2) + (1 if dw.fuses_selection else 2))
     # the same steps in the other composition (selection fused or separate)
     other_step_ms, _, _ = timed_steps(args.steps, "other")
+    # the same steps with the insert as its own launch
+    unmerged_step_ms = timed_steps(args.steps, "unmerged")[0] if dw.merges_insert else None
     # per-kernel breakdown, outside the timed region, with an event between every kernel
     _, _, per = timed_steps(min(args.steps, 50), "all")
     local_s = sum(step_ms) / 1e3
@@ -377,7 +385,7 @@ def run_ours(args, world, rank, local):
     sel = dw.selected.cpu().numpy()
     ab = attention_bytes(dw, sel)
     att_ms = statistics.mean(per["sparse_gqa"])
-    traffic = NCU_TRAFFIC.get(("index_score", _src_hash("index_score.cu", "msa_device.cuh")))
+    traffic = NCU_TRAFFIC.get(("index_score", _src_hash("index_score.cu", "insert_rows.cuh", "msa_device.cuh")))
     att_traffic = NCU_TRAFFIC.get(("sparse_gqa", _src_hash("sparse_gqa.cu", "select_row.cuh", "msa_device.cuh")))
     if args.workload != "b32_32k" or args.batch:
         traffic = att_traffic = None          # the counters were taken on the default workload
@@ -390,10 +398,15 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "hbm", "kernel": "index_score", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic,
                      "algorithmic_bytes_per_launch": ib, "avg_launch_ms": idx_ms,
-                     "timed_in": f"{args.steps} further steps with events around the kernel "
+                     "timed_in": f"{args.steps} further steps (insert as its own launch) with events around the kernel "
                                  f"({statistics.mean(idx_step_ms):.4f} ms per step there)"},
         "kernels_ms": {n: statistics.mean(v) for n, v in per.items()},
         "selection_in_attention_launch": dw.fuses_selection,
+        "insert_in_index_launch": dw.merges_insert,
+        "insert_as_own_launch": (None if unmerged_step_ms is None else
+                                 {"value": B * Q / (statistics.mean(unmerged_step_ms) / 1e3),
+                                  "unit": "query-tokens/s", "ms_per_step": statistics.mean(unmerged_step_ms),
+                                  "what": "the same step with the insert as its own launch"}),
         "other_composition": {"value": B * Q / (statistics.mean(other_step_ms) / 1e3), "unit": "query-tokens/s",
                               "ms_per_step": statistics.mean(other_step_ms),
                               "what": ("selection as its own launch" if dw.fuses_selection
@@ -409,7 +422,7 @@ def run_ours(args, world, rank, local):
                 "eager_value": B * Q * args.steps * world / e2e_eager_tot},
         "graph": {"value": B * Q / (statistics.mean(graph_ms) / 1e3), "unit": "query-tokens/s",
                   "ms_per_step": statistics.mean(graph_ms),
-                  "what": "the same step (4 kernels) replayed from one captured CUDA graph per step"},
+                  "what": "the same step replayed from one captured CUDA graph per step"},
         "gpu_launches": launches,
         "clocks": clk,
         "wall_s_timed_region": wall,

@@ -23,7 +23,7 @@
 // runs of a key row. The warps of a head merge their column maxima through a
 // shared-memory slot per stage: the last to arrive (by a ticket counter) writes
 // the score, so none waits for another.
-#include "msa_internal.h"
+#include "insert_rows.cuh"
 
 namespace msa {
 
@@ -46,7 +46,37 @@ struct IdxParams {
   uint32_t* flags;
   float global_scale;       // NVFP4 keys: fp32 per-tensor scale
   int B, Q, I, NB, P;
+  int ins_on;               // 1: also insert the step's new tokens (one per request, Q = 1)
+  InsertParams ins;
 };
+
+// The insert fused into the index launch (one query position): token t is
+// request t's token at position L_t - 1, so it lands in the request's local
+// block, which this launch never scores. A token whose slot is not that
+// position is flagged (MSA_FLAG_BAD_SLOT) and skipped; a negative slot is a
+// padding token and is skipped silently. The consumer warps take the
+// (token, head) rows before their first page arrives; the attention that
+// reads the new K/V waits for this whole launch.
+__device__ __noinline__ void fused_insert(const IdxParams& p, int64_t cw, int64_t ncw, int lane) {
+  const InsertParams& ins = p.ins;
+  const int64_t total = static_cast<int64_t>(ins.T) * ins.G;
+  for (int64_t w = cw; w < total; w += ncw) {
+    const int t = static_cast<int>(w / ins.G), h = static_cast<int>(w % ins.G);
+    const int64_t slot = ins.slots[t];
+    if (slot < 0) continue;
+    const int L = p.seq_lens[t];
+    bool ok = L >= 1 && L <= p.NB * kBlock;
+    if (ok) {
+      const int page = p.block_table[static_cast<int64_t>(t) * p.NB + (L - 1) / kBlock];
+      ok = page >= 0 && page < p.P && slot == static_cast<int64_t>(page) * kBlock + (L - 1) % kBlock;
+    }
+    if (!ok) {
+      if (lane == 0) set_flag(p.flags, MSA_FLAG_BAD_SLOT);
+      continue;
+    }
+    insert_row(ins, t, h, lane);
+  }
+}
 
 // Blocks of request b that some query position can select: every n < l_last,
 // l_last being the local block of the last position. -1 for an invalid length.
@@ -145,6 +175,10 @@ __global__ void __launch_bounds__(kIdxThreads, kFp4Keys ? kFp4CtasPerSm : 1) ind
   for (int x = threadIdx.x; x < kStages * kMaxIdxHeads; x += blockDim.x) ticket[x] = 0u;
   __syncthreads();
   fill_tails(p, pref);
+  if (p.ins_on && warp > 0) {
+    const int64_t nc = blockDim.x / 32 - 1;
+    fused_insert(p, static_cast<int64_t>(blockIdx.x) * nc + (warp - 1), nc * gridDim.x, lane);
+  }
 
   const int64_t U = pref[p.B];
   const int64_t u0 = U * blockIdx.x / gridDim.x, u1 = U * (blockIdx.x + 1) / gridDim.x;
@@ -498,9 +532,15 @@ __global__ void __launch_bounds__(kBlock) index_score_f32_kernel(IdxParams p) {
   }
 }
 
-cudaError_t launch_index_score(const IndexArgs& a, cudaStream_t stream, DispatchRecord* rec) {
+cudaError_t launch_index_score(const IndexArgs& a, const InsertArgs* ins, cudaStream_t stream, DispatchRecord* rec) {
   IdxParams p{a.q, a.keys, a.scale, a.block_table, a.seq_lens, a.scores, a.flags, a.global_scale,
               a.B, a.Q, a.I, a.NB, a.P};
+  p.ins_on = 0;
+  if (ins != nullptr) {
+    if (!(a.fp8 || a.fp4) || a.Q != 1) return cudaErrorInvalidValue;   // the caller checks both
+    p.ins_on = 1;
+    p.ins = make_insert_params(*ins);
+  }
   const int sms = device_sm_count();
   cudaError_t err;
   if (a.fp8 || a.fp4) {
@@ -518,7 +558,7 @@ cudaError_t launch_index_score(const IndexArgs& a, cudaStream_t stream, Dispatch
     const int block = 32 * (1 + kWarpsPerHead * a.I);
     err = launch_pdl(kern, dim3(grid), dim3(block), smem, stream, p);
     if (err != cudaSuccess) return err;
-    rec->set("index_score %s grid=%d block=%d smem=%zu stages=%d q_len=%d idx_heads=%d",
+    rec->set("%sindex_score %s grid=%d block=%d smem=%zu stages=%d q_len=%d idx_heads=%d", p.ins_on ? "insert+" : "",
              !a.fp4 ? "fp8_mma_f16" : a.Q == 1 ? "nvfp4_group_cols_mma_f16" : "nvfp4_mma_f16", grid, block, smem,
              stages, a.Q, a.I);
   } else {

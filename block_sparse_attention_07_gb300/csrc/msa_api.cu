@@ -203,16 +203,16 @@ msa_status_t msa_qk_norm_rope_insert(const msa_dims_t* dims, const void* q, cons
   return cuda_status(launch_qk_norm_rope_insert(a, static_cast<cudaStream_t>(stream), &g_record));
 }
 
-msa_status_t msa_index_score(const msa_dims_t* dims, const void* idx_q, msa_dtype_t q_dtype,
-                             const msa_index_cache_t* idx_cache, const int32_t* block_table,
-                             const int32_t* seq_lens, float* scores, uint32_t* dev_flags, void* stream) {
+// Validation and arguments of the index-score step (shared by the fused insert).
+static msa_status_t index_args(const msa_dims_t* dims, const void* idx_q, msa_dtype_t q_dtype,
+                               const msa_index_cache_t* idx_cache, const int32_t* block_table,
+                               const int32_t* seq_lens, float* scores, uint32_t* dev_flags, IndexArgs& a) {
   msa_status_t st = check_dims(dims);
   if (st != MSA_OK) return st;
   if (idx_q == nullptr || idx_cache == nullptr || idx_cache->keys == nullptr || block_table == nullptr ||
       seq_lens == nullptr || scores == nullptr || dev_flags == nullptr)
     return MSA_ERR_INVALID_ARG;
   if (!aligned16(idx_q) || !aligned16(idx_cache->keys)) return MSA_ERR_INVALID_ARG;
-  IndexArgs a;
   a.fp8 = 0;
   a.fp4 = 0;
   a.scale = nullptr;
@@ -245,7 +245,39 @@ msa_status_t msa_index_score(const msa_dims_t* dims, const void* idx_q, msa_dtyp
   a.I = dims->n_idx_heads;
   a.NB = dims->max_blocks_per_seq;
   a.P = dims->num_pages;
-  return cuda_status(launch_index_score(a, static_cast<cudaStream_t>(stream), &g_record));
+  return MSA_OK;
+}
+
+msa_status_t msa_index_score(const msa_dims_t* dims, const void* idx_q, msa_dtype_t q_dtype,
+                             const msa_index_cache_t* idx_cache, const int32_t* block_table,
+                             const int32_t* seq_lens, float* scores, uint32_t* dev_flags, void* stream) {
+  IndexArgs a;
+  const msa_status_t st = index_args(dims, idx_q, q_dtype, idx_cache, block_table, seq_lens, scores, dev_flags, a);
+  if (st != MSA_OK) return st;
+  return cuda_status(launch_index_score(a, nullptr, static_cast<cudaStream_t>(stream), &g_record));
+}
+
+msa_status_t msa_insert_index_score(const msa_dims_t* dims, const void* k_new, const void* v_new,
+                                    const void* idx_k_new, const int64_t* slot_mapping,
+                                    const msa_kv_cache_t* cache, const void* idx_q,
+                                    const msa_index_cache_t* idx_cache, const int32_t* block_table,
+                                    const int32_t* seq_lens, float* scores, uint32_t* dev_flags, void* stream) {
+  IndexArgs a;
+  msa_status_t st = index_args(dims, idx_q, MSA_BF16, idx_cache, block_table, seq_lens, scores, dev_flags, a);
+  if (st != MSA_OK) return st;
+  if (dims->q_len != 1 || !(a.fp8 || a.fp4)) return MSA_ERR_UNSUPPORTED;
+  if (cache == nullptr || k_new == nullptr || v_new == nullptr || idx_k_new == nullptr || slot_mapping == nullptr)
+    return MSA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(idx_k_new)) return MSA_ERR_INVALID_ARG;
+  InsertArgs ins;
+  st = insert_targets(dims, true, MSA_BF16, cache, idx_cache, dev_flags, ins);
+  if (st != MSA_OK) return st;
+  ins.k_new = k_new;
+  ins.v_new = v_new;
+  ins.idx_new = idx_k_new;
+  ins.slots = slot_mapping;
+  ins.T = dims->batch;
+  return cuda_status(launch_index_score(a, &ins, static_cast<cudaStream_t>(stream), &g_record));
 }
 
 msa_status_t msa_select_blocks(const msa_dims_t* dims, const float* scores, const int32_t* seq_lens,

@@ -136,7 +136,9 @@ struct PrologueArgs {
   int H, I;
 };
 cudaError_t launch_qk_norm_rope_insert(const PrologueArgs& a, cudaStream_t stream, DispatchRecord* rec);
-cudaError_t launch_index_score(const IndexArgs& a, cudaStream_t stream, DispatchRecord* rec);
+// ins: the step's insert run inside the same launch (FP8 / NVFP4 index keys,
+// one query position, token t = request t's token at position L_t - 1), or null.
+cudaError_t launch_index_score(const IndexArgs& a, const InsertArgs* ins, cudaStream_t stream, DispatchRecord* rec);
 cudaError_t launch_select_blocks(const SelectArgs& a, cudaStream_t stream, DispatchRecord* rec);
 cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRecord* rec);
 

@@ -24,7 +24,7 @@ FLAG_BAD_PAGE, FLAG_BAD_BLOCK, FLAG_BAD_SEQLEN, FLAG_BAD_SLOT, FLAG_TIMEOUT, FLA
 
 # Every function include/msa.h declares.
 EXPORTED = ("msa_abi_version", "msa_status_string", "msa_get_last_dispatch", "msa_kv_insert_quant",
-            "msa_index_score", "msa_select_blocks", "msa_sparse_gqa_workspace_size", "msa_sparse_gqa_decode",
+            "msa_index_score", "msa_insert_index_score", "msa_select_blocks", "msa_sparse_gqa_workspace_size", "msa_sparse_gqa_decode",
             "msa_sparse_gqa_decode_noalloc", "msa_read_device_flags", "msa_qk_norm_rope_insert",
             "msa_select_sparse_gqa_decode")
 
@@ -73,6 +73,8 @@ def _load():
                                         ctypes.POINTER(_KVCache), ctypes.POINTER(_IndexCache), vp, vp]
     lib.msa_index_score.argtypes = [ctypes.POINTER(Dims), vp, ctypes.c_int, ctypes.POINTER(_IndexCache), vp, vp,
                                     vp, vp, vp]
+    lib.msa_insert_index_score.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, vp, ctypes.POINTER(_KVCache), vp,
+                                           ctypes.POINTER(_IndexCache), vp, vp, vp, vp, vp]
     lib.msa_select_blocks.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, vp, vp]
     lib.msa_sparse_gqa_workspace_size.restype = sz
     lib.msa_sparse_gqa_workspace_size.argtypes = [ctypes.POINTER(Dims), ctypes.c_int]
@@ -225,6 +227,15 @@ def index_score(dims: Dims, idx_q, q_dtype: int, idx_cache: IndexCache, block_ta
     args = (ctypes.byref(dims), _ptr(idx_q), q_dtype, ctypes.byref(ic), _ptr(block_table), _ptr(seq_lens),
             _ptr(scores), _ptr(flags), _stream(stream))
     return _call(lib.msa_index_score, args, (dims, ic), "msa_index_score", prepare)
+
+
+def insert_index_score(dims: Dims, k_new, v_new, idx_k_new, slot_mapping, cache: KVCache, idx_q,
+                       idx_cache: IndexCache, block_table, seq_lens, scores, flags, stream=None, prepare=False):
+    kc, ic = cache.c(), idx_cache.c()
+    args = (ctypes.byref(dims), _ptr(k_new), _ptr(v_new), _ptr(idx_k_new), _ptr(slot_mapping), ctypes.byref(kc),
+            _ptr(idx_q), ctypes.byref(ic), _ptr(block_table), _ptr(seq_lens), _ptr(scores), _ptr(flags),
+            _stream(stream))
+    return _call(lib.msa_insert_index_score, args, (dims, kc, ic), "msa_insert_index_score", prepare)
 
 
 def select_blocks(dims: Dims, scores, seq_lens, selected, flags, stream=None, prepare=False):

@@ -158,6 +158,10 @@ class DeviceWorkload:
                                           self.block_table_d, self.seq_lens_d, self.scores, self.flags, prepare=True),
                     select=msa.select_blocks(self.dims, self.scores, self.seq_lens_d, self.selected, self.flags,
                                              prepare=True))
+            if self.merges_insert:
+                self._prep.update(insert_index=msa.insert_index_score(
+                    self.dims, self.new_k, self.new_v, self.new_idx, self.new_slots, self.cache, self.q_idx,
+                    self.idx_cache, self.block_table_d, self.seq_lens_d, self.scores, self.flags, prepare=True))
         return self._prep
 
     def insert_step_tokens(self, stream=None):
@@ -171,6 +175,14 @@ class DeviceWorkload:
             return self.prepared()["index"]()
         msa.index_score(self.dims, self.q_idx, self.q_idx_dtype, self.idx_cache, self.block_table_d,
                         self.seq_lens_d, self.scores, self.flags, stream)
+
+    def insert_index_score(self, stream=None):
+        """The insert and the scoring in one launch (one query position, FP8 or NVFP4 index keys)."""
+        if stream is None:
+            return self.prepared()["insert_index"]()
+        msa.insert_index_score(self.dims, self.new_k, self.new_v, self.new_idx, self.new_slots, self.cache,
+                               self.q_idx, self.idx_cache, self.block_table_d, self.seq_lens_d, self.scores,
+                               self.flags, stream)
 
     def select(self, stream=None):
         if stream is None:
@@ -198,13 +210,32 @@ class DeviceWorkload:
         rows are split over CTAs and the separate selection launch is faster."""
         return self.w.kv_dtype != "nvfp4"
 
+    @property
+    def merges_insert(self) -> bool:
+        """Whether ``step`` inserts the new tokens inside the index launch: with one
+        query position each request's new token is in its local block, which
+        the scoring never reads (FP8 or NVFP4 index keys)."""
+        return self.has_index and self.w.q_len == 1 and self.w.idx_dtype in ("fp8", "nvfp4")
+
     def step(self, stream=None):
-        """One decode step: insert this step's tokens, score, select, attend
-        (selection and attention in one launch where that is faster)."""
-        if self.fuses_selection:
-            self.step_fused(stream)
+        """One decode step: insert this step's tokens, score, select, attend. The
+        insert runs inside the index launch and the selection inside the
+        attention launch wherever that is faster."""
+        if self.merges_insert:
+            self.insert_index_score(stream)
         else:
-            self.step_separate(stream)
+            self.insert_step_tokens(stream)
+            self.index_score(stream)
+        if self.fuses_selection:
+            self.select_attend(stream)
+        else:
+            self.select(stream)
+            self.attend(stream)
+
+    def step_merged(self, stream=None):
+        """Insert and scoring in one launch, then selection and attention in one launch."""
+        self.insert_index_score(stream)
+        self.select_attend(stream)
 
     def step_separate(self, stream=None):
         """The step with the selection as its own launch."""

@@ -234,6 +234,29 @@ msa_status_t msa_index_score(const msa_dims_t* dims, const void* idx_q, msa_dtyp
                              void* stream);
 
 /*
+ * The insert of msa_kv_insert_quant and the scoring of msa_index_score in one
+ * launch, for a decode step with one query position ("MSA 実行プロセス" steps
+ * 0-1; "EAGLE3 を用いた投機的デコード" for the single-position case). The
+ * step's new token of request b sits at position seq_lens[b] - 1, in the
+ * request's local block, which the scoring never reads. So the scoring warps
+ * insert the B tokens before their first index page arrives, and the
+ * attention call that follows sees the new K/V because it waits for the whole
+ * launch.
+ * k_new, v_new: bf16 [B, G, D]; idx_k_new: bf16 [B, I, D]; slot_mapping:
+ * int64 [B], the new token of request b, which must equal
+ *   block_table[b, (seq_lens[b] - 1) / 128] * 128 + (seq_lens[b] - 1) % 128
+ * (negative: a padding request, skipped). A token whose slot is anything else
+ * is skipped and raises MSA_FLAG_BAD_SLOT. idx_q is bf16; the index cache must
+ * be FP8 E4M3 or NVFP4 and q_len 1, else MSA_ERR_UNSUPPORTED. Results are the
+ * two separate calls' results, byte for byte.
+ */
+msa_status_t msa_insert_index_score(const msa_dims_t* dims, const void* k_new, const void* v_new,
+                                    const void* idx_k_new, const int64_t* slot_mapping,
+                                    const msa_kv_cache_t* cache, const void* idx_q,
+                                    const msa_index_cache_t* idx_cache, const int32_t* block_table,
+                                    const int32_t* seq_lens, float* scores, uint32_t* dev_flags, void* stream);
+
+/*
  * Stage 2, block selection ("MSA 実行プロセス" step 2, local_blocks=1). For
  * every (b, j, g): order the candidates n < l_j by score (higher first, then
  * lower block id), keep the first min(K-1, l_j), add l_j, and write them in
