@@ -238,7 +238,9 @@ msa_status_t msa_index_score(const msa_dims_t* dims, const void* idx_q, msa_dtyp
  * launch, for a decode step with one query position ("MSA 実行プロセス" steps
  * 0-1; "EAGLE3 を用いた投機的デコード" for the single-position case). The
  * step's new token of request b sits at position seq_lens[b] - 1, in the
- * request's local block, which the scoring never reads. So the scoring warps
+ * request's local block, which the scoring never reads. That page must not be
+ * a fully visible block in any other request's table; a paged allocator that
+ * shares only full prefix blocks guarantees this. So the scoring warps
  * insert the B tokens before their first index page arrives, and the
  * attention call that follows sees the new K/V because it waits for the whole
  * launch.
