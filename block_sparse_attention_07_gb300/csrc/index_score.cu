@@ -469,6 +469,7 @@ __global__ void __launch_bounds__(kBlock) index_score_f32_kernel(IdxParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_launch_dependents();
   griddep_wait();
+  if (p.ins_on) fused_insert(p, static_cast<int64_t>(blockIdx.x) * 4 + warp, static_cast<int64_t>(gridDim.x) * 4, lane);
   if (warp == 0) build_prefix(p, pref, blockIdx.x == 0);
   __syncthreads();
   fill_tails(p, pref);
@@ -537,7 +538,7 @@ cudaError_t launch_index_score(const IndexArgs& a, const InsertArgs* ins, cudaSt
               a.B, a.Q, a.I, a.NB, a.P};
   p.ins_on = 0;
   if (ins != nullptr) {
-    if (!(a.fp8 || a.fp4) || a.Q != 1) return cudaErrorInvalidValue;   // the caller checks both
+    if (a.Q != 1) return cudaErrorInvalidValue;   // the caller checks it
     p.ins_on = 1;
     p.ins = make_insert_params(*ins);
   }
@@ -569,7 +570,8 @@ cudaError_t launch_index_score(const IndexArgs& a, const InsertArgs* ins, cudaSt
     const int grid = sms * 8;                   // grid-stride over (request, block, head) tasks
     err = launch_pdl(index_score_f32_kernel, dim3(grid), dim3(kBlock), smem, stream, p);
     if (err != cudaSuccess) return err;
-    rec->set("index_score f32_fma grid=%d block=%d smem=%zu q_len=%d idx_heads=%d", grid, kBlock, smem, a.Q, a.I);
+    rec->set("%sindex_score f32_fma grid=%d block=%d smem=%zu q_len=%d idx_heads=%d", p.ins_on ? "insert+" : "", grid,
+             kBlock, smem, a.Q, a.I);
   }
   return cudaGetLastError();
 }

@@ -262,15 +262,17 @@ msa_status_t msa_insert_index_score(const msa_dims_t* dims, const void* k_new, c
                                     const msa_kv_cache_t* cache, const void* idx_q,
                                     const msa_index_cache_t* idx_cache, const int32_t* block_table,
                                     const int32_t* seq_lens, float* scores, uint32_t* dev_flags, void* stream) {
+  // the index query and the new index keys are fp32 with an fp32 index cache, bf16 otherwise
+  const msa_dtype_t idx_dt = idx_cache != nullptr && idx_cache->dtype == MSA_F32 ? MSA_F32 : MSA_BF16;
   IndexArgs a;
-  msa_status_t st = index_args(dims, idx_q, MSA_BF16, idx_cache, block_table, seq_lens, scores, dev_flags, a);
+  msa_status_t st = index_args(dims, idx_q, idx_dt, idx_cache, block_table, seq_lens, scores, dev_flags, a);
   if (st != MSA_OK) return st;
-  if (dims->q_len != 1 || !(a.fp8 || a.fp4)) return MSA_ERR_UNSUPPORTED;
+  if (dims->q_len != 1) return MSA_ERR_UNSUPPORTED;
   if (cache == nullptr || k_new == nullptr || v_new == nullptr || idx_k_new == nullptr || slot_mapping == nullptr)
     return MSA_ERR_INVALID_ARG;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(idx_k_new)) return MSA_ERR_INVALID_ARG;
   InsertArgs ins;
-  st = insert_targets(dims, true, MSA_BF16, cache, idx_cache, dev_flags, ins);
+  st = insert_targets(dims, true, idx_dt, cache, idx_cache, dev_flags, ins);
   if (st != MSA_OK) return st;
   ins.k_new = k_new;
   ins.v_new = v_new;

@@ -177,7 +177,7 @@ class DeviceWorkload:
                         self.seq_lens_d, self.scores, self.flags, stream)
 
     def insert_index_score(self, stream=None):
-        """The insert and the scoring in one launch (one query position, FP8 or NVFP4 index keys)."""
+        """The insert and the scoring in one launch (one query position)."""
         if stream is None:
             return self.prepared()["insert_index"]()
         msa.insert_index_score(self.dims, self.new_k, self.new_v, self.new_idx, self.new_slots, self.cache,
@@ -214,8 +214,8 @@ class DeviceWorkload:
     def merges_insert(self) -> bool:
         """Whether ``step`` inserts the new tokens inside the index launch: with one
         query position each request's new token is in its local block, which
-        the scoring never reads (FP8 or NVFP4 index keys)."""
-        return self.has_index and self.w.q_len == 1 and self.w.idx_dtype in ("fp8", "nvfp4")
+        the scoring never reads."""
+        return self.has_index and self.w.q_len == 1
 
     def step(self, stream=None):
         """One decode step: insert this step's tokens, score, select, attend. The

@@ -244,13 +244,14 @@ msa_status_t msa_index_score(const msa_dims_t* dims, const void* idx_q, msa_dtyp
  * insert the B tokens before their first index page arrives, and the
  * attention call that follows sees the new K/V because it waits for the whole
  * launch.
- * k_new, v_new: bf16 [B, G, D]; idx_k_new: bf16 [B, I, D]; slot_mapping:
+ * k_new, v_new: bf16 [B, G, D]; idx_k_new: [B, I, D]; slot_mapping:
  * int64 [B], the new token of request b, which must equal
  *   block_table[b, (seq_lens[b] - 1) / 128] * 128 + (seq_lens[b] - 1) % 128
  * (negative: a padding request, skipped). A token whose slot is anything else
- * is skipped and raises MSA_FLAG_BAD_SLOT. idx_q is bf16; the index cache must
- * be FP8 E4M3 or NVFP4 and q_len 1, else MSA_ERR_UNSUPPORTED. Results are the
- * two separate calls' results, byte for byte.
+ * is skipped and raises MSA_FLAG_BAD_SLOT. idx_q and idx_k_new are fp32 with
+ * an MSA_F32 index cache and bf16 with an FP8 E4M3 or NVFP4 one. q_len must be
+ * 1, else MSA_ERR_UNSUPPORTED. Results are the two separate calls' results,
+ * byte for byte.
  */
 msa_status_t msa_insert_index_score(const msa_dims_t* dims, const void* k_new, const void* v_new,
                                     const void* idx_k_new, const int64_t* slot_mapping,

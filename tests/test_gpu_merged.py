@@ -15,7 +15,7 @@ from test_gpu_pipeline import REDUCED
 pytestmark = pytest.mark.gpu
 
 W = synth.WORKLOADS
-MERGED = ["b32_32k", "fp8kv_32k", "b32_32k_fp4idx", "nvfp4_256k"]
+MERGED = ["b32_32k", "fp8kv_32k", "b32_32k_fp4idx", "nvfp4_256k", "tiny"]
 
 
 def _cache_tensors(dw):
@@ -81,7 +81,3 @@ def test_unsupported_shapes_are_rejected():
     with pytest.raises(msa.MSAError):
         msa.insert_index_score(dw.dims, dw.new_k, dw.new_v, dw.new_idx, dw.new_slots, dw.cache, dw.q_idx,
                                dw.idx_cache, dw.block_table_d, dw.seq_lens_d, dw.scores, dw.flags)
-    t = parity.build(W["tiny"])                   # fp32 index keys
-    with pytest.raises(msa.MSAError):
-        msa.insert_index_score(t.dims, t.new_k, t.new_v, t.new_idx, t.new_slots, t.cache, t.q_idx,
-                               t.idx_cache, t.block_table_d, t.seq_lens_d, t.scores, t.flags)
