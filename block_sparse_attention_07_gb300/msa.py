@@ -24,9 +24,9 @@ FLAG_BAD_PAGE, FLAG_BAD_BLOCK, FLAG_BAD_SEQLEN, FLAG_BAD_SLOT, FLAG_TIMEOUT, FLA
 
 # Every function include/msa.h declares.
 EXPORTED = ("msa_abi_version", "msa_status_string", "msa_get_last_dispatch", "msa_kv_insert_quant",
-            "msa_index_score", "msa_insert_index_score", "msa_select_blocks", "msa_sparse_gqa_workspace_size", "msa_sparse_gqa_decode",
-            "msa_sparse_gqa_decode_noalloc", "msa_read_device_flags", "msa_qk_norm_rope_insert",
-            "msa_select_sparse_gqa_decode")
+            "msa_index_score", "msa_insert_index_score", "msa_select_blocks", "msa_sparse_gqa_workspace_size",
+            "msa_sparse_gqa_decode", "msa_sparse_gqa_decode_noalloc", "msa_read_device_flags",
+            "msa_qk_norm_rope_insert", "msa_select_sparse_gqa_decode")
 
 
 class Dims(ctypes.Structure):
@@ -231,6 +231,8 @@ def index_score(dims: Dims, idx_q, q_dtype: int, idx_cache: IndexCache, block_ta
 
 def insert_index_score(dims: Dims, k_new, v_new, idx_k_new, slot_mapping, cache: KVCache, idx_q,
                        idx_cache: IndexCache, block_table, seq_lens, scores, flags, stream=None, prepare=False):
+    """msa_insert_index_score: the step's new tokens (one per request, at its last position)
+    inserted and every block scored, in one launch; one query position only."""
     kc, ic = cache.c(), idx_cache.c()
     args = (ctypes.byref(dims), _ptr(k_new), _ptr(v_new), _ptr(idx_k_new), _ptr(slot_mapping), ctypes.byref(kc),
             _ptr(idx_q), ctypes.byref(ic), _ptr(block_table), _ptr(seq_lens), _ptr(scores), _ptr(flags),
