@@ -2,9 +2,12 @@
 
 One step = one decode pass over a batch: insert the step's new K/V/index-key
 tokens (with quantisation), score every candidate block, select the top
-blocks, run split-K sparse GQA and its combine. The default workload is
-batch 32 x 32,768-token contexts, 1 query token, 64/4/4 heads, FP8 index keys,
-bf16 KV, top-16 blocks.
+blocks, run split-K sparse GQA and its combine. The headline workload is the
+largest configuration: batch 64 with contexts drawn from 8K to 128K tokens,
+1 query token, 64/4/4 heads, FP8 index keys, bf16 KV, top-16 blocks. The line
+then carries, under ``configs``, the same measurements for batch 32 x 32K,
+batch 32 x 64K with 8 speculative positions, and batch 16 x 256K with NVFP4
+K/V (``--configs``).
 
 Prints one JSON line (rank 0). ``value`` is query-tokens/s over all ranks with
 the inputs already resident in HBM; ``e2e`` is the same metric through the
@@ -42,13 +45,18 @@ sys.path.insert(0, ROOT)
 METRIC = "MSA decode query-tokens/s at 1 GB300; achieved HBM GB/s vs peak per kernel"
 FALLBACK_HBM_GBS = 6800.0
 
-# ncu dram__bytes_read.sum + dram__bytes_write.sum per launch on the default
-# workload, keyed by the hash of the kernel's sources when it was measured (a
-# changed kernel reports null until it is measured again). Summaries: profiles/.
+# ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, keyed by kernel,
+# workload and the hash of the kernel's sources when it was measured (a changed
+# kernel reports null until it is measured again). Summaries: profiles/.
 NCU_TRAFFIC = {
-    ("index_score", "b355f71dbdd4de60"): 551650816 + 258048,
-    ("sparse_gqa", "a1d657ef6852a159"): 134992128 + 123648,
+    ("index_score", "b32_32k", "b355f71dbdd4de60"): 551650816 + 258048,
+    ("sparse_gqa", "b32_32k", "a1d657ef6852a159"): 134992128 + 123648,
 }
+
+# The headline workload (the largest configuration on one GPU: batch 64, ragged
+# 8K-128K contexts) and the further configurations measured after it.
+DEFAULT_WORKLOAD = "ragged"
+DEFAULT_CONFIGS = "b32_32k,spec8,nvfp4_256k"
 
 
 def _src_hash(*names):
@@ -181,6 +189,131 @@ def attention_bytes(dw, sel):
 
 
 # ------------------------------------------------------------------ our arm --
+class StepTimer:
+    """Timed passes of one workload's decode step on one device (CUDA events on
+    the launching stream)."""
+
+    NAMES = ("insert", "index_score", "select", "sparse_gqa")
+
+    def __init__(self, dw, stream, flush):
+        self.dw, self.stream, self.flush = dw, stream, flush
+
+    def steps(self, n, events):
+        """n steps. events "step": records only at step boundaries, so the
+        kernels launch back to back and overlap through programmatic dependent
+        launch (the insert inside the index launch and the selection inside the
+        attention launch where the workload's step does that,
+        ``dw.merges_insert`` / ``dw.fuses_selection``); "index": the insert as
+        its own launch, with events around the index-score kernel (its duration
+        for the roofline; the events cut the overlap on both sides of it);
+        "other": step boundaries only, the other selection composition;
+        "unmerged": step boundaries only, the insert as its own launch; "all":
+        four separate launches with events between every kernel (no overlap;
+        the per-kernel breakdown)."""
+        import torch
+        dw, stream = self.dw, self.stream
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+        for s in range(n):
+            self.flush(s)
+            e = ev[s]
+            e[0].record(stream)
+            if dw.merges_insert and events in ("step", "other"):
+                dw.insert_index_score()
+            else:
+                dw.insert_step_tokens()
+                if events in ("index", "all"):
+                    e[1].record(stream)
+                dw.index_score()
+                if events in ("index", "all"):
+                    e[2].record(stream)
+            fused = dw.fuses_selection if events in ("step", "index", "unmerged") else (
+                not dw.fuses_selection if events == "other" else False)
+            if fused:
+                dw.select_attend()
+            else:
+                dw.select()
+                if events == "all":
+                    e[3].record(stream)
+                dw.attend()
+            e[4].record(stream)
+        torch.cuda.synchronize(dw.device)
+        step = [ev[s][0].elapsed_time(ev[s][4]) for s in range(n)]
+        idx = [ev[s][1].elapsed_time(ev[s][2]) for s in range(n)] if events in ("index", "all") else None
+        per = None
+        if events == "all":
+            per = {nm: [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(n)] for i, nm in enumerate(self.NAMES)}
+        return step, idx, per
+
+    def launches_per_step(self):
+        """[insert,] index, [select,] attention (the split-K combine is fused)."""
+        return (1 if self.dw.merges_insert else 2) + (1 if self.dw.fuses_selection else 2)
+
+
+def kernel_rooflines(args, dw, idx_ms, att_ms, peak, peak_kind, idx_step_ms):
+    """The index kernel's and the attention kernel's achieved HBM GB/s: algorithmic
+    bytes per launch over the mean launch duration timed live on this machine."""
+    ib = index_bytes(dw)
+    ab = attention_bytes(dw, dw.selected.cpu().numpy())
+    name = dw.w.name if not args.batch else None
+    traffic = NCU_TRAFFIC.get(("index_score", name, _src_hash("index_score.cu", "insert_rows.cuh", "msa_device.cuh")))
+    att_traffic = NCU_TRAFFIC.get(("sparse_gqa", name, _src_hash("sparse_gqa.cu", "select_row.cuh", "msa_device.cuh")))
+    idx = {"bound": "hbm", "kernel": "index_score", "achieved": ib / (idx_ms / 1e3) / 1e9, "peak": peak,
+           "unit": "GB/s", "frac": ib / (idx_ms / 1e3) / 1e9 / peak, "peak_source": peak_kind, "traffic": traffic,
+           "algorithmic_bytes_per_launch": ib, "avg_launch_ms": idx_ms,
+           "timed_in": f"{args.steps} further steps (insert as its own launch) with events around the kernel "
+                       f"({idx_step_ms:.4f} ms per step there)"}
+    att = {"bound": "hbm", "kernel": "sparse_gqa", "achieved": ab / (att_ms / 1e3) / 1e9, "peak": peak,
+           "unit": "GB/s", "frac": ab / (att_ms / 1e3) / 1e9 / peak, "peak_source": peak_kind,
+           "algorithmic_bytes_per_launch": ab, "avg_launch_ms": att_ms, "traffic": att_traffic,
+           "timed_in": "per-kernel breakdown pass (events between every kernel, selection as its own launch)"}
+    return idx, att
+
+
+def measure_config(args, name, dev, stream, flush, world, peak, peak_kind):
+    """One further workload, measured like the headline's step (outside its timed
+    region): value, ms per step, both kernels' roofline fractions, bytes."""
+    import torch
+    from block_sparse_attention_07_gb300 import synth
+    from block_sparse_attention_07_gb300.workload import DeviceWorkload
+    w = synth.WORKLOADS[name]
+    t0 = time.perf_counter()
+    dw = DeviceWorkload(w, dev)
+    build_s = time.perf_counter() - t0
+    tm = StepTimer(dw, stream, flush)
+    for s in range(args.warmup):
+        flush(s)
+        dw.step()
+    torch.cuda.synchronize(dev)
+    assert dw.check_flags() == 0, f"device flags raised during warm-up ({name})"
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    time.sleep(0.15)
+    barrier(world)
+    step_ms, _, _ = tm.steps(args.steps, "step")
+    barrier(world)
+    idx_step_ms, idx_launch_ms, _ = tm.steps(args.steps, "index")
+    clk = clocks.stop()
+    _, _, per = tm.steps(min(args.steps, 50), "all")
+    assert dw.check_flags() == 0, f"device flags raised ({name})"
+    B, Q = len(dw.which), w.q_len
+    tot_s, tot_units = aggregate(sum(step_ms) / 1e3, B * Q * args.steps, world, dev)
+    idx, att = kernel_rooflines(args, dw, statistics.mean(idx_launch_ms), statistics.mean(per["sparse_gqa"]),
+                                peak, peak_kind, statistics.mean(idx_step_ms))
+    out = {"workload": workload_desc(w), "value": tot_units / tot_s, "unit": "query-tokens/s",
+           "ms_per_step": statistics.mean(step_ms), "global_batch": B * world, "q_len": Q,
+           "index_frac": idx["frac"], "sparse_gqa_frac": att["frac"],
+           "index_bytes_per_launch": idx["algorithmic_bytes_per_launch"],
+           "sparse_gqa_bytes_per_launch": att["algorithmic_bytes_per_launch"],
+           "index_ms": idx["avg_launch_ms"], "sparse_gqa_ms": att["avg_launch_ms"],
+           "index_traffic": idx["traffic"], "sparse_gqa_traffic": att["traffic"],
+           "kernels_ms": {n: statistics.mean(v) for n, v in per.items()},
+           "gpu_launches_per_step": tm.launches_per_step(), "clocks": clk,
+           "setup_s": build_s}
+    del tm, dw
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, world, rank, local):
     import torch
     from block_sparse_attention_07_gb300 import synth
@@ -203,57 +336,12 @@ def run_ours(args, world, rank, local):
         elif args.flush == "read":
             torch.sum(flush_buf, dim=0, out=sink)
 
+    tm = StepTimer(dw, stream, flush)
     for s in range(args.warmup):
         flush(s)
         dw.step()
     torch.cuda.synchronize(dev)
     assert dw.check_flags() == 0, "device flags raised during warm-up"
-
-    names = ("insert", "index_score", "select", "sparse_gqa")
-
-    def timed_steps(n, events):
-        """n steps. events "step": records only at step boundaries, so the
-        kernels launch back to back and overlap through programmatic dependent
-        launch (the insert inside the index launch and the selection inside the
-        attention launch where the workload's step does that,
-        ``dw.merges_insert`` / ``dw.fuses_selection``); "index": the insert as
-        its own launch, with events around the index-score kernel (its duration
-        for the roofline; the events cut the overlap on both sides of it);
-        "other": step boundaries only, the other selection composition;
-        "unmerged": step boundaries only, the insert as its own launch; "all":
-        four separate launches with events between every kernel (no overlap;
-        the per-kernel breakdown)."""
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
-        for s in range(n):
-            flush(s)
-            e = ev[s]
-            e[0].record(stream)
-            if dw.merges_insert and events in ("step", "other"):
-                dw.insert_index_score()
-            else:
-                dw.insert_step_tokens()
-                if events in ("index", "all"):
-                    e[1].record(stream)
-                dw.index_score()
-                if events in ("index", "all"):
-                    e[2].record(stream)
-            fused = dw.fuses_selection if events in ("step", "index", "unmerged") else (
-                not dw.fuses_selection if events == "other" else False)
-            if fused:
-                dw.select_attend()
-            else:
-                dw.select()
-                if events == "all":
-                    e[3].record(stream)
-                dw.attend()
-            e[4].record(stream)
-        torch.cuda.synchronize(dev)
-        step = [ev[s][0].elapsed_time(ev[s][4]) for s in range(n)]
-        idx = [ev[s][1].elapsed_time(ev[s][2]) for s in range(n)] if events in ("index", "all") else None
-        per = None
-        if events == "all":
-            per = {nm: [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(n)] for i, nm in enumerate(names)}
-        return step, idx, per
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -261,20 +349,19 @@ def run_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
-    step_ms, _, _ = timed_steps(args.steps, "step")
+    step_ms, _, _ = tm.steps(args.steps, "step")
     barrier(world)
     wall = time.perf_counter() - wall0
     # the index-score kernel's launch duration (roofline), timed live over K more steps
-    idx_step_ms, idx_launch_ms, _ = timed_steps(args.steps, "index")
+    idx_step_ms, idx_launch_ms, _ = tm.steps(args.steps, "index")
     clk = clocks.stop()
-    # [insert,] index, [select,] attention (split-K combine fused)
-    launches = args.steps * ((1 if dw.merges_insert else 2) + (1 if dw.fuses_selection else 2))
+    launches = args.steps * tm.launches_per_step()
     # the same steps in the other composition (selection fused or separate)
-    other_step_ms, _, _ = timed_steps(args.steps, "other")
+    other_step_ms, _, _ = tm.steps(args.steps, "other")
     # the same steps with the insert as its own launch
-    unmerged_step_ms = timed_steps(args.steps, "unmerged")[0] if dw.merges_insert else None
+    unmerged_step_ms = tm.steps(args.steps, "unmerged")[0] if dw.merges_insert else None
     # per-kernel breakdown, outside the timed region, with an event between every kernel
-    _, _, per = timed_steps(min(args.steps, 50), "all")
+    _, _, per = tm.steps(min(args.steps, 50), "all")
     local_s = sum(step_ms) / 1e3
     tot_s, tot_units = aggregate(local_s, B * Q * args.steps, world, dev)
     value = tot_units / tot_s
@@ -321,6 +408,7 @@ def run_ours(args, world, rank, local):
 
     e2e_tot = e2e_timed(e2e_replay)
     e2e_eager_tot = e2e_timed(e2e_eager)
+    del e2e_graph
     assert dw.check_flags() == 0, "device flags raised"
 
     def event_timed(fn, n):
@@ -338,6 +426,7 @@ def run_ours(args, world, rank, local):
     for _ in range(args.warmup):
         graph.replay()
     graph_ms = event_timed(graph.replay, args.steps)
+    del graph
     assert dw.check_flags() == 0, "device flags raised (graph replay)"
     # The fused QK-norm + RoPE + K/V/index insert of the step's tokens, alone and
     # as the first kernel of a step (in place of the plain insert).
@@ -350,6 +439,7 @@ def run_ours(args, world, rank, local):
         for _ in range(args.warmup):
             burst.replay()
         prologue_ms = [t / 20 for t in event_timed(burst.replay, args.steps)]
+        del burst
 
         def pro_step():
             dw.qk_norm_rope_insert()
@@ -372,34 +462,21 @@ def run_ours(args, world, rank, local):
         assert layer.check_flags() == 0, "device flags raised (reusing layer)"
         del layer
 
-    if rank != 0:
-        return None
     peak, peak_kind = measured_peaks()
     ib = index_bytes(dw)
     per_step_mb = (ib + attention_bytes(dw, dw.selected.cpu().numpy())) / 1e6
     l2_note = {"none": f"not flushed: each step reads {per_step_mb:.0f} MB of inputs, more than the 129 MB L2",
                "read": "flushed by reading a 512 MB buffer before every step",
                "write": "flushed by writing a 512 MB buffer before every step"}[args.flush]
-    idx_ms = statistics.mean(idx_launch_ms)
-    achieved = ib / (idx_ms / 1e3) / 1e9
-    sel = dw.selected.cpu().numpy()
-    ab = attention_bytes(dw, sel)
-    att_ms = statistics.mean(per["sparse_gqa"])
-    traffic = NCU_TRAFFIC.get(("index_score", _src_hash("index_score.cu", "insert_rows.cuh", "msa_device.cuh")))
-    att_traffic = NCU_TRAFFIC.get(("sparse_gqa", _src_hash("sparse_gqa.cu", "select_row.cuh", "msa_device.cuh")))
-    if args.workload != "b32_32k" or args.batch:
-        traffic = att_traffic = None          # the counters were taken on the default workload
+    roof, att_roof = kernel_rooflines(args, dw, statistics.mean(idx_launch_ms), statistics.mean(per["sparse_gqa"]),
+                                      peak, peak_kind, statistics.mean(idx_step_ms))
     line = {
         "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": statistics.mean(step_ms), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8/bf16 (fp32 accumulate)", "data": "synthetic",
         "config": {"workload": workload_desc(w), "global_batch": B * world, "q_len": Q, "l2": l2_note,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": "index_score", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": ib, "avg_launch_ms": idx_ms,
-                     "timed_in": f"{args.steps} further steps (insert as its own launch) with events around the kernel "
-                                 f"({statistics.mean(idx_step_ms):.4f} ms per step there)"},
+        "roofline": roof,
         "kernels_ms": {n: statistics.mean(v) for n, v in per.items()},
         "selection_in_attention_launch": dw.fuses_selection,
         "insert_in_index_launch": dw.merges_insert,
@@ -411,9 +488,7 @@ def run_ours(args, world, rank, local):
                               "ms_per_step": statistics.mean(other_step_ms),
                               "what": ("selection as its own launch" if dw.fuses_selection
                                        else "selection inside the attention launch")},
-        "sparse_gqa_roofline": {"achieved": ab / (att_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
-                                "frac": ab / (att_ms / 1e3) / 1e9 / peak, "algorithmic_bytes_per_launch": ab,
-                                "traffic": att_traffic},
+        "sparse_gqa_roofline": att_roof,
         "e2e": {"value": B * Q * args.steps * world / e2e_tot, "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "what": "host wall clock per step: the step's inputs copied from pinned host memory, the library "
@@ -441,8 +516,17 @@ def run_ours(args, world, rank, local):
             "ms_per_step": statistics.mean(reuse_ms),
             "what": "a second layer (own q/K/V) reusing this step's block selection: K/V insert + sparse GQA, "
                     "no index keys, scoring or selection"}
+    cfg_w = w
+    del tm, dw
+    torch.cuda.empty_cache()
+    # The other workloads, each measured like the headline (after its timed region).
+    names = [n for n in (args.configs.split(",") if args.configs not in ("", "none") else []) if n != args.workload]
+    if names and not args.batch:
+        line["configs"] = {n: measure_config(args, n, dev, stream, flush, world, peak, peak_kind) for n in names}
+    if rank != 0:
+        return None
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_requests)
+        line["cpu_baseline"] = cpu_baseline(cfg_w, args.cpu_requests)
     return line
 
 
@@ -571,7 +655,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
-    ap.add_argument("--workload", default="b32_32k")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--configs", default=DEFAULT_CONFIGS,
+                    help="further workloads measured after the headline, comma-separated ('none' for none)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch size (smaller profiling cases)")
     ap.add_argument("--flush", default="none", choices=("none", "read", "write"),
                     help="L2 treatment before each timed step: none (per-step inputs exceed L2), "

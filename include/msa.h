@@ -295,6 +295,11 @@ size_t msa_sparse_gqa_workspace_size(const msa_dims_t* dims, msa_dtype_t kv_dtyp
  * (B * Q * G * (topk * 8,320 + 8)), 256-byte aligned: split-K partials and one
  * tagged ticket per row. Its contents need no initialisation and are not
  * meaningful after the call; calls that overlap on the GPU must not share it.
+ * Each call tags its tickets with a new epoch, but a captured CUDA graph
+ * replays the epoch of its capture: after a launch that raised
+ * MSA_FLAG_TIMEOUT, a ticket may keep that launch's partial count, so zero the
+ * workspace (or capture again) before replaying such a graph. Direct calls
+ * are unaffected.
  */
 msa_status_t msa_sparse_gqa_decode(const msa_dims_t* dims, const void* q, const msa_kv_cache_t* cache,
                                    const int32_t* block_table, const int32_t* seq_lens,
@@ -324,11 +329,15 @@ msa_status_t msa_select_sparse_gqa_decode(const msa_dims_t* dims, const void* q,
  * without the workspace: the split-K partials go to a 64 MiB array inside the
  * library, which every GPU that loads the library holds until the process
  * exits. The first call on a device looks up that array's address (make it
- * before any stream capture on that device). All calls on a device share the
+ * before any stream capture on that device); so does the first call after the
+ * device's context changed (after a cudaDeviceReset, for example), which
+ * should also come before any capture. All calls on a device share the
  * array, so calls whose kernels overlap on the GPU race; nothing in it needs
  * to start at zero. Shapes whose workspace (msa_sparse_gqa_workspace_size:
  * B * Q * G * (topk * 8,320 + 8) bytes) exceeds 64 MiB return
- * MSA_ERR_WORKSPACE without launching.
+ * MSA_ERR_WORKSPACE without launching. After a call that raised
+ * MSA_FLAG_TIMEOUT, a captured graph of this call must be captured again
+ * before it is replayed (the array cannot be zeroed from outside).
  * Calls no allocating routine.
  */
 msa_status_t msa_sparse_gqa_decode_noalloc(const msa_dims_t* dims, const void* q, const msa_kv_cache_t* cache,

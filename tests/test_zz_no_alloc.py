@@ -44,6 +44,37 @@ def test_noalloc_matches_workspace_entry_point(name, changes):
         assert np.abs(l - ref_lse).max() <= parity.LSE_ABS, f"call {call}"
 
 
+def test_noalloc_split_rows_across_changing_shapes():
+    """NVFP4 K/V rows are split over CTAs and merged through the scratch array.
+    A large batch, then a small one with other lengths, then the large one
+    again: each call finds the previous call's partials and tickets in the
+    array (laid out for another shape) and must still match the workspace
+    entry point."""
+    big = parity.build(synth.scaled(synth.WORKLOADS["nvfp4_256k"], batch=64, ctx=3000))
+    small = parity.build(synth.scaled(synth.WORKLOADS["nvfp4_256k"], batch=3, ctx=None, ctx_range=(900, 5000),
+                                      seed=20261301))
+    refs = {}
+    for name, dw in (("big", big), ("small", small)):
+        dw.index_score()
+        dw.select()
+        dw.attend()
+        torch.cuda.synchronize()
+        assert msa.read_device_flags(dw.flags) == 0
+        refs[name] = (dw.out.float().cpu().numpy(), dw.lse.cpu().numpy())
+    for name, dw in (("big", big), ("small", small), ("big", big)):
+        out = torch.full_like(dw.out, float("nan"))
+        lse = torch.full_like(dw.lse, float("nan"))
+        msa.sparse_gqa_decode_noalloc(dw.dims, dw.q, dw.cache, dw.block_table_d, dw.seq_lens_d, dw.selected, out,
+                                      lse, dw.flags)
+        assert msa.read_device_flags(dw.flags) == 0
+        o, l = out.float().cpu().numpy(), lse.cpu().numpy()
+        ro, rl = refs[name]
+        assert np.isfinite(o).all() and np.isfinite(l).all(), name
+        err = np.abs(o - ro)
+        assert err.max() <= parity.OUT_MAX_ABS and err.mean() <= parity.OUT_MEAN_ABS, name
+        assert np.abs(l - rl).max() <= parity.LSE_ABS, name
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     # 64 MiB holds about 8,000 split-K partials of 8,320 bytes
     dims = msa.make_dims(64, 8, max_blocks_per_seq=4, num_pages=8)      # 64 * 8 * 4 * 16 = 32768 partials
