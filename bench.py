@@ -51,6 +51,9 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     ("index_score", "b32_32k", "b355f71dbdd4de60"): 551650816 + 258048,
     ("sparse_gqa", "b32_32k", "a1d657ef6852a159"): 134992128 + 123648,
+    ("index_score", "ragged", "b355f71dbdd4de60"): 2316355328 + 937728,
+    ("sparse_gqa", "ragged", "a1d657ef6852a159"): 270275072 + 466944,
+    ("sparse_gqa", "spec8", "a1d657ef6852a159"): 1057814784 + 3709696,
 }
 
 # The headline workload (the largest configuration on one GPU: batch 64, ragged
