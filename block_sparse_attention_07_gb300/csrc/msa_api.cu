@@ -21,6 +21,19 @@ int device_sm_count() {
   return cached[dev];
 }
 
+// One thread waits on an mbarrier that nothing arrives at, through the bounded
+// wait every kernel of the library uses; when the wait gives up it records
+// MSA_FLAG_TIMEOUT and the kernel returns. No copy targets the barrier or the
+// CTA's shared memory, so giving up leaves nothing in flight.
+__global__ void bounded_wait_selftest_kernel(uint32_t* flags) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_addr(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  if (!mbar_wait(b, 0)) set_flag(flags, MSA_FLAG_TIMEOUT);
+}
+
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Shape rules shared by every entry point.
@@ -369,6 +382,15 @@ msa_status_t msa_select_sparse_gqa_decode(const msa_dims_t* dims, const void* q,
   if (scores == nullptr) return MSA_ERR_INVALID_ARG;
   return sparse_gqa_common(dims, q, cache, block_table, seq_lens, selected, scores, out, lse, workspace,
                            workspace_bytes, dev_flags, stream);
+}
+
+msa_status_t msa_selftest_bounded_wait(uint32_t* dev_flags, void* stream) {
+  if (dev_flags == nullptr) return MSA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(dev_flags);
+  const cudaError_t err = cudaGetLastError();
+  g_record.set("selftest bounded_wait grid=1 block=32");
+  return err == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 msa_status_t msa_read_device_flags(const uint32_t* dev_flags, uint32_t* host_flags, void* stream) {

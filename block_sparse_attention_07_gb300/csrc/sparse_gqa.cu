@@ -840,6 +840,387 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
 }
 
 // ---------------------------------------------------------------------------
+// Several query positions per request (speculative verification: "MiniMax M3
+// vLLM サポート：…", section "EAGLE3 を用いた投機的デコード", every draft
+// position of a request in one decode pass). The positions of one (request,
+// KV head) pair share their local block and often more, so this form streams
+// the union of their selected blocks once instead of once per position. One
+// CTA owns a (request, KV head) group: a producer warp copies each union block
+// (bf16 K and V, 64 KB) into a stage, and consumer warp j attends for query
+// position j over the blocks of its own selection, all 128 tokens of each in
+// four 32-token slices, with its own online softmax and causal limit. A stage
+// is released once every position that selected its block has used it; when
+// the producer fills a stage it arrives in advance for the positions that did
+// not select the block. Each position's output is complete in one warp, so
+// there is no split-K merge. Every wait is bounded.
+
+constexpr int kUnWarps = 8;                      // consumer warps: one per query position (q_len <= 8)
+constexpr int kUnStages = 3;                     // 64 KB bf16 K/V tiles
+constexpr int kUnMaxNB = 8192;                   // block bitmaps kept in shared memory up to this many blocks
+
+struct UnLayout {
+  uint32_t stages, surv, bits, ubits, prefix, tags, bars, total;
+};
+
+// nw = 32-bit words per block bitmap (ceil(NB / 32)).
+__host__ __device__ inline UnLayout un_layout(int nw) {
+  UnLayout s{};
+  s.stages = 0;
+  s.surv = kUnStages * kTileBytes;                               // fused selection: each warp's survivors
+  s.bits = s.surv + (1 + kUnWarps) * (kWarpSurvCap + 8) * 8;     // [kUnWarps][nw] selected blocks per position
+  s.ubits = s.bits + kUnWarps * nw * 4;                          // [nw] their union
+  s.prefix = s.ubits + nw * 4;                                   // [nw] union blocks in the words before
+  s.tags = s.prefix + nw * 4;                                    // [kUnStages] union index held by each stage, abort word
+  s.bars = (s.tags + (kUnStages + 2) * 4 + 7) & ~7u;
+  s.total = s.bars + 2 * kUnStages * 8;
+  return s;
+}
+
+__device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Waits until *tag == n (a stage filled with union block n), bounded in time.
+__device__ __forceinline__ bool wait_tag(const volatile int* tag, int n) {
+  if (*tag == n) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int k = 0; k < 64; ++k)
+      if (*tag == n) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__global__ void __launch_bounds__(32 * (1 + kUnWarps), 1)
+    sparse_gqa_union_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                            GqaParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base_addr = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base_addr - raw);
+  const int nw = (p.NB + 31) >> 5;
+  const UnLayout Ly = un_layout(nw);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(sm + Ly.bits);
+  uint32_t* ubits = reinterpret_cast<uint32_t*>(sm + Ly.ubits);
+  int* prefix = reinterpret_cast<int*>(sm + Ly.prefix);
+  volatile int* tags = reinterpret_cast<volatile int*>(sm + Ly.tags);
+  volatile int* abort_flag = tags + kUnStages;
+  volatile int* group_total = tags + kUnStages + 1;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + Ly.bars);
+  uint64_t* empty = full + kUnStages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  griddep_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kUnStages; ++s) {
+      mbar_init(smem_addr(&full[s]), 1);
+      mbar_init(smem_addr(&empty[s]), kUnWarps);
+      tags[s] = -1;
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
+  }
+  __syncthreads();
+  griddep_wait();
+
+  const int groups = p.B * p.G;
+  const int j = warp - 1;                       // consumers: query position
+  const int gr = lane >> 2, c = lane & 3;
+  int n_base = 0;                               // union index of the group's first block (counted over the CTA's groups)
+  int n_issued = 0;                             // producer: union blocks whose copies it issued
+  bool ok = true;
+
+  // ldmatrix offsets inside a 32-token slice (slice q adds q * 4096 bytes,
+  // which keeps every row's 128-byte swizzle phase)
+  uint32_t k_off[2], v_off[4];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) k_off[h] = (lane & 7) * 128u + ((((4 * h) + (lane >> 3)) ^ (lane & 7)) << 4);
+#pragma unroll
+  for (int h = 0; h < 4; ++h)
+    v_off[h] = (8 * ((lane >> 3) & 1) + (lane & 7)) * 128u + ((((2 * h) + (lane >> 4)) ^ (lane & 7)) << 4);
+
+  for (int grp = blockIdx.x; grp < groups; grp += gridDim.x) {
+    const int b = grp / p.G, g = grp - b * p.G;
+    const int L = p.seq_lens[b];
+    const bool len_ok = L >= p.Q && L >= 1 && L <= p.NB * kBlock;
+    // 1. (fused) selection of the group's rows; bitmaps cleared
+    for (int i = threadIdx.x; i < kUnWarps * nw; i += blockDim.x) bits[i] = 0u;
+    if (p.scores != nullptr && warp < p.Q) {
+      const int64_t row_off = (static_cast<int64_t>(b) * p.Q + warp) * p.G + g;
+      int32_t* out = p.sel_out + row_off * p.K;
+      uint64_t* surv = reinterpret_cast<uint64_t*>(sm + Ly.surv) + warp * (kWarpSurvCap + 8);
+      if (!len_ok) {
+        for (int e = lane; e < p.K; e += 32) out[e] = -1;
+      } else {
+        warp_select_row(p.scores + row_off * p.NB, (L - p.Q + warp) / kBlock, p.K, out, surv,
+                        reinterpret_cast<int*>(surv + kWarpSurvCap), lane);
+      }
+    }
+    __syncthreads();
+    // 2. each position's valid selected blocks into its bitmap
+    if (j >= 0 && j < p.Q) {
+      if (!len_ok) {
+        if (j == 0 && lane == 0) set_flag(p.flags, MSA_FLAG_BAD_SEQLEN);
+      } else {
+        const int ell = (L - p.Q + j) / kBlock;
+        const int32_t* sel = p.selected + ((static_cast<int64_t>(b) * p.Q + j) * p.G + g) * p.K;
+        for (int e = lane; e < p.K; e += 32) {
+          const int blk = sel[e];
+          if (blk < 0) continue;
+          if (blk > ell) { set_flag(p.flags, MSA_FLAG_BAD_BLOCK); continue; }
+          const int page = p.block_table[static_cast<int64_t>(b) * p.NB + blk];
+          if (page < 0 || page >= p.P) { set_flag(p.flags, MSA_FLAG_BAD_PAGE); continue; }
+          atomicOr(&bits[j * nw + (blk >> 5)], 1u << (blk & 31));
+        }
+      }
+    }
+    __syncthreads();
+    // 3. union and its running count per word (producer warp)
+    if (warp == 0) {
+      int run = 0;
+      for (int w0 = 0; w0 < nw; w0 += 32) {
+        const int w = w0 + lane;
+        uint32_t u = 0u;
+        if (w < nw)
+          for (int q = 0; q < p.Q; ++q) u |= bits[q * nw + w];
+        const int cnt = __popc(u);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(kAll, incl, o);
+          if (lane >= o) incl += t;
+        }
+        if (w < nw) {
+          ubits[w] = u;
+          prefix[w] = run + incl - cnt;
+        }
+        run += __shfl_sync(kAll, incl, 31);
+      }
+      if (lane == 0) *group_total = run;
+    }
+    __syncthreads();
+    const int total = *group_total;
+
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer --
+      int n = n_base;
+      for (int w = 0; w < nw && ok; ++w) {
+        uint32_t u = ubits[w];
+        while (u != 0u && ok) {
+          const int bit = __ffs(u) - 1;
+          u &= u - 1u;
+          if (lane == 0) {
+            const int s = n % kUnStages;
+            const uint32_t ph = static_cast<uint32_t>(n / kUnStages) & 1u;
+            if (!mbar_wait(smem_addr(&empty[s]), ph ^ 1u)) {
+              set_flag(p.flags, MSA_FLAG_TIMEOUT);
+              ok = false;
+            } else {
+              int users = 0;
+              for (int q = 0; q < p.Q; ++q) users += (bits[q * nw + w] >> bit) & 1;
+              tags[s] = n;
+              if (users < kUnWarps) mbar_arrive_n(smem_addr(&empty[s]), static_cast<uint32_t>(kUnWarps - users));
+              const int blk = (w << 5) + bit;
+              const int page = p.block_table[static_cast<int64_t>(b) * p.NB + blk];
+              const int y = static_cast<int>((static_cast<int64_t>(page) * p.G + g) * kBlock);
+              const uint32_t fb = smem_addr(&full[s]);
+              const uint32_t dst = base_addr + Ly.stages + s * kTileBytes;
+              mbar_arrive_expect_tx(fb, kTileBytes);
+              tma_load_2d(dst, &tk, 0, y, fb);
+              tma_load_2d(dst + kBoxBytes, &tk, 64, y, fb);
+              tma_load_2d(dst + 2 * kBoxBytes, &tv, 0, y, fb);
+              tma_load_2d(dst + 3 * kBoxBytes, &tv, 64, y, fb);
+            }
+          }
+          ok = __shfl_sync(kAll, ok ? 1 : 0, 0) != 0;
+          if (ok) n_issued = n + 1;
+          ++n;
+        }
+      }
+    } else if (j < p.Q) {
+      // ------------------------------------------------- consumer: position j --
+      const int pj = L - p.Q + j;                 // causal limit of position j (valid when len_ok)
+      const int ell = pj / kBlock;
+      const int last_blk = (L - 1) / kBlock;      // block holding the last cached token
+      uint32_t qf[8][4];
+      float o[16][4];
+      float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
+      const float mul = p.scale_log2;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+      if (len_ok) {
+        const uint16_t* qh =
+            p.q + ((static_cast<int64_t>(b) * p.Q + j) * p.H + static_cast<int64_t>(g) * kGroup) * kDim;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const uint16_t* row = qh + (gr + 8 * r) * kDim + 16 * s + 2 * c;
+            qf[s][r] = *reinterpret_cast<const uint32_t*>(row);
+            qf[s][2 + r] = *reinterpret_cast<const uint32_t*>(row + 8);
+          }
+        }
+      }
+      for (int w = 0; w < nw && ok && len_ok; ++w) {
+        uint32_t mine = bits[j * nw + w];
+        const uint32_t uw = ubits[w];
+        const int pw = prefix[w];
+        while (mine != 0u) {
+          const int bit = __ffs(mine) - 1;
+          mine &= mine - 1u;
+          const int blk = (w << 5) + bit;
+          const int n = n_base + pw + __popc(uw & ((1u << bit) - 1u));
+          const int s = n % kUnStages;
+          if (!wait_tag(tags + s, n) ||
+              !mbar_wait(smem_addr(&full[s]), static_cast<uint32_t>(n / kUnStages) & 1u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t kt = base_addr + Ly.stages + s * kTileBytes;
+#pragma unroll 1
+          for (int qs = 0; qs < kBlock / kTokPerWarp; ++qs) {
+            const uint32_t ks = kt + qs * (kTokPerWarp * 128u);
+            float sc[kNT][4];
+#pragma unroll
+            for (int nt = 0; nt < kNT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+            for (int sp = 0; sp < 4; ++sp) {
+              const uint32_t kb = ks + (sp >> 1) * kBoxBytes + k_off[sp & 1];
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {          // two n-tiles at a time: 9 warps leave 168 registers
+                uint32_t bq[2][4];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+                  ldsm_x4(kb + (2 * h2 + nt) * 8 * 128, bq[nt][0], bq[nt][1], bq[nt][2], bq[nt][3]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) mma_bf16(sc[2 * h2 + nt], qf[2 * sp], bq[nt][0], bq[nt][1]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) mma_bf16(sc[2 * h2 + nt], qf[2 * sp + 1], bq[nt][2], bq[nt][3]);
+              }
+            }
+            const int tbase = blk * kBlock + qs * kTokPerWarp;
+            if (blk == ell) {                       // causal limit of this position
+#pragma unroll
+              for (int nt = 0; nt < kNT; ++nt) {
+                const int t0 = tbase + 8 * nt + 2 * c;
+                if (t0 > pj) { sc[nt][0] = -INFINITY; sc[nt][2] = -INFINITY; }
+                if (t0 + 1 > pj) { sc[nt][1] = -INFINITY; sc[nt][3] = -INFINITY; }
+              }
+            }
+            // online softmax, log2 domain (as in sparse_gqa_kernel)
+            float bmax[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              float mx = -INFINITY;
+#pragma unroll
+              for (int nt = 0; nt < kNT; ++nt) mx = fmaxf(mx, fmaxf(sc[nt][2 * r], sc[nt][2 * r + 1]));
+              mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 1));
+              mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 2));
+              bmax[r] = mx * mul;
+            }
+            const bool raise0 = bmax[0] > m_r[0] + kRescaleSlack, raise1 = bmax[1] > m_r[1] + kRescaleSlack;
+            if (__any_sync(kAll, raise0 || raise1)) {
+              float alpha[2] = {1.f, 1.f};
+              if (raise0) { alpha[0] = ex2_approx(m_r[0] - bmax[0]); m_r[0] = bmax[0]; }
+              if (raise1) { alpha[1] = ex2_approx(m_r[1] - bmax[1]); m_r[1] = bmax[1]; }
+#pragma unroll
+              for (int r = 0; r < 2; ++r) {
+                l_r[r] *= alpha[r];
+#pragma unroll
+                for (int n2 = 0; n2 < 16; ++n2) {
+                  o[n2][2 * r] *= alpha[r];
+                  o[n2][2 * r + 1] *= alpha[r];
+                }
+              }
+            }
+            // V rows past the last cached token may hold any bytes (never
+            // written); every position masks them, and each warp that reads
+            // this block zeroes them first (all writers store zeros)
+            if (blk == last_blk && tbase + lane > L - 1) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t row = ks + (2 + h) * kBoxBytes + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) st_shared_zero16(row + 16u * i);
+              }
+              fence_proxy_async_smem();
+            }
+            __syncwarp();
+            float pr[kNT][4];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const float neg_ref = m_r[r] == -INFINITY ? 0.f : -m_r[r];
+              float ls = 0.f;
+#pragma unroll
+              for (int nt = 0; nt < kNT; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const float pv = ex2_approx(fmaf(sc[nt][2 * r + e], mul, neg_ref));
+                  pr[nt][2 * r + e] = pv;
+                  ls += pv;
+                }
+              }
+              l_r[r] += ls;
+            }
+#pragma unroll
+            for (int kk = 0; kk < kKK; ++kk) {
+              uint32_t a[4];
+              a[0] = pack_bf16x2(pr[2 * kk][0], pr[2 * kk][1]);
+              a[1] = pack_bf16x2(pr[2 * kk][2], pr[2 * kk][3]);
+              a[2] = pack_bf16x2(pr[2 * kk + 1][0], pr[2 * kk + 1][1]);
+              a[3] = pack_bf16x2(pr[2 * kk + 1][2], pr[2 * kk + 1][3]);
+#pragma unroll
+              for (int np = 0; np < 8; ++np) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(ks + (2 + (np >> 2)) * kBoxBytes + kk * 16 * 128 + v_off[np & 3], b0, b1, b2, b3);
+                mma_bf16(o[2 * np], a, b0, b1);
+                mma_bf16(o[2 * np + 1], a, b2, b3);
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+        }
+      }
+      // position j's output: 16 heads of KV head g
+      float lt[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        float v = l_r[r];
+        v += __shfl_xor_sync(kAll, v, 1);
+        v += __shfl_xor_sync(kAll, v, 2);
+        lt[r] = v;
+      }
+      const int64_t head0 = (static_cast<int64_t>(b) * p.Q + j) * p.H + static_cast<int64_t>(g) * kGroup;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float inv = lt[r] > 0.f ? 1.f / lt[r] : 0.f;
+        uint16_t* orow = p.out + (head0 + gr + 8 * r) * kDim + 2 * c;
+#pragma unroll
+        for (int n2 = 0; n2 < 16; ++n2)
+          *reinterpret_cast<uint32_t*>(orow + 8 * n2) = pack_bf16x2(o[n2][2 * r] * inv, o[n2][2 * r + 1] * inv);
+        if (p.lse != nullptr && c == 0)
+          p.lse[head0 + gr + 8 * r] = lt[r] > 0.f ? (m_r[r] + log2f(lt[r])) * kLn2 : -INFINITY;
+      }
+    }
+    if (!ok) *abort_flag = 1;
+    n_base += total;
+    __syncthreads();                 // the next group rebuilds the bitmaps
+    if (*abort_flag) break;
+  }
+  if (*abort_flag && lane == 0) set_flag(p.flags, MSA_FLAG_TIMEOUT);
+  if (warp == 0 && lane == 0) {
+    // no copy of this CTA may still be in flight when it exits
+    const int first = n_issued > kUnStages ? n_issued - kUnStages : 0;
+    for (int k = first; k < n_issued; ++k)
+      if (!mbar_wait(smem_addr(&full[k % kUnStages]), static_cast<uint32_t>((k / kUnStages) & 1))) break;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // bf16 K/V on the fifth-generation tensor cores. The 16-head tile is below
 // tcgen05's minimum M, so both products run transposed:
 //   S^T = K Q^T   (M = 128 tokens, N = 16 heads, K = 128 dims)
@@ -1369,6 +1750,19 @@ static bool bf16_tcgen05_selected() {
   return e != nullptr && strcmp(e, "tcgen05") == 0;
 }
 
+// With several query positions and bf16 K/V, the union form (one CTA per
+// (request, KV head), each block read once) is used when there are at least
+// three groups for every four SMs; with fewer the per-position rows spread
+// better over the SMs. MSA_MULTIPOS_ATTENTION=union or =rows in the environment
+// (read on every call) forces one form.
+static bool multipos_union_selected(const GqaArgs& a, int sms) {
+  if (a.Q < 2 || a.NB > kUnMaxNB) return false;
+  const char* e = getenv("MSA_MULTIPOS_ATTENTION");
+  if (e != nullptr && strcmp(e, "union") == 0) return true;
+  if (e != nullptr && strcmp(e, "rows") == 0) return false;
+  return 4ll * a.B * a.G >= 3ll * sms;
+}
+
 cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRecord* rec) {
   GqaParams p;
   p.q = a.q;
@@ -1423,6 +1817,21 @@ cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRec
   p.epoch = epoch.fetch_add(1);
   if (p.epoch == 0) p.epoch = epoch.fetch_add(1);    // 0 never tags a ticket
   p.tickets = reinterpret_cast<unsigned long long*>(a.workspace + (p.W / p.K) * p.K * kPartialFloats);
+  if (!a.nvfp4 && !a.fp8 && !bf16_tcgen05_selected() && multipos_union_selected(a, sms)) {
+    // several positions, bf16 K/V: the union of each group's blocks, one CTA per group
+    const int nw = (a.NB + 31) / 32;
+    const size_t usmem = un_layout(nw).total + 1024;
+    const int64_t groups = static_cast<int64_t>(a.B) * a.G;
+    const int UC = static_cast<int>(groups < sms ? groups : sms);
+    err = cudaFuncSetAttribute(sparse_gqa_union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(usmem));
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(sparse_gqa_union_kernel, dim3(UC), dim3(32 * (1 + kUnWarps)), usmem, stream, tk, tv, p);
+    rec->set("%ssparse_gqa bf16_tma_mma union_of_positions grid=%d block=%d smem=%zu stages=%d groups=%lld",
+             a.scores != nullptr ? "select+" : "", UC, 32 * (1 + kUnWarps), usmem, kUnStages,
+             static_cast<long long>(groups));
+    return err != cudaSuccess ? err : cudaGetLastError();
+  }
   if (!a.nvfp4 && !a.fp8 && bf16_tcgen05_selected()) {
     // bf16 K/V on the tcgen05 kernel, when selected (whole rows)
     const size_t tsmem = tc_layout().total + 1024;

@@ -26,7 +26,7 @@ FLAG_BAD_PAGE, FLAG_BAD_BLOCK, FLAG_BAD_SEQLEN, FLAG_BAD_SLOT, FLAG_TIMEOUT, FLA
 EXPORTED = ("msa_abi_version", "msa_status_string", "msa_get_last_dispatch", "msa_kv_insert_quant",
             "msa_index_score", "msa_insert_index_score", "msa_select_blocks", "msa_sparse_gqa_workspace_size",
             "msa_sparse_gqa_decode", "msa_sparse_gqa_decode_noalloc", "msa_read_device_flags",
-            "msa_qk_norm_rope_insert", "msa_select_sparse_gqa_decode")
+            "msa_qk_norm_rope_insert", "msa_select_sparse_gqa_decode", "msa_selftest_bounded_wait")
 
 
 class Dims(ctypes.Structure):
@@ -85,6 +85,7 @@ def _load():
     lib.msa_sparse_gqa_decode_noalloc.argtypes = [ctypes.POINTER(Dims), vp, ctypes.POINTER(_KVCache), vp, vp, vp,
                                                   vp, vp, vp, vp]
     lib.msa_read_device_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+    lib.msa_selftest_bounded_wait.argtypes = [vp, vp]
     lib.msa_qk_norm_rope_insert.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, vp, vp, vp, vp, i32,
                                             ctypes.POINTER(NormRope), vp, vp, ctypes.POINTER(_KVCache),
                                             ctypes.POINTER(_IndexCache), vp, vp]
@@ -267,6 +268,12 @@ def sparse_gqa_decode_noalloc(dims: Dims, q, cache: KVCache, block_table, seq_le
                                            _ptr(seq_lens), _ptr(selected), _ptr(out), _ptr(lse), _ptr(flags),
                                            _stream(stream))
     _check(st, "msa_sparse_gqa_decode_noalloc")
+
+
+def selftest_bounded_wait(flags, stream=None):
+    """msa_selftest_bounded_wait: a kernel whose barrier wait runs out (about 2 s)
+    and reports MSA_FLAG_TIMEOUT in ``flags``."""
+    _check(lib.msa_selftest_bounded_wait(_ptr(flags), _stream(stream)), "msa_selftest_bounded_wait")
 
 
 def read_device_flags(flags, stream=None) -> int:

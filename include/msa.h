@@ -345,6 +345,17 @@ msa_status_t msa_sparse_gqa_decode_noalloc(const msa_dims_t* dims, const void* q
                                            const int32_t* selected, void* out, float* lse, uint32_t* dev_flags,
                                            void* stream);
 
+/*
+ * Diagnostic of the bounded waits (the pages have no counterpart). Launches
+ * one thread that waits on a shared-memory barrier which nothing completes,
+ * through the same bounded wait the library's kernels use; when the wait gives
+ * up (after about 2 s) the kernel ORs MSA_FLAG_TIMEOUT into *dev_flags and
+ * returns. No copy is in flight when it gives up, so the context stays usable:
+ * a caller can check on its GPU that a kernel whose wait runs out reports an
+ * error status instead of hanging. Asynchronous on `stream`.
+ */
+msa_status_t msa_selftest_bounded_wait(uint32_t* dev_flags, void* stream);
+
 /* Synchronises `stream`, copies *dev_flags to *host_flags (host pointer) and
  * returns MSA_ERR_DEVICE_FLAG if any bit is set, MSA_OK otherwise. */
 msa_status_t msa_read_device_flags(const uint32_t* dev_flags, uint32_t* host_flags, void* stream);

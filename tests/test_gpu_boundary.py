@@ -119,3 +119,19 @@ def test_fused_selection_flags_bad_pages_and_lengths():
     assert dw.check_flags() & msa.FLAG_BAD_SEQLEN
     assert (dw.selected[1] == -1).all()
     assert torch.isfinite(dw.out.float()).all()
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """A kernel whose barrier wait runs out (nothing completes it; no copy in
+    flight) sets MSA_FLAG_TIMEOUT and returns; the context stays usable: a
+    decode step afterwards runs clean and matches the one before."""
+    w, dw = _small()
+    dw.step()
+    assert dw.check_flags() == 0
+    before = dw.out.clone()
+    msa.selftest_bounded_wait(dw.flags)
+    assert dw.check_flags() == msa.FLAG_TIMEOUT
+    dw.flags.zero_()
+    dw.step()
+    assert dw.check_flags() == 0
+    assert torch.equal(dw.out, before)
