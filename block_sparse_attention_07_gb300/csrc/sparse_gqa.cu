@@ -840,6 +840,473 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
 }
 
 // ---------------------------------------------------------------------------
+// NVFP4 K/V ("MiniMax-M3.1-Flash Day-0 対応", section "何が新しいか": E2M1
+// values with an E4M3 scale per 16 and an fp32 global scale, 576 bytes per
+// token per layer). A block's 18 KB hold too little data to hide the
+// conversion behind the copy, so this form spreads every block over eight
+// consumer warps of 16 tokens (two warps per SM sub-partition, which overlap
+// each other's dependency chains). There is no producer warp: warp 0 also
+// issues the copies, up to kF4Stages blocks ahead of the slowest warp. K codes
+// are converted straight into mma operands: lane (r, c) of an n-tile loads the
+// 16 code bytes 16c .. 16c + 15 of token r (dims 32c .. 32c + 31), so k-step s
+// of the product takes dims 32c + 4s .. + 3 from every lane, and the query
+// fragments are loaded with the same dims. V is expanded (E2M1 x E4M3 is exact
+// in fp16) into the warp's rows of a swizzled fp16 tile, with the rows past
+// the causal limit written as zeros, and read with ldmatrix.trans for P V. The
+// fp32 global scales multiply the logits and the output. Item ranges are
+// balanced over the CTAs and split rows merged through the workspace, as in
+// sparse_gqa_kernel.
+
+constexpr int kF4Warps = 8;
+constexpr int kF4Tok = kBlock / kF4Warps;          // 16 tokens per warp and block
+constexpr int kF4Stages = 6;
+constexpr uint32_t kF4Codes = kBlock * kDim / 2;   // 8 KB of E2M1 codes per K or V block
+constexpr uint32_t kF4Scales = kBlock * kDim / 16; // 1 KB of E4M3 scales
+
+struct F4Layout {
+  uint32_t stages, vtile, comb_o, comb_ml, bars, total;
+};
+__host__ __device__ constexpr F4Layout f4_layout() {
+  F4Layout s{};
+  s.stages = 0;
+  s.vtile = kF4Stages * kFp4StageBytes;                     // fp16 V: two 128-row x 64-dim swizzled boxes
+  s.comb_o = s.vtile + 2 * kBoxBytes;
+  s.comb_ml = s.comb_o + kF4Warps * kGroup * kDim * 4;
+  s.bars = s.comb_ml + kF4Warps * kGroup * 2 * 4;
+  s.total = s.bars + (2 * kF4Stages + 2) * 8 + 16;          // + the last-arriver flag
+  return s;
+}
+
+__global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  constexpr F4Layout Ly = f4_layout();
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base_addr = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base_addr - raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + Ly.bars);
+  uint64_t* empty = full + kF4Stages;
+  uint64_t* gbar = empty + kF4Stages;        // [0]: states staged, [1]: states read
+  float* comb_o = reinterpret_cast<float*>(sm + Ly.comb_o);
+  float* comb_m = reinterpret_cast<float*>(sm + Ly.comb_ml);
+  float* comb_l = comb_m + kF4Warps * kGroup;
+  int* last_flag = reinterpret_cast<int*>(sm + Ly.bars + (2 * kF4Stages + 2) * 8);
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gr = lane >> 2, c = lane & 3;
+
+  griddep_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kF4Stages; ++s) {
+      mbar_init(smem_addr(&full[s]), 1);
+      mbar_init(smem_addr(&empty[s]), kF4Warps);
+    }
+    mbar_init(smem_addr(&gbar[0]), kF4Warps);
+    mbar_init(smem_addr(&gbar[1]), kF4Warps);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  griddep_wait();
+
+  const int C = gridDim.x;
+  const int64_t x0 = p.W * blockIdx.x / C, x1 = p.W * (blockIdx.x + 1) / C;
+  if (x0 >= x1) return;
+  if (p.scores != nullptr) {
+    // Stage 2 inside this launch: every warp selects rows this CTA touches
+    // (rows shared with other CTAs get the same result from each), staging its
+    // survivors in the row-merge buffer, unused until a row ends.
+    uint64_t* surv = reinterpret_cast<uint64_t*>(sm + Ly.comb_o) + w * (kWarpSurvCap + 8);
+    int* chosen = reinterpret_cast<int*>(surv + kWarpSurvCap);
+    for (int64_t r = x0 / p.K + w; r <= (x1 - 1) / p.K; r += kF4Warps) {
+      const RowPos rp = row_pos(p, r);
+      const int64_t row_off = (static_cast<int64_t>(rp.b) * p.Q + rp.j) * p.G + rp.g;
+      int32_t* out = p.sel_out + row_off * p.K;
+      const int L = p.seq_lens[rp.b];
+      if (L < p.Q || L > p.NB * kBlock || L < 1) {           // (flagged by the item loads below)
+        for (int e = lane; e < p.K; e += 32) out[e] = -1;
+        continue;
+      }
+      warp_select_row(p.scores + row_off * p.NB, (L - p.Q + rp.j) / kBlock, p.K, out, surv, chosen, lane);
+    }
+    __syncthreads();                  // the item loads below read these rows back
+  }
+  const uint64_t pol = l2_evict_first_policy();
+  uint32_t gph[2] = {0u, 0u};
+  bool ok = true;
+
+  // Item cursor (every warp): `cur` holds the infos of items base .. base + 31,
+  // `nxt` the next 32. Warp 0 reports bad items (it also issues their copies).
+  ItemInfo cur = load_item(p, x0 + lane, x1, w == 0);
+  ItemInfo nxt = load_item(p, x0 + 32 + lane, x1, w == 0);
+  int64_t base = x0;
+  int kx = 0;
+
+  // Copy issue (warp 0): item ia is the next to examine, `is` counts the valid
+  // items whose copies were issued; the consumers have used `cs` valid items.
+  int64_t ia = x0;
+  int is = 0, cs = 0;
+  auto issue_upto = [&](int need) {
+    // issues the valid items' copies in order: waiting for a free stage until
+    // `need` are issued, then while a stage is already free, at most
+    // kF4Stages items ahead of this warp (items past the 64 loaded infos wait
+    // for a later call)
+    while (ok && ia < x1 && ia < base + 64 && is < cs + kF4Stages) {
+      const int k = static_cast<int>(ia - base);
+      const int valid = __shfl_sync(kAll, k < 32 ? cur.valid : nxt.valid, k & 31);
+      const int page = __shfl_sync(kAll, k < 32 ? cur.page : nxt.page, k & 31);
+      const int g = __shfl_sync(kAll, k < 32 ? cur.g : nxt.g, k & 31);
+      if (!valid) { ++ia; continue; }
+      const int s = is % kF4Stages;
+      const uint32_t par = (static_cast<uint32_t>(is / kF4Stages) & 1u) ^ 1u;
+      int go = 0;
+      if (lane == 0) {
+        if (is < need) go = mbar_wait(smem_addr(&empty[s]), par) ? 1 : -1;
+        else go = mbar_try_wait(smem_addr(&empty[s]), par) ? 1 : 0;
+        if (go == 1) {
+          const uint32_t fb = smem_addr(&full[s]);
+          const uint32_t dst = base_addr + Ly.stages + s * kFp4StageBytes;
+          const int64_t ph = static_cast<int64_t>(page) * p.G + g;
+          mbar_arrive_expect_tx(fb, kFp4StageBytes);
+          bulk_g2s(dst, p.k4 + ph * kF4Codes, kF4Codes, fb, pol);
+          bulk_g2s(dst + kF4Codes, p.ks + ph * kF4Scales, kF4Scales, fb, pol);
+          bulk_g2s(dst + kF4Codes + kF4Scales, p.v4 + ph * kF4Codes, kF4Codes, fb, pol);
+          bulk_g2s(dst + 2 * kF4Codes + kF4Scales, p.vs + ph * kF4Scales, kF4Scales, fb, pol);
+        }
+      }
+      go = __shfl_sync(kAll, go, 0);
+      if (go < 0) { set_flag(p.flags, MSA_FLAG_TIMEOUT); ok = false; break; }
+      if (go == 0) break;
+      ++ia;
+      ++is;
+    }
+  };
+
+  uint32_t qf[8][4];
+  float o[16][4];
+  float m_r[2], l_r[2], mul_r[2];
+  int64_t seg_row = -1;
+  int seg_b = 0, seg_g = 0, seg_j = 0, seg_p = 0, seg_ell = 0;
+
+  auto begin_segment = [&](int64_t r) {
+    const RowPos rp = row_pos(p, r);
+    seg_row = r;
+    seg_b = rp.b; seg_g = rp.g; seg_j = rp.j;
+    seg_p = p.seq_lens[rp.b] - p.Q + rp.j;
+    seg_ell = seg_p / kBlock;
+    const uint16_t* qh = p.q + ((static_cast<int64_t>(rp.b) * p.Q + rp.j) * p.H + static_cast<int64_t>(rp.g) * kGroup) * kDim;
+    // k-step s, lane c: dims 32c + 4s .. + 3 (a0/a1: the first two, a2/a3: the last two)
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint2 wq = *reinterpret_cast<const uint2*>(qh + (gr + 8 * r) * kDim + 32 * c + 4 * s);
+        qf[s][r] = wq.x;
+        qf[s][2 + r] = wq.y;
+      }
+    }
+    // fp16 operands: each query row scaled by an exact power of two into range
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float amax = 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t wq = qf[s][2 * h + r];
+          amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_f32(wq & 0xFFFF)), fabsf(bf16_bits_to_f32(wq >> 16))));
+        }
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(kAll, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(kAll, amax, 2));
+      const int sh = fp16_shift_for(amax);
+      const float f = exp2_int(sh);
+      mul_r[r] = p.scale_log2 * p.k_global * exp2_int(-sh);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t wq = qf[s][2 * h + r];
+          qf[s][2 * h + r] = pack_f16x2(bf16_bits_to_f32(wq & 0xFFFF) * f, bf16_bits_to_f32(wq >> 16) * f);
+        }
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    m_r[0] = m_r[1] = -INFINITY;
+    l_r[0] = l_r[1] = 0.f;
+  };
+
+  // Merges the eight warps' states of the current row; writes the output when
+  // the CTA covered the whole row, a split-K partial otherwise (the CTA that
+  // delivers a row's last partial merges them all).
+  auto end_segment = [&]() -> bool {
+    float lt[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float v = l_r[r];
+      v += __shfl_xor_sync(kAll, v, 1);
+      v += __shfl_xor_sync(kAll, v, 2);
+      lt[r] = v;
+    }
+    {
+      float* mo = comb_o + w * kGroup * kDim;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        *reinterpret_cast<float2*>(mo + gr * kDim + 8 * n + 2 * c) = make_float2(o[n][0], o[n][1]);
+        *reinterpret_cast<float2*>(mo + (gr + 8) * kDim + 8 * n + 2 * c) = make_float2(o[n][2], o[n][3]);
+      }
+      if (c == 0) {
+        comb_m[w * kGroup + gr] = m_r[0];
+        comb_m[w * kGroup + gr + 8] = m_r[1];
+        comb_l[w * kGroup + gr] = lt[0];
+        comb_l[w * kGroup + gr + 8] = lt[1];
+      }
+    }
+    if (!group_sync(smem_addr(&gbar[0]), gph[0], lane)) return false;
+    // 256 threads: head hh = tid / 16, dims d0 .. d0 + 7
+    const int tid = threadIdx.x;
+    const int hh = tid >> 4, d0 = (tid & 15) * 8;
+    float M = -INFINITY, Ls = 0.f;
+    float acc[8];
+#pragma unroll
+    for (int k = 0; k < kF4Warps; ++k) M = fmaxf(M, comb_m[k * kGroup + hh]);
+#pragma unroll
+    for (int d = 0; d < 8; ++d) acc[d] = 0.f;
+#pragma unroll
+    for (int k = 0; k < kF4Warps; ++k) {
+      const float fw = M == -INFINITY ? 0.f : ex2_approx(comb_m[k * kGroup + hh] - M);
+      Ls += fw * comb_l[k * kGroup + hh];
+      const float4 a = *reinterpret_cast<const float4*>(comb_o + (k * kGroup + hh) * kDim + d0);
+      const float4 b = *reinterpret_cast<const float4*>(comb_o + (k * kGroup + hh) * kDim + d0 + 4);
+      acc[0] += fw * a.x; acc[1] += fw * a.y; acc[2] += fw * a.z; acc[3] += fw * a.w;
+      acc[4] += fw * b.x; acc[5] += fw * b.y; acc[6] += fw * b.z; acc[7] += fw * b.w;
+    }
+#pragma unroll
+    for (int d = 0; d < 8; ++d) acc[d] *= p.v_global;
+    const int64_t r = seg_row;
+    const bool whole = x0 <= r * p.K && (r + 1) * p.K <= x1;
+    const int64_t head = (static_cast<int64_t>(seg_b) * p.Q + seg_j) * p.H + static_cast<int64_t>(seg_g) * kGroup + hh;
+    auto write_out = [&](const float (&v)[8], float mm, float ll) {
+      const float inv = ll > 0.f ? 1.f / ll : 0.f;
+      uint4 pk;
+      pk.x = pack_bf16x2(v[0] * inv, v[1] * inv);
+      pk.y = pack_bf16x2(v[2] * inv, v[3] * inv);
+      pk.z = pack_bf16x2(v[4] * inv, v[5] * inv);
+      pk.w = pack_bf16x2(v[6] * inv, v[7] * inv);
+      *reinterpret_cast<uint4*>(p.out + head * kDim + d0) = pk;
+      if (p.lse != nullptr && (tid & 15) == 0) p.lse[head] = ll > 0.f ? (mm + log2f(ll)) * kLn2 : -INFINITY;
+    };
+    if (whole) {
+      write_out(acc, M, Ls);
+      return group_sync(smem_addr(&gbar[1]), gph[1], lane);
+    }
+    const int first = cta_of(r * p.K, p.W, C);
+    const int nslots = cta_of(r * p.K + p.K - 1, p.W, C) - first + 1;
+    float* rowp = p.ws + r * p.K * static_cast<int64_t>(kPartialFloats);
+    float* part = rowp + (static_cast<int>(blockIdx.x) - first) * static_cast<int64_t>(kPartialFloats);
+    {
+      float4* dst = reinterpret_cast<float4*>(part + hh * kDim + d0);
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      if ((tid & 15) == 0) {
+        part[kGroup * kDim + hh] = M;
+        part[kGroup * kDim + kGroup + hh] = Ls;
+      }
+    }
+    if (!group_sync(smem_addr(&gbar[1]), gph[1], lane)) return false;
+    if (tid == 0) {
+      fence_acq_rel_gpu();
+      const bool last = ticket_is_last(p, r, nslots);
+      if (last) fence_acq_rel_gpu();
+      *last_flag = last ? 1 : 0;
+    }
+    if (!group_sync(smem_addr(&gbar[0]), gph[0], lane)) return false;
+    if (*last_flag) {
+      float M2 = -INFINITY;
+      for (int q = 0; q < nslots; ++q) M2 = fmaxf(M2, __ldcg(rowp + q * kPartialFloats + kGroup * kDim + hh));
+      float L2 = 0.f;
+      float v[8];
+#pragma unroll
+      for (int d = 0; d < 8; ++d) v[d] = 0.f;
+      if (M2 != -INFINITY) {
+        for (int q = 0; q < nslots; ++q) {
+          const float* pq = rowp + q * kPartialFloats;
+          const float f = ex2_approx(__ldcg(pq + kGroup * kDim + hh) - M2);
+          L2 += f * __ldcg(pq + kGroup * kDim + kGroup + hh);
+          const float4 a = __ldcg(reinterpret_cast<const float4*>(pq + hh * kDim + d0));
+          const float4 b = __ldcg(reinterpret_cast<const float4*>(pq + hh * kDim + d0 + 4));
+          v[0] += f * a.x; v[1] += f * a.y; v[2] += f * a.z; v[3] += f * a.w;
+          v[4] += f * b.x; v[5] += f * b.y; v[6] += f * b.z; v[7] += f * b.w;
+        }
+      }
+      write_out(v, M2, L2);
+    }
+    return true;
+  };
+
+  const uint32_t vtile = base_addr + Ly.vtile;
+  uint32_t v_off[4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h)
+    v_off[h] = (static_cast<uint32_t>(kF4Tok * w) + 8 * ((lane >> 3) & 1) + (lane & 7)) * 128u +
+               ((((2 * h) + (lane >> 4)) ^ (lane & 7)) << 4);
+
+  int s = 0;
+  uint32_t phase = 0;
+  int64_t xrow = x0 / p.K;
+  int xslot = static_cast<int>(x0 - xrow * p.K);
+  while (ok && base + kx < x1) {
+    if (xrow != seg_row) {
+      if (seg_row >= 0 && !end_segment()) { ok = false; break; }
+      begin_segment(xrow);
+    }
+    const int valid = __shfl_sync(kAll, cur.valid, kx);
+    const int it_blk = __shfl_sync(kAll, cur.blk, kx);
+    if (++xslot == p.K) { xslot = 0; ++xrow; }
+    if (!valid) {
+      if (++kx == 32) { kx = 0; base += 32; cur = nxt; nxt = load_item(p, base + 32 + lane, x1, w == 0); }
+      continue;
+    }
+    if (w == 0) issue_upto(cs + 1);                 // this item's copy, and more while stages are free
+    if (!mbar_wait(smem_addr(&full[s]), phase)) { ok = false; break; }
+    const uint8_t* st = sm + Ly.stages + s * kFp4StageBytes;
+    const int tb = it_blk * kBlock + kF4Tok * w;   // first token of this warp's rows
+    // ---- V rows of this warp -> fp16 tile (rows past the causal limit as zeros)
+    {
+      const int row = kF4Tok * w + (lane >> 1), hh = lane & 1;
+      const uint8_t* vc = st + kF4Codes + kF4Scales + row * 64 + 32 * hh;
+      const uint4 c0 = *reinterpret_cast<const uint4*>(vc);
+      const uint4 c1 = *reinterpret_cast<const uint4*>(vc + 16);
+      const uint32_t sw = *reinterpret_cast<const uint32_t*>(st + 2 * kF4Codes + kF4Scales + row * 8 + 4 * hh);
+      const bool live = tb + (lane >> 1) <= seg_p;
+      const uint32_t s01 = e4m3x2_to_f16x2(static_cast<uint16_t>(sw & 0xFFFF));
+      const uint32_t s23 = e4m3x2_to_f16x2(static_cast<uint16_t>(sw >> 16));
+      const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      const uint32_t box = vtile + hh * kBoxBytes;
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) {               // 16 dims: scale group 4 hh + gg
+        const uint32_t sg = gg < 2 ? s01 : s23;
+        const __half2 scl = __half2half2(__ushort_as_half(static_cast<unsigned short>((gg & 1) ? (sg >> 16) : (sg & 0xFFFF))));
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {                // 8 dims -> one 16-byte chunk
+          uint32_t h[4];
+          e2m1x8_to_f16x2x4(words[2 * gg + k], h);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h[e]), scl);
+            h[e] = live ? *reinterpret_cast<uint32_t*>(&v) : 0u;
+          }
+          const uint32_t a = swz(box, row, 2 * gg + k);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(h[0]), "r"(h[1]), "r"(h[2]),
+                       "r"(h[3])
+                       : "memory");
+        }
+      }
+    }
+    // ---- S = Q K^T for the warp's 16 tokens, K codes converted in registers
+    float sc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+      const int t = kF4Tok * w + 8 * nt + gr;
+      const uint4 cw = *reinterpret_cast<const uint4*>(st + t * 64 + 16 * c);
+      const uint32_t s2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(st + kF4Codes + t * 8 + 2 * c));
+      const __half2 sa = __half2half2(__ushort_as_half(static_cast<unsigned short>(s2 & 0xFFFF)));
+      const __half2 sb = __half2half2(__ushort_as_half(static_cast<unsigned short>(s2 >> 16)));
+      const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {               // word q4: k-steps 2 q4 and 2 q4 + 1
+        uint32_t h[4];
+        e2m1x8_to_f16x2x4(words[q4], h);
+        const __half2 scl = q4 < 2 ? sa : sb;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h[e]), scl);
+          h[e] = *reinterpret_cast<uint32_t*>(&v);
+        }
+        mma_f16(sc[nt], qf[2 * q4], h[0], h[1]);
+        mma_f16(sc[nt], qf[2 * q4 + 1], h[2], h[3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&empty[s]));   // codes no longer needed
+    ++cs;
+    if (++s == kF4Stages) { s = 0; phase ^= 1u; }
+    if (w == 0) issue_upto(cs);
+    // ---- causal limit, online softmax (log2 domain), P V
+    if (it_blk == seg_ell) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int t0 = tb + 8 * nt + 2 * c;
+        if (t0 > seg_p) { sc[nt][0] = -INFINITY; sc[nt][2] = -INFINITY; }
+        if (t0 + 1 > seg_p) { sc[nt][1] = -INFINITY; sc[nt][3] = -INFINITY; }
+      }
+    }
+    float bmax[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float mx = fmaxf(fmaxf(sc[0][2 * r], sc[0][2 * r + 1]), fmaxf(sc[1][2 * r], sc[1][2 * r + 1]));
+      mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 2));
+      bmax[r] = mx * mul_r[r];
+    }
+    const bool raise0 = bmax[0] > m_r[0] + kRescaleSlack, raise1 = bmax[1] > m_r[1] + kRescaleSlack;
+    if (__any_sync(kAll, raise0 || raise1)) {
+      float alpha[2] = {1.f, 1.f};
+      if (raise0) { alpha[0] = ex2_approx(m_r[0] - bmax[0]); m_r[0] = bmax[0]; }
+      if (raise1) { alpha[1] = ex2_approx(m_r[1] - bmax[1]); m_r[1] = bmax[1]; }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        l_r[r] *= alpha[r];
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          o[n][2 * r] *= alpha[r];
+          o[n][2 * r + 1] *= alpha[r];
+        }
+      }
+    }
+    float pr[2][4];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const float neg_ref = m_r[r] == -INFINITY ? 0.f : -m_r[r];
+      float ls = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float pv = ex2_approx(fmaf(sc[nt][2 * r + e], mul_r[r], neg_ref));
+          pr[nt][2 * r + e] = pv;
+          ls += pv;
+        }
+      }
+      l_r[r] += ls;
+    }
+    {
+      uint32_t a[4];
+      a[0] = pack_f16x2(pr[0][0], pr[0][1]);
+      a[1] = pack_f16x2(pr[0][2], pr[0][3]);
+      a[2] = pack_f16x2(pr[1][0], pr[1][1]);
+      a[3] = pack_f16x2(pr[1][2], pr[1][3]);
+      __syncwarp();                                   // the warp's V rows are in the tile
+#pragma unroll
+      for (int np = 0; np < 8; ++np) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vtile + (np >> 2) * kBoxBytes + v_off[np & 3], b0, b1, b2, b3);
+        mma_f16(o[2 * np], a, b0, b1);
+        mma_f16(o[2 * np + 1], a, b2, b3);
+      }
+      __syncwarp();                                   // before the next block's expansion overwrites the rows
+    }
+    if (++kx == 32) { kx = 0; base += 32; cur = nxt; nxt = load_item(p, base + 32 + lane, x1, w == 0); }
+  }
+  if (ok && seg_row >= 0) ok = end_segment();
+  if (!ok && lane == 0) set_flag(p.flags, MSA_FLAG_TIMEOUT);
+  if (w == 0 && lane == 0) {
+    // no copy of this CTA may still be in flight when it exits
+    for (int k = is > kF4Stages ? is - kF4Stages : 0; k < is; ++k)
+      if (!mbar_wait(smem_addr(&full[k % kF4Stages]), static_cast<uint32_t>((k / kF4Stages) & 1))) break;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Several query positions per request (speculative verification: "MiniMax M3
 // vLLM サポート：…", section "EAGLE3 を用いた投機的デコード", every draft
 // position of a request in one decode pass). The positions of one (request,
@@ -857,9 +1324,10 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
 constexpr int kUnWarps = 8;                      // consumer warps: one per query position (q_len <= 8)
 constexpr int kUnStages = 3;                     // 64 KB bf16 K/V tiles
 constexpr int kUnMaxNB = 8192;                   // block bitmaps kept in shared memory up to this many blocks
+constexpr int kUnAhead = 2;                      // union blocks prefetched into L2 beyond the stages
 
 struct UnLayout {
-  uint32_t stages, surv, bits, ubits, prefix, tags, bars, total;
+  uint32_t stages, surv, bits, ubits, prefix, ulist, tags, bars, total;
 };
 
 // nw = 32-bit words per block bitmap (ceil(NB / 32)).
@@ -870,7 +1338,8 @@ __host__ __device__ inline UnLayout un_layout(int nw) {
   s.bits = s.surv + (1 + kUnWarps) * (kWarpSurvCap + 8) * 8;     // [kUnWarps][nw] selected blocks per position
   s.ubits = s.bits + kUnWarps * nw * 4;                          // [nw] their union
   s.prefix = s.ubits + nw * 4;                                   // [nw] union blocks in the words before
-  s.tags = s.prefix + nw * 4;                                    // [kUnStages] union index held by each stage, abort word
+  s.ulist = s.prefix + nw * 4;                                   // [kUnWarps * 16] union blocks in ascending order
+  s.tags = s.ulist + kUnWarps * 16 * 4;                          // [kUnStages] union index held by each stage, abort word
   s.bars = (s.tags + (kUnStages + 2) * 4 + 7) & ~7u;
   s.total = s.bars + 2 * kUnStages * 8;
   return s;
@@ -904,6 +1373,7 @@ __global__ void __launch_bounds__(32 * (1 + kUnWarps), 1)
   uint32_t* bits = reinterpret_cast<uint32_t*>(sm + Ly.bits);
   uint32_t* ubits = reinterpret_cast<uint32_t*>(sm + Ly.ubits);
   int* prefix = reinterpret_cast<int*>(sm + Ly.prefix);
+  int* ulist = reinterpret_cast<int*>(sm + Ly.ulist);
   volatile int* tags = reinterpret_cast<volatile int*>(sm + Ly.tags);
   volatile int* abort_flag = tags + kUnStages;
   volatile int* group_total = tags + kUnStages + 1;
@@ -996,6 +1466,8 @@ __global__ void __launch_bounds__(32 * (1 + kUnWarps), 1)
         if (w < nw) {
           ubits[w] = u;
           prefix[w] = run + incl - cnt;
+          int at = run + incl - cnt;             // the union's blocks in ascending order (at most 8 x 16)
+          for (uint32_t v = u; v != 0u; v &= v - 1u) ulist[at++] = (w << 5) + __ffs(v) - 1;
         }
         run += __shfl_sync(kAll, incl, 31);
       }
@@ -1006,39 +1478,48 @@ __global__ void __launch_bounds__(32 * (1 + kUnWarps), 1)
 
     if (warp == 0) {
       // ------------------------------------------------------------ producer --
-      int n = n_base;
-      for (int w = 0; w < nw && ok; ++w) {
-        uint32_t u = ubits[w];
-        while (u != 0u && ok) {
-          const int bit = __ffs(u) - 1;
-          u &= u - 1u;
-          if (lane == 0) {
-            const int s = n % kUnStages;
-            const uint32_t ph = static_cast<uint32_t>(n / kUnStages) & 1u;
-            if (!mbar_wait(smem_addr(&empty[s]), ph ^ 1u)) {
-              set_flag(p.flags, MSA_FLAG_TIMEOUT);
-              ok = false;
-            } else {
-              int users = 0;
-              for (int q = 0; q < p.Q; ++q) users += (bits[q * nw + w] >> bit) & 1;
-              tags[s] = n;
-              if (users < kUnWarps) mbar_arrive_n(smem_addr(&empty[s]), static_cast<uint32_t>(kUnWarps - users));
-              const int blk = (w << 5) + bit;
-              const int page = p.block_table[static_cast<int64_t>(b) * p.NB + blk];
-              const int y = static_cast<int>((static_cast<int64_t>(page) * p.G + g) * kBlock);
-              const uint32_t fb = smem_addr(&full[s]);
-              const uint32_t dst = base_addr + Ly.stages + s * kTileBytes;
-              mbar_arrive_expect_tx(fb, kTileBytes);
-              tma_load_2d(dst, &tk, 0, y, fb);
-              tma_load_2d(dst + kBoxBytes, &tk, 64, y, fb);
-              tma_load_2d(dst + 2 * kBoxBytes, &tv, 0, y, fb);
-              tma_load_2d(dst + 3 * kBoxBytes, &tv, 64, y, fb);
-            }
-          }
-          ok = __shfl_sync(kAll, ok ? 1 : 0, 0) != 0;
-          if (ok) n_issued = n + 1;
-          ++n;
+      // Union block i goes to stage (n_base + i) % kUnStages. Lane 0 also asks
+      // L2 for the K and V slabs of block i + kUnStages + kUnAhead - 1, so that
+      // when a stage frees its copy finds the data close by.
+      auto l2_prefetch = [&](int i) {
+        if (i < total) {
+          const int page = p.block_table[static_cast<int64_t>(b) * p.NB + ulist[i]];
+          const int64_t off = (static_cast<int64_t>(page) * p.G + g) * (kBlock * kDim * 2);
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.k4 + off), "r"(kBlock * kDim * 2) : "memory");
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.v4 + off), "r"(kBlock * kDim * 2) : "memory");
         }
+      };
+      if (lane == 0)
+        for (int i = kUnStages; i < kUnStages + kUnAhead - 1; ++i) l2_prefetch(i);
+      for (int i = 0; i < total && ok; ++i) {
+        if (lane == 0) {
+          const int n = n_base + i;
+          const int s = n % kUnStages;
+          const uint32_t ph = static_cast<uint32_t>(n / kUnStages) & 1u;
+          if (!mbar_wait(smem_addr(&empty[s]), ph ^ 1u)) {
+            set_flag(p.flags, MSA_FLAG_TIMEOUT);
+            ok = false;
+          } else {
+            const int blk = ulist[i];
+            const int w = blk >> 5, bit = blk & 31;
+            int users = 0;
+            for (int q = 0; q < p.Q; ++q) users += (bits[q * nw + w] >> bit) & 1;
+            tags[s] = n;
+            if (users < kUnWarps) mbar_arrive_n(smem_addr(&empty[s]), static_cast<uint32_t>(kUnWarps - users));
+            const int page = p.block_table[static_cast<int64_t>(b) * p.NB + blk];
+            const int y = static_cast<int>((static_cast<int64_t>(page) * p.G + g) * kBlock);
+            const uint32_t fb = smem_addr(&full[s]);
+            const uint32_t dst = base_addr + Ly.stages + s * kTileBytes;
+            mbar_arrive_expect_tx(fb, kTileBytes);
+            tma_load_2d(dst, &tk, 0, y, fb);
+            tma_load_2d(dst + kBoxBytes, &tk, 64, y, fb);
+            tma_load_2d(dst + 2 * kBoxBytes, &tv, 0, y, fb);
+            tma_load_2d(dst + 3 * kBoxBytes, &tv, 64, y, fb);
+            l2_prefetch(i + kUnStages + kUnAhead - 1);
+          }
+        }
+        ok = __shfl_sync(kAll, ok ? 1 : 0, 0) != 0;
+        if (ok) n_issued = n_base + i + 1;
       }
     } else if (j < p.Q) {
       // ------------------------------------------------- consumer: position j --
@@ -1842,7 +2323,18 @@ cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRec
              a.scores != nullptr ? "select+" : "", C, 32 * kTcWarps, tsmem, kTcStages, static_cast<long long>(p.W));
     return err != cudaSuccess ? err : cudaGetLastError();
   }
-  auto kern = a.nvfp4 ? sparse_gqa_kernel<kKvNvfp4> : a.fp8 ? sparse_gqa_kernel<kKvFp8> : sparse_gqa_kernel<kKvBf16>;
+  if (a.nvfp4) {
+    constexpr size_t fsmem = f4_layout().total + 1024;
+    err = cudaFuncSetAttribute(sparse_gqa_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(fsmem));
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(sparse_gqa_fp4_kernel, dim3(C), dim3(32 * kF4Warps), fsmem, stream, p);
+    rec->set("%ssparse_gqa nvfp4_regk_f16_mma 8warps persistent split_k_fused_combine grid=%d block=%d smem=%zu "
+             "stages=%d items=%lld",
+             a.scores != nullptr ? "select+" : "", C, 32 * kF4Warps, fsmem, kF4Stages, static_cast<long long>(p.W));
+    return err != cudaSuccess ? err : cudaGetLastError();
+  }
+  auto kern = a.fp8 ? sparse_gqa_kernel<kKvFp8> : sparse_gqa_kernel<kKvBf16>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   err = launch_pdl(kern, dim3(C), dim3(32 * (1 + kCWarps)), smem, stream, tk, tv, p);

@@ -276,7 +276,8 @@ size_t msa_sparse_gqa_workspace_size(const msa_dims_t* dims, msa_dtype_t kv_dtyp
  * Stage 3, sparse GQA decode ("MSA 実行プロセス" step 3; split-K decode path
  * of "EAGLE3 を用いた投機的デコード"). For every query head h of position j of
  * request b, with KV head g = h / (H / G), over the tokens t of the blocks in
- * selected[b, j, g, :] (entries < 0 ignored) with t <= p:
+ * selected[b, j, g, :] (entries < 0 ignored; each block id at most once per
+ * row, as msa_select_blocks writes them) with t <= p:
  *   out[b, j, h] = sum_t softmax_t(softmax_scale * q . k_t) * v_t
  *   lse[b, j, h] = log sum_t exp(softmax_scale * q . k_t)
  * The work is split over the selected blocks and the partial results merged
@@ -285,6 +286,12 @@ size_t msa_sparse_gqa_workspace_size(const msa_dims_t* dims, msa_dtype_t kv_dtyp
  * never reach its result: their logits are masked and their V rows are zeroed
  * before the P.V product. So slots that were never written, such as the tail
  * of a request's last page, may hold any bytes, NaN patterns included.
+ * With several query positions and bf16 K/V, the positions of a (request, KV
+ * head) pair are attended together when there are at least three such pairs
+ * for every four SMs: one CTA streams the union of their selected blocks once
+ * and each position attends over its own blocks. MSA_MULTIPOS_ATTENTION=union
+ * or =rows in the environment (read on every call) forces that form or the
+ * per-position one; both give the same results within the same tolerances.
  * For bf16 K/V the environment variable MSA_BF16_ATTENTION=tcgen05, read on
  * every call, selects a tcgen05 form of the tile. It computes S^T = K.Q^T and
  * O^T = V^T.P^T with S and O in tensor memory and gives the same results

@@ -81,7 +81,7 @@ def test_dispatch_record_names_the_variant():
     w4 = synth.scaled(synth.WORKLOADS["nvfp4_256k"], batch=1, ctx=700)
     dw4 = parity.build(w4)
     dw4.step()
-    assert "sparse_gqa nvfp4_dequant_f16_mma" in msa.last_dispatch()
+    assert "sparse_gqa nvfp4_regk_f16_mma 8warps" in msa.last_dispatch()
     w5 = synth.scaled(synth.WORKLOADS["b32_32k_fp4idx"], batch=1, ctx=700)
     dw5 = parity.build(w5)
     dw5.index_score()
