@@ -7,19 +7,21 @@
 // decode_query_len. "vLLM、AMD Instinct MI355X上で…", question 1: 64 query
 // heads share 4 KV heads, so the 16 heads of a KV head form one M=16 tile.
 //
-// Work items are (row, selection slot) pairs, row = (request, KV head,
-// position) with the positions of one (request, KV head) adjacent so that
-// shared pages are still in L2. A persistent grid gives each CTA a contiguous
-// item range; whenever the row changes inside the range the CTA merges its
-// four warps' online-softmax states and writes either the final output (the
-// CTA covered the whole row) or a partial (o, m, l) that the combine kernel
-// merges. A producer thread fetches each selected page: bf16 K/V through
-// 2-D tensor maps with 128-byte swizzle (conflict-free ldmatrix), NVFP4 K/V as
-// four contiguous bulk copies that the consumers expand to fp16 tiles in the
-// same swizzled layout (e2m1 x e4m3 is exact in fp16; the fp32 global scales
-// are applied to the logits and the output). Each of the four consumer warps
-// owns 32 tokens of every block: QK^T and PV run on m16n8k16 tensor-core mma.
-// All waits are bounded; a kernel never traps.
+// Four forms, all persistent, all with bounded waits and no traps:
+//   sparse_gqa_kernel<bf16 | FP8>: work items are (row, selection slot) pairs,
+//     row = (request, KV head, position), positions of one (request, KV head)
+//     adjacent; every CTA owns whole rows. A producer warp fetches each
+//     selected page through 2-D tensor maps with 128-byte swizzle
+//     (conflict-free ldmatrix); each of four consumer warps owns 32 tokens of
+//     every block; QK^T and PV run on m16n8k16 tensor-core mma. At a row's end
+//     the CTA merges its warps' online-softmax states and writes the output.
+//   sparse_gqa_fp4_kernel (NVFP4): eight consumer warps of 16 tokens, item
+//     ranges balanced over the SMs, split rows merged by the CTA that
+//     delivers the last partial.
+//   sparse_gqa_union_kernel (bf16, several query positions): the union of a
+//     (request, KV head) group's blocks streamed once, one warp per position.
+//   sparse_gqa_tc_kernel (bf16, opt-in): the tile on tcgen05 with S and O in
+//     tensor memory.
 #include <cuda.h>
 
 #include <atomic>
@@ -32,15 +34,14 @@
 namespace msa {
 
 // K/V cache formats (template argument of the kernel).
-constexpr int kKvBf16 = 0, kKvNvfp4 = 1, kKvFp8 = 2;
+constexpr int kKvBf16 = 0, kKvFp8 = 2;
 template <int kKv>
-constexpr int stages_for() { return kKv == kKvBf16 ? 3 : 6; }   // 64 KB bf16 / 32 KB FP8 / 18 KB NVFP4 pages
+constexpr int stages_for() { return kKv == kKvBf16 ? 3 : 6; }   // 64 KB bf16 / 32 KB FP8 pages
 constexpr int kTokPerWarp = 32;                  // tokens of every block that one consumer warp owns
 constexpr int kCWarps = kBlock / kTokPerWarp;    // consumer warps (one per SM sub-partition)
 constexpr int kNT = kTokPerWarp / 8;             // QK^T n-tiles of 8 tokens per warp
 constexpr int kKK = kTokPerWarp / 16;            // PV k-steps of 16 tokens per warp
 constexpr int kCombWarps = kCWarps;              // states staged in shared memory at a row's end
-constexpr int kLanesPerRow = 32 / kTokPerWarp;   // NVFP4 expansion: lanes per token row
 static_assert(kCWarps == 4, "the row merge runs on 4 warps x 32 threads");
 constexpr int kBoxBytes = kBlock * 64 * 2;       // 128 rows x 128 B (64 fp16/bf16)
 constexpr int kTileBytes = 4 * kBoxBytes;        // K lo/hi + V lo/hi = 64 KB
@@ -49,7 +50,7 @@ constexpr int kFp8BoxBytes = kBlock * kDim;      // 128 rows x 128 E4M3 codes
 constexpr int kFp8StageBytes = 2 * kFp8BoxBytes; // K + V = 32 KB
 template <int kKv>
 constexpr uint32_t stage_bytes_for() {
-  return kKv == kKvBf16 ? kTileBytes : kKv == kKvFp8 ? kFp8StageBytes : kFp4StageBytes;
+  return kKv == kKvBf16 ? kTileBytes : kFp8StageBytes;
 }
 constexpr uint32_t kAll = 0xffffffffu;
 constexpr float kLn2 = 0.693147180559945309f;
@@ -89,7 +90,7 @@ __host__ __device__ constexpr SmemLayout gqa_layout() {
   SmemLayout s{};
   s.stages = 0;
   s.tiles = s.stages + stages_for<kKv>() * stage_bytes_for<kKv>();
-  s.comb_o = s.tiles + (kKv == kKvNvfp4 ? kTileBytes : 0);
+  s.comb_o = s.tiles;
   s.comb_ml = s.comb_o + kCombWarps * kGroup * kDim * 4;
   s.bars = s.comb_ml + kCombWarps * kGroup * 2 * 4;
   s.total = s.bars + (2 * stages_for<kKv>() + 2) * 8 + 16;   // + the last-arriver flag
@@ -201,7 +202,8 @@ template <int kKv>
 __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     sparse_gqa_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, GqaParams p) {
   extern __shared__ uint8_t smem_raw[];
-  constexpr bool kFp4 = kKv == kKvNvfp4, kFp8 = kKv == kKvFp8;
+  constexpr bool kFp8 = kKv == kKvFp8;
+  static_assert(kKv == kKvBf16 || kKv == kKvFp8, "four-warp form: bf16 or FP8 K/V");
   static_assert(!kFp8 || kNT == 4, "the FP8 fragment loads take 4 n-tiles per ldmatrix.x4");
   constexpr SmemLayout Ly = gqa_layout<kKv>();
   constexpr uint32_t kStageBytes = stage_bytes_for<kKv>();
@@ -227,10 +229,8 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     mbar_init(smem_addr(&gbar[0]), kCWarps);
     mbar_init(smem_addr(&gbar[1]), kCWarps);
     fence_mbar_init();
-    if (!kFp4) {
-      prefetch_tensormap(&tk);
-      prefetch_tensormap(&tv);
-    }
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
   }
   __syncthreads();
   griddep_wait();
@@ -272,7 +272,6 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     // ------------------------------------------------------------ producer --
     // The warp fetches the next 32 items' block, page and validity at once
     // (one chunk ahead); lane 0 issues the copies.
-    const uint64_t pol = l2_evict_first_policy();
     ItemInfo cur = load_item(p, x0 + lane, x1, true);
     int64_t i = 0;
     int s = 0;
@@ -298,18 +297,12 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
               const int y = static_cast<int>(ph * kBlock);
               tma_load_2d(dst, &tk, 0, y, fb);
               tma_load_2d(dst + kFp8BoxBytes, &tv, 0, y, fb);
-            } else if (!kFp4) {
+            } else {
               const int y = static_cast<int>(ph * kBlock);
               tma_load_2d(dst, &tk, 0, y, fb);
               tma_load_2d(dst + kBoxBytes, &tk, 64, y, fb);
               tma_load_2d(dst + 2 * kBoxBytes, &tv, 0, y, fb);
               tma_load_2d(dst + 3 * kBoxBytes, &tv, 64, y, fb);
-            } else {
-              constexpr uint32_t cb = kBlock * kDim / 2, sb = kBlock * kDim / 16;
-              bulk_g2s(dst, p.k4 + ph * cb, cb, fb, pol);
-              bulk_g2s(dst + cb, p.ks + ph * sb, sb, fb, pol);
-              bulk_g2s(dst + cb + sb, p.v4 + ph * cb, cb, fb, pol);
-              bulk_g2s(dst + 2 * cb + sb, p.vs + ph * sb, sb, fb, pol);
             }
           }
         }
@@ -368,7 +361,7 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
         }
       }
     }
-    if (kFp4 || kFp8) {
+    if (kFp8) {
       // fp16 operands: rescale each query row by an exact power of two that
       // keeps it inside the fp16 range; the logit multiplier undoes it.
 #pragma unroll
@@ -465,7 +458,7 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
         float v = 0.f;
 #pragma unroll
         for (int k = 0; k < kCombWarps; ++k) v += fw[k] * comb_o[(k * kGroup + hh) * kDim + d0 + d];
-        acc[d] = v * ((kFp4 || kFp8) ? p.v_global : 1.f);
+        acc[d] = v * (kFp8 ? p.v_global : 1.f);
       }
     }
     const int64_t r = seg_row;
@@ -586,13 +579,11 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
       for (int nt = 0; nt < kNT; ++nt) ldsm_x4(kb + nt * 8 * 128, b[nt][0], b[nt][1], b[nt][2], b[nt][3]);
 #pragma unroll
       for (int nt = 0; nt < kNT; ++nt) {
-        if (kFp4) mma_f16(sc[nt], qf[2 * sp], b[nt][0], b[nt][1]);
-        else mma_bf16(sc[nt], qf[2 * sp], b[nt][0], b[nt][1]);
+        mma_bf16(sc[nt], qf[2 * sp], b[nt][0], b[nt][1]);
       }
 #pragma unroll
       for (int nt = 0; nt < kNT; ++nt) {
-        if (kFp4) mma_f16(sc[nt], qf[2 * sp + 1], b[nt][2], b[nt][3]);
-        else mma_bf16(sc[nt], qf[2 * sp + 1], b[nt][2], b[nt][3]);
+        mma_bf16(sc[nt], qf[2 * sp + 1], b[nt][2], b[nt][3]);
       }
     }
   };
@@ -642,7 +633,12 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
   };
 
   // Second half: probabilities, row sums and O += P V from the V boxes at kt.
-  auto softmax_pv = [&](uint32_t kt, const float (&sc)[kNT][4]) {
+  // V rows of tokens past the causal limit (in the local block) may hold any
+  // bytes, NaN patterns included (cache slots not written yet): their
+  // probabilities are 0, but 0 x NaN is NaN, so their V fragments are cleared
+  // in registers. (Zeroing them in the stage instead, which the next tensor
+  // copy overwrites, raced with that copy.)
+  auto softmax_pv = [&](uint32_t kt, const float (&sc)[kNT][4], int it_blk) {
     float pr[kNT][4];
     // p = 2^(s * mul - m): masked logits (-inf) give 0 since mul > 0; while the
     // reference is still -inf every logit so far is -inf, and 0 stands in for it.
@@ -664,8 +660,15 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     // ---- O += P V (kKK k-steps of 16 tokens, 16 n-tiles of 8 dims)
 #pragma unroll
     for (int kk = 0; kk < kKK; ++kk) {
+      // lane (r, c) holds tokens 16 kk + 2c, + 1 (vm0) and 16 kk + 8 + 2c, + 1 (vm1)
+      uint32_t vm0 = kAll, vm1 = kAll;
+      if (it_blk == seg_ell) {
+        const int tA = it_blk * kBlock + kTokPerWarp * w + 16 * kk + 2 * c;
+        vm0 = (tA <= seg_p ? 0xFFFFu : 0u) | (tA + 1 <= seg_p ? 0xFFFF0000u : 0u);
+        vm1 = (tA + 8 <= seg_p ? 0xFFFFu : 0u) | (tA + 9 <= seg_p ? 0xFFFF0000u : 0u);
+      }
       uint32_t a[4];
-      if (kFp4 || kFp8) {
+      if (kFp8) {
         a[0] = pack_f16x2(pr[2 * kk][0], pr[2 * kk][1]);
         a[1] = pack_f16x2(pr[2 * kk][2], pr[2 * kk][3]);
         a[2] = pack_f16x2(pr[2 * kk + 1][0], pr[2 * kk + 1][1]);
@@ -692,10 +695,10 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
           for (int h = 0; h < 2; ++h) {
             const uint32_t t0 = __byte_perm(v[2 * h], 0, 0x3120), t1 = __byte_perm(v[2 * h + 1], 0, 0x3120);
             const int n = 2 * (2 * qp + h);
-            mma_f16(o[n], a, e4m3x2_to_f16x2(static_cast<uint16_t>(t0 & 0xFFFF)),
-                    e4m3x2_to_f16x2(static_cast<uint16_t>(t1 & 0xFFFF)));
-            mma_f16(o[n + 1], a, e4m3x2_to_f16x2(static_cast<uint16_t>(t0 >> 16)),
-                    e4m3x2_to_f16x2(static_cast<uint16_t>(t1 >> 16)));
+            mma_f16(o[n], a, e4m3x2_to_f16x2(static_cast<uint16_t>(t0 & 0xFFFF)) & vm0,
+                    e4m3x2_to_f16x2(static_cast<uint16_t>(t1 & 0xFFFF)) & vm1);
+            mma_f16(o[n + 1], a, e4m3x2_to_f16x2(static_cast<uint16_t>(t0 >> 16)) & vm0,
+                    e4m3x2_to_f16x2(static_cast<uint16_t>(t1 >> 16)) & vm1);
           }
         }
         continue;
@@ -704,90 +707,10 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
       for (int np = 0; np < 8; ++np) {
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(kt + (2 + (np >> 2)) * kBoxBytes + kk * 16 * 128 + v_off[np & 3], b0, b1, b2, b3);
-        if (kFp4) {
-          mma_f16(o[2 * np], a, b0, b1);
-          mma_f16(o[2 * np + 1], a, b2, b3);
-        } else {
-          mma_bf16(o[2 * np], a, b0, b1);
-          mma_bf16(o[2 * np + 1], a, b2, b3);
-        }
+        mma_bf16(o[2 * np], a, b0 & vm0, b1 & vm1);
+        mma_bf16(o[2 * np + 1], a, b2 & vm0, b3 & vm1);
       }
     }
-  };
-
-  // NVFP4: expands stage s into the warp's rows of the fp16 tile, releases the stage.
-  auto expand = [&](int s) -> uint32_t {
-    // Expand this page's NVFP4 K and V into the fp16 tile. The warp expands
-    // its own token rows (kLanesPerRow lanes per row), which only it reads
-    // afterwards, so a warp-level barrier suffices and the tile can be reused
-    // at once.
-    const uint32_t tile = base_addr + Ly.tiles;
-    const uint8_t* st = sm + Ly.stages + s * kStageBytes;
-    const int t = kTokPerWarp * w + lane / kLanesPerRow;
-    const int sub = lane % kLanesPerRow;
-#pragma unroll
-    for (int kv = 0; kv < 2; ++kv) {
-      const uint8_t* codes = st + kv * (kBlock * kDim / 2 + kBlock * kDim / 16);
-      const uint8_t* scl = codes + kBlock * kDim / 2;
-      const uint32_t dbox = tile + kv * 2 * kBoxBytes;
-#pragma unroll
-      for (int q = 0; q < 4 / kLanesPerRow; ++q) {
-        const int qq = (q * kLanesPerRow + sub + (t >> 1)) & 3;   // rotate 16-byte chunks: fewer bank conflicts
-        const uint4 cw = *reinterpret_cast<const uint4*>(codes + t * 64 + qq * 16);
-        const uint16_t sc2 = *reinterpret_cast<const uint16_t*>(scl + t * 8 + 2 * qq);
-        const uint32_t s2 = e4m3x2_to_f16x2(sc2);
-        const __half2 sa = __half2half2(__ushort_as_half(static_cast<unsigned short>(s2 & 0xFFFF)));
-        const __half2 sb = __half2half2(__ushort_as_half(static_cast<unsigned short>(s2 >> 16)));
-        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {            // 8 codes -> 8 fp16 -> one 16-byte chunk
-          uint32_t h[4];
-          e2m1x4_to_f16x2x2(static_cast<uint16_t>(words[k] & 0xFFFF), h[0], h[1]);
-          e2m1x4_to_f16x2x2(static_cast<uint16_t>(words[k] >> 16), h[2], h[3]);
-          const __half2 scl2 = k < 2 ? sa : sb;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h[e]), scl2);
-            h[e] = *reinterpret_cast<uint32_t*>(&v);
-          }
-          const int chunk = 4 * qq + k;          // dims 8*chunk .. 8*chunk+7
-          const uint32_t a = swz(dbox + (chunk >> 3) * kBoxBytes, t, chunk & 7);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(h[0]), "r"(h[1]), "r"(h[2]),
-                       "r"(h[3])
-                       : "memory");
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
-    return tile;
-  };
-
-  // Zeroes the V rows of this warp's tokens that lie past the causal limit in
-  // the local block. Their probabilities are exactly 0, but a cache slot that
-  // has not been written yet may hold a NaN or infinity bit pattern, and
-  // 0 x NaN would reach the output through the P V product. kt: the tile
-  // (bf16 or expanded NVFP4: V in two 64-dim boxes; FP8: one 128-code box);
-  // async_tile: the tile is a stage that the next bulk copy overwrites.
-  auto clear_masked_v = [&](uint32_t kt, int it_blk, bool async_tile) {
-    if (it_blk != seg_ell) return;               // uniform over the warp
-    const int t = kTokPerWarp * w + lane;        // this lane's token row
-    if (it_blk * kBlock + t > seg_p) {
-      if (kFp8) {
-        const uint32_t row = kt + kFp8BoxBytes + static_cast<uint32_t>(t) * 128u;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) st_shared_zero16(row + 16u * i);
-      } else {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t row = kt + (2 + h) * kBoxBytes + static_cast<uint32_t>(t) * 128u;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) st_shared_zero16(row + 16u * i);
-        }
-      }
-      if (async_tile) fence_proxy_async_smem();
-    }
-    __syncwarp();
   };
 
   // Item cursor: `cur` holds the infos of items base .. base + 31, `nxt` of the
@@ -816,23 +739,13 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
       nxt = load_item(p, base + 32 + lane, x1, false);
     }
     if (!valid) continue;
-    uint32_t kt = base_addr + Ly.stages + s * kStageBytes;   // bf16 tile: K lo, K hi, V lo, V hi
-    if (kFp4) {
-      if (!mbar_wait(smem_addr(&full[s]), phase)) { ok = false; break; }
-      kt = expand(s);
-      qk(kt, sc);
-      softmax_prep(sc, it_blk);
-      clear_masked_v(kt, it_blk, false);
-      softmax_pv(kt, sc);
-    } else {
-      if (!mbar_wait(smem_addr(&full[s]), phase)) { ok = false; break; }
-      qk(kt, sc);
-      softmax_prep(sc, it_blk);
-      clear_masked_v(kt, it_blk, true);
-      softmax_pv(kt, sc);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
-    }
+    const uint32_t kt = base_addr + Ly.stages + s * kStageBytes;   // bf16: K lo, K hi, V lo, V hi; FP8: K, V
+    if (!mbar_wait(smem_addr(&full[s]), phase)) { ok = false; break; }
+    qk(kt, sc);
+    softmax_prep(sc, it_blk);
+    softmax_pv(kt, sc, it_blk);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
     if (++s == kGqaStages) { s = 0; phase ^= 1u; }
   }
   if (ok && seg_row >= 0) ok = end_segment();
@@ -842,20 +755,23 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
 // ---------------------------------------------------------------------------
 // NVFP4 K/V ("MiniMax-M3.1-Flash Day-0 対応", section "何が新しいか": E2M1
 // values with an E4M3 scale per 16 and an fp32 global scale, 576 bytes per
-// token per layer). A block's 18 KB hold too little data to hide the
-// conversion behind the copy, so this form spreads every block over eight
-// consumer warps of 16 tokens (two warps per SM sub-partition, which overlap
-// each other's dependency chains). There is no producer warp: warp 0 also
-// issues the copies, up to kF4Stages blocks ahead of the slowest warp. K codes
-// are converted straight into mma operands: lane (r, c) of an n-tile loads the
-// 16 code bytes 16c .. 16c + 15 of token r (dims 32c .. 32c + 31), so k-step s
-// of the product takes dims 32c + 4s .. + 3 from every lane, and the query
-// fragments are loaded with the same dims. V is expanded (E2M1 x E4M3 is exact
-// in fp16) into the warp's rows of a swizzled fp16 tile, with the rows past
-// the causal limit written as zeros, and read with ldmatrix.trans for P V. The
-// fp32 global scales multiply the logits and the output. Item ranges are
-// balanced over the CTAs and split rows merged through the workspace, as in
-// sparse_gqa_kernel.
+// token per layer). The conversion to fp16 operands, not the copy of a block's
+// 18 KB, sets the pace, so every block is spread over eight consumer warps of
+// 16 tokens (two warps per SM sub-partition, which overlap each other's
+// dependency chains). There is no producer warp: warp 0 also issues the
+// copies, up to the stage count ahead of its own progress, and waits for a
+// free stage only for the block it needs next. K codes are converted straight
+// into mma operands: lane (r, c) of an n-tile loads the 16 code bytes
+// 16c .. 16c + 15 of token r (dims 32c .. 32c + 31), so k-step s of the product
+// takes dims 32c + 4s .. + 3 from every lane, and the query fragments are
+// loaded with the same dims. V is expanded (E2M1 x E4M3 is exact in fp16) into
+// the warp's rows of a swizzled fp16 tile, rows past the causal limit written
+// as zeros, and read with ldmatrix.trans for P V; the stage is released after
+// Q K^T. The fp32 global scales multiply the logits and the output. Item
+// ranges are balanced over the CTAs and split rows merged through the
+// workspace, as in sparse_gqa_kernel. (The same eight-warp form for FP8 K/V
+// measured slower than four warps on whole rows, 32.3 against 24.8 us on
+// 32 x 32K: that conversion is bound by the ALU pipe, not by latency.)
 
 constexpr int kF4Warps = 8;
 constexpr int kF4Tok = kBlock / kF4Warps;          // 16 tokens per warp and block
@@ -879,6 +795,7 @@ __host__ __device__ constexpr F4Layout f4_layout() {
 
 __global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaParams p) {
   extern __shared__ uint8_t smem_raw[];
+  constexpr uint32_t kStageBytes = kFp4StageBytes;
   constexpr F4Layout Ly = f4_layout();
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base_addr = (raw + 1023u) & ~1023u;
@@ -962,9 +879,9 @@ __global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaPar
         else go = mbar_try_wait(smem_addr(&empty[s]), par) ? 1 : 0;
         if (go == 1) {
           const uint32_t fb = smem_addr(&full[s]);
-          const uint32_t dst = base_addr + Ly.stages + s * kFp4StageBytes;
+          const uint32_t dst = base_addr + Ly.stages + s * kStageBytes;
           const int64_t ph = static_cast<int64_t>(page) * p.G + g;
-          mbar_arrive_expect_tx(fb, kFp4StageBytes);
+          mbar_arrive_expect_tx(fb, kStageBytes);
           bulk_g2s(dst, p.k4 + ph * kF4Codes, kF4Codes, fb, pol);
           bulk_g2s(dst + kF4Codes, p.ks + ph * kF4Scales, kF4Scales, fb, pol);
           bulk_g2s(dst + kF4Codes + kF4Scales, p.v4 + ph * kF4Codes, kF4Codes, fb, pol);
@@ -978,6 +895,8 @@ __global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaPar
       ++is;
     }
   };
+
+  if (w == 0) issue_upto(0);        // the first copies, before the first row's query loads
 
   uint32_t qf[8][4];
   float o[16][4];
@@ -1112,7 +1031,7 @@ __global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaPar
       }
     }
     if (!group_sync(smem_addr(&gbar[1]), gph[1], lane)) return false;
-    if (tid == 0) {
+    if (tid == 32) {              // not warp 0's lane 0, whose bulk copies may still be in flight
       fence_acq_rel_gpu();
       const bool last = ticket_is_last(p, r, nslots);
       if (last) fence_acq_rel_gpu();
@@ -1167,7 +1086,7 @@ __global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaPar
     }
     if (w == 0) issue_upto(cs + 1);                 // this item's copy, and more while stages are free
     if (!mbar_wait(smem_addr(&full[s]), phase)) { ok = false; break; }
-    const uint8_t* st = sm + Ly.stages + s * kFp4StageBytes;
+    const uint8_t* st = sm + Ly.stages + s * kStageBytes;
     const int tb = it_blk * kBlock + kF4Tok * w;   // first token of this warp's rows
     // ---- V rows of this warp -> fp16 tile (rows past the causal limit as zeros)
     {
@@ -1617,19 +1536,6 @@ __global__ void __launch_bounds__(32 * (1 + kUnWarps), 1)
                 }
               }
             }
-            // V rows past the last cached token may hold any bytes (never
-            // written); every position masks them, and each warp that reads
-            // this block zeroes them first (all writers store zeros)
-            if (blk == last_blk && tbase + lane > L - 1) {
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const uint32_t row = ks + (2 + h) * kBoxBytes + static_cast<uint32_t>(lane) * 128u;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) st_shared_zero16(row + 16u * i);
-              }
-              fence_proxy_async_smem();
-            }
-            __syncwarp();
             float pr[kNT][4];
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
@@ -1648,6 +1554,15 @@ __global__ void __launch_bounds__(32 * (1 + kUnWarps), 1)
             }
 #pragma unroll
             for (int kk = 0; kk < kKK; ++kk) {
+              // V rows past the last cached token may hold any bytes (never
+              // written): every position gives them probability 0, and their
+              // fragments are cleared in registers (0 x NaN is NaN)
+              uint32_t vm0 = kAll, vm1 = kAll;
+              if (blk == last_blk) {
+                const int tA = tbase + 16 * kk + 2 * c;
+                vm0 = (tA <= L - 1 ? 0xFFFFu : 0u) | (tA + 1 <= L - 1 ? 0xFFFF0000u : 0u);
+                vm1 = (tA + 8 <= L - 1 ? 0xFFFFu : 0u) | (tA + 9 <= L - 1 ? 0xFFFF0000u : 0u);
+              }
               uint32_t a[4];
               a[0] = pack_bf16x2(pr[2 * kk][0], pr[2 * kk][1]);
               a[1] = pack_bf16x2(pr[2 * kk][2], pr[2 * kk][3]);
@@ -1657,8 +1572,8 @@ __global__ void __launch_bounds__(32 * (1 + kUnWarps), 1)
               for (int np = 0; np < 8; ++np) {
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4_t(ks + (2 + (np >> 2)) * kBoxBytes + kk * 16 * 128 + v_off[np & 3], b0, b1, b2, b3);
-                mma_bf16(o[2 * np], a, b0, b1);
-                mma_bf16(o[2 * np + 1], a, b2, b3);
+                mma_bf16(o[2 * np], a, b0 & vm0, b1 & vm1);
+                mma_bf16(o[2 * np + 1], a, b2 & vm0, b3 & vm1);
               }
             }
           }
@@ -2292,8 +2207,7 @@ cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRec
     p.row_aligned = 0;
     C = static_cast<int>(p.W < sms ? p.W : sms);
   }
-  const size_t smem = (a.nvfp4 ? gqa_layout<kKvNvfp4>().total
-                               : a.fp8 ? gqa_layout<kKvFp8>().total : gqa_layout<kKvBf16>().total) + 1024;
+  const size_t smem = (a.fp8 ? gqa_layout<kKvFp8>().total : gqa_layout<kKvBf16>().total) + 1024;
   static std::atomic<uint32_t> epoch{1};
   p.epoch = epoch.fetch_add(1);
   if (p.epoch == 0) p.epoch = epoch.fetch_add(1);    // 0 never tags a ticket
@@ -2324,14 +2238,16 @@ cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRec
     return err != cudaSuccess ? err : cudaGetLastError();
   }
   if (a.nvfp4) {
-    constexpr size_t fsmem = f4_layout().total + 1024;
+    // NVFP4 K/V: eight consumer warps, balanced item ranges
+    constexpr size_t wsmem = f4_layout().total + 1024;
     err = cudaFuncSetAttribute(sparse_gqa_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(fsmem));
+                               static_cast<int>(wsmem));
     if (err != cudaSuccess) return err;
-    err = launch_pdl(sparse_gqa_fp4_kernel, dim3(C), dim3(32 * kF4Warps), fsmem, stream, p);
+    err = launch_pdl(sparse_gqa_fp4_kernel, dim3(C), dim3(32 * kF4Warps), wsmem, stream, p);
     rec->set("%ssparse_gqa nvfp4_regk_f16_mma 8warps persistent split_k_fused_combine grid=%d block=%d smem=%zu "
              "stages=%d items=%lld",
-             a.scores != nullptr ? "select+" : "", C, 32 * kF4Warps, fsmem, kF4Stages, static_cast<long long>(p.W));
+             a.scores != nullptr ? "select+" : "", C, 32 * kF4Warps, wsmem, kF4Stages,
+             static_cast<long long>(p.W));
     return err != cudaSuccess ? err : cudaGetLastError();
   }
   auto kern = a.fp8 ? sparse_gqa_kernel<kKvFp8> : sparse_gqa_kernel<kKvBf16>;
@@ -2340,9 +2256,9 @@ cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRec
   err = launch_pdl(kern, dim3(C), dim3(32 * (1 + kCWarps)), smem, stream, tk, tv, p);
   rec->set("%ssparse_gqa %s persistent %s grid=%d block=%d smem=%zu stages=%d items=%lld",
            a.scores != nullptr ? "select+" : "",
-           a.nvfp4 ? "nvfp4_dequant_f16_mma" : a.fp8 ? "fp8_tma_cvt_f16_mma" : "bf16_tma_mma",
+           a.fp8 ? "fp8_tma_cvt_f16_mma" : "bf16_tma_mma",
            p.row_aligned ? "whole_rows" : "split_k_fused_combine", C, 32 * (1 + kCWarps), smem,
-           a.nvfp4 ? stages_for<kKvNvfp4>() : a.fp8 ? stages_for<kKvFp8>() : stages_for<kKvBf16>(),
+           a.fp8 ? stages_for<kKvFp8>() : stages_for<kKvBf16>(),
            static_cast<long long>(p.W));
   return err != cudaSuccess ? err : cudaGetLastError();
 }
