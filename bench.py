@@ -124,12 +124,20 @@ class ClockSampler:
         self.gpu = gpu_index
 
     def start(self):
+        """Starts sampling and returns once the first sample has arrived, so that
+        the sampler's start-up does not overlap the timed region."""
+        self.first = ""
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
+            return
+        import select
+        ready, _, _ = select.select([self.proc.stdout], [], [], 5.0)
+        if ready:
+            self.first = self.proc.stdout.readline()
 
     def stop(self):
         if self.proc is None:
@@ -140,6 +148,7 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
+        out = self.first + out
         rows = []
         for line in out.strip().splitlines():
             parts = [x.strip() for x in line.split(",")]

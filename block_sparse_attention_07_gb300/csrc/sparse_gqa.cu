@@ -81,7 +81,7 @@ struct GqaParams {
 };
 
 struct SmemLayout {
-  uint32_t stages, tiles, comb_o, comb_ml, bars;
+  uint32_t stages, tiles, comb_o, comb_ml, bars, zero;
   uint32_t total;
 };
 
@@ -93,7 +93,8 @@ __host__ __device__ constexpr SmemLayout gqa_layout() {
   s.comb_o = s.tiles;
   s.comb_ml = s.comb_o + kCombWarps * kGroup * kDim * 4;
   s.bars = s.comb_ml + kCombWarps * kGroup * 2 * 4;
-  s.total = s.bars + (2 * stages_for<kKv>() + 2) * 8 + 16;   // + the last-arriver flag
+  s.zero = s.bars + (2 * stages_for<kKv>() + 2) * 8 + 16;    // after the last-arriver flag
+  s.total = s.zero + 16;                                       // 16 zero bytes: the V row of a masked token
   return s;
 }
 
@@ -231,6 +232,7 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
     fence_mbar_init();
     prefetch_tensormap(&tk);
     prefetch_tensormap(&tv);
+    st_shared_zero16(base_addr + Ly.zero);
   }
   __syncthreads();
   griddep_wait();
@@ -635,9 +637,9 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
   // Second half: probabilities, row sums and O += P V from the V boxes at kt.
   // V rows of tokens past the causal limit (in the local block) may hold any
   // bytes, NaN patterns included (cache slots not written yet): their
-  // probabilities are 0, but 0 x NaN is NaN, so their V fragments are cleared
-  // in registers. (Zeroing them in the stage instead, which the next tensor
-  // copy overwrites, raced with that copy.)
+  // probabilities are 0, but 0 x NaN is NaN, so the ldmatrix lanes of those
+  // rows read a 16-byte zero row instead. (Zeroing them in the stage, which
+  // the next tensor copy overwrites, raced with that copy.)
   auto softmax_pv = [&](uint32_t kt, const float (&sc)[kNT][4], int it_blk) {
     float pr[kNT][4];
     // p = 2^(s * mul - m): masked logits (-inf) give 0 since mul > 0; while the
@@ -658,15 +660,14 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
       l_r[r] += ls;
     }
     // ---- O += P V (kKK k-steps of 16 tokens, 16 n-tiles of 8 dims)
+    const bool local = it_blk == seg_ell;
 #pragma unroll
     for (int kk = 0; kk < kKK; ++kk) {
-      // lane (r, c) holds tokens 16 kk + 2c, + 1 (vm0) and 16 kk + 8 + 2c, + 1 (vm1)
-      uint32_t vm0 = kAll, vm1 = kAll;
-      if (it_blk == seg_ell) {
-        const int tA = it_blk * kBlock + kTokPerWarp * w + 16 * kk + 2 * c;
-        vm0 = (tA <= seg_p ? 0xFFFFu : 0u) | (tA + 1 <= seg_p ? 0xFFFF0000u : 0u);
-        vm1 = (tA + 8 <= seg_p ? 0xFFFFu : 0u) | (tA + 9 <= seg_p ? 0xFFFF0000u : 0u);
-      }
+      // the V row this lane addresses in each ldmatrix.x4.trans: token
+      // 16 kk + 8 ((lane >> 3) & 1) + (lane & 7) of the warp's slice; past the
+      // causal limit the lane points at a 16-byte zero row instead
+      const bool zrow = local && it_blk * kBlock + kTokPerWarp * w + 16 * kk + 8 * ((lane >> 3) & 1) + (lane & 7) > seg_p;
+      const uint32_t zaddr = base_addr + Ly.zero;
       uint32_t a[4];
       if (kFp8) {
         a[0] = pack_f16x2(pr[2 * kk][0], pr[2 * kk][1]);
@@ -690,15 +691,16 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
 #pragma unroll
         for (int qp = 0; qp < 4; ++qp) {
           uint32_t v[4];
-          ldsm_x4_t(vt + (((static_cast<uint32_t>(2 * qp) + (lane >> 4)) << 4) ^ lane_x), v[0], v[1], v[2], v[3]);
+          const uint32_t va = vt + (((static_cast<uint32_t>(2 * qp) + (lane >> 4)) << 4) ^ lane_x);
+          ldsm_x4_t(zrow ? zaddr : va, v[0], v[1], v[2], v[3]);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const uint32_t t0 = __byte_perm(v[2 * h], 0, 0x3120), t1 = __byte_perm(v[2 * h + 1], 0, 0x3120);
             const int n = 2 * (2 * qp + h);
-            mma_f16(o[n], a, e4m3x2_to_f16x2(static_cast<uint16_t>(t0 & 0xFFFF)) & vm0,
-                    e4m3x2_to_f16x2(static_cast<uint16_t>(t1 & 0xFFFF)) & vm1);
-            mma_f16(o[n + 1], a, e4m3x2_to_f16x2(static_cast<uint16_t>(t0 >> 16)) & vm0,
-                    e4m3x2_to_f16x2(static_cast<uint16_t>(t1 >> 16)) & vm1);
+            mma_f16(o[n], a, e4m3x2_to_f16x2(static_cast<uint16_t>(t0 & 0xFFFF)),
+                    e4m3x2_to_f16x2(static_cast<uint16_t>(t1 & 0xFFFF)));
+            mma_f16(o[n + 1], a, e4m3x2_to_f16x2(static_cast<uint16_t>(t0 >> 16)),
+                    e4m3x2_to_f16x2(static_cast<uint16_t>(t1 >> 16)));
           }
         }
         continue;
@@ -706,9 +708,10 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
 #pragma unroll
       for (int np = 0; np < 8; ++np) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(kt + (2 + (np >> 2)) * kBoxBytes + kk * 16 * 128 + v_off[np & 3], b0, b1, b2, b3);
-        mma_bf16(o[2 * np], a, b0 & vm0, b1 & vm1);
-        mma_bf16(o[2 * np + 1], a, b2 & vm0, b3 & vm1);
+        const uint32_t va = kt + (2 + (np >> 2)) * kBoxBytes + kk * 16 * 128 + v_off[np & 3];
+        ldsm_x4_t(zrow ? zaddr : va, b0, b1, b2, b3);
+        mma_bf16(o[2 * np], a, b0, b1);
+        mma_bf16(o[2 * np + 1], a, b2, b3);
       }
     }
   };
@@ -1246,7 +1249,7 @@ constexpr int kUnMaxNB = 8192;                   // block bitmaps kept in shared
 constexpr int kUnAhead = 2;                      // union blocks prefetched into L2 beyond the stages
 
 struct UnLayout {
-  uint32_t stages, surv, bits, ubits, prefix, ulist, tags, bars, total;
+  uint32_t stages, surv, bits, ubits, prefix, ulist, tags, bars, zero, total;
 };
 
 // nw = 32-bit words per block bitmap (ceil(NB / 32)).
@@ -1260,7 +1263,8 @@ __host__ __device__ inline UnLayout un_layout(int nw) {
   s.ulist = s.prefix + nw * 4;                                   // [kUnWarps * 16] union blocks in ascending order
   s.tags = s.ulist + kUnWarps * 16 * 4;                          // [kUnStages] union index held by each stage, abort word
   s.bars = (s.tags + (kUnStages + 2) * 4 + 7) & ~7u;
-  s.total = s.bars + 2 * kUnStages * 8;
+  s.zero = (s.bars + 2 * kUnStages * 8 + 15) & ~15u;            // 16 zero bytes: the V row of a token past L - 1
+  s.total = s.zero + 16;
   return s;
 }
 
@@ -1308,6 +1312,7 @@ __global__ void __launch_bounds__(32 * (1 + kUnWarps), 1)
       tags[s] = -1;
     }
     *abort_flag = 0;
+    st_shared_zero16(base_addr + Ly.zero);
     fence_mbar_init();
     prefetch_tensormap(&tk);
     prefetch_tensormap(&tv);
@@ -1552,17 +1557,13 @@ __global__ void __launch_bounds__(32 * (1 + kUnWarps), 1)
               }
               l_r[r] += ls;
             }
+            // V rows past the last cached token may hold any bytes (never
+            // written): every position gives them probability 0, and the
+            // ldmatrix lanes of those rows read a 16-byte zero row instead
+            // (0 x NaN is NaN)
 #pragma unroll
             for (int kk = 0; kk < kKK; ++kk) {
-              // V rows past the last cached token may hold any bytes (never
-              // written): every position gives them probability 0, and their
-              // fragments are cleared in registers (0 x NaN is NaN)
-              uint32_t vm0 = kAll, vm1 = kAll;
-              if (blk == last_blk) {
-                const int tA = tbase + 16 * kk + 2 * c;
-                vm0 = (tA <= L - 1 ? 0xFFFFu : 0u) | (tA + 1 <= L - 1 ? 0xFFFF0000u : 0u);
-                vm1 = (tA + 8 <= L - 1 ? 0xFFFFu : 0u) | (tA + 9 <= L - 1 ? 0xFFFF0000u : 0u);
-              }
+              const bool zrow = blk == last_blk && tbase + 16 * kk + 8 * ((lane >> 3) & 1) + (lane & 7) > L - 1;
               uint32_t a[4];
               a[0] = pack_bf16x2(pr[2 * kk][0], pr[2 * kk][1]);
               a[1] = pack_bf16x2(pr[2 * kk][2], pr[2 * kk][3]);
@@ -1571,9 +1572,10 @@ __global__ void __launch_bounds__(32 * (1 + kUnWarps), 1)
 #pragma unroll
               for (int np = 0; np < 8; ++np) {
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(ks + (2 + (np >> 2)) * kBoxBytes + kk * 16 * 128 + v_off[np & 3], b0, b1, b2, b3);
-                mma_bf16(o[2 * np], a, b0 & vm0, b1 & vm1);
-                mma_bf16(o[2 * np + 1], a, b2 & vm0, b3 & vm1);
+                const uint32_t va = ks + (2 + (np >> 2)) * kBoxBytes + kk * 16 * 128 + v_off[np & 3];
+                ldsm_x4_t(zrow ? base_addr + Ly.zero : va, b0, b1, b2, b3);
+                mma_bf16(o[2 * np], a, b0, b1);
+                mma_bf16(o[2 * np + 1], a, b2, b3);
               }
             }
           }
@@ -2093,6 +2095,456 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// The union form on the fifth-generation tensor cores. With several query
+// positions per request the 16 heads of the 8 positions of a (request, KV
+// head) group make an M = 128 tile, tcgen05's native shape: S = Q K^T
+// (M = 128 query rows, N = 128 tokens, K = 128 dims) and O += P V (N = 128
+// dims, K = 128 tokens), one pair of MMAs per union block for every position
+// at once. Q and P are the A operands, held in tensor memory (bf16 pairs per
+// 32-bit column); K and V are the B operands, read from the TMA-loaded
+// 128-byte-swizzled stage (K K-major, V MN-major); S (two buffers, P written
+// over the buffer's first 64 columns) and O accumulate in tensor memory.
+// Roles: a producer warp (copies, L2 prefetch), an MMA warp (one thread issues,
+// commits release the stage and the S/P buffer), and four softmax warps whose
+// thread r owns query row r (position r / 16, head r % 16): its 128 logits of
+// a block sit in its registers, so the online softmax needs no exchange. A
+// position that did not select a block gets P = 0 for it. The output
+// accumulator is rescaled in tensor memory only when a row's maximum rises by
+// more than 2^8. V rows past the last cached token are zeroed in the stage
+// before P V (their probability is 0, but they may hold NaN patterns). One
+// CTA per group; every wait is bounded.
+
+constexpr int kTuWarps = 6;                      // producer, MMA warp, 4 softmax warps
+constexpr int kTuMmaWarp = 1;
+constexpr int kTuStages = 3;
+constexpr uint32_t kTuCols = 512;                // TMEM: Q (64) | S0 (128) | S1 (128) | O (128)
+constexpr uint32_t kTuQ = 0, kTuS = 64, kTuO = 320;
+
+struct TuLayout {
+  uint32_t stages, surv, bits, ubits, prefix, ulist, umask, misc, bars, total;
+};
+__host__ __device__ inline TuLayout tu_layout(int nw) {
+  TuLayout s{};
+  s.stages = 0;
+  s.surv = kTuStages * kTileBytes;                                // fused selection: each warp's survivors
+  s.bits = s.surv + kTuWarps * (kWarpSurvCap + 8) * 8;            // [8][nw] selected blocks per position
+  s.ubits = s.bits + kUnWarps * nw * 4;                           // [nw] union
+  s.prefix = s.ubits + nw * 4;                                    // [nw] union blocks in the words before
+  s.ulist = s.prefix + nw * 4;                                    // [128] union blocks, ascending
+  s.umask = s.ulist + kUnWarps * 16 * 4;                          // [128] positions that selected each
+  s.misc = s.umask + kUnWarps * 16;                               // group total, abort, TMEM base
+  s.bars = (s.misc + 16 + 7) & ~7u;                               // 16 mbarriers
+  s.total = s.bars + 16 * 8;
+  return s;
+}
+
+__device__ __forceinline__ void tc_mma_ta(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+               ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc ? 1 : 0) : "memory");
+}
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+               "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                 "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+                 "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+                 "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+               "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+               ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+                 "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+                 "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+                 "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+               : "memory");
+}
+
+__global__ void __launch_bounds__(32 * kTuWarps, 1)
+    sparse_gqa_union_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                               GqaParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base_addr = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base_addr - raw);
+  const int nw = (p.NB + 31) >> 5;
+  const TuLayout Ly = tu_layout(nw);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(sm + Ly.bits);
+  uint32_t* ubits = reinterpret_cast<uint32_t*>(sm + Ly.ubits);
+  int* prefix = reinterpret_cast<int*>(sm + Ly.prefix);
+  int* ulist = reinterpret_cast<int*>(sm + Ly.ulist);
+  uint8_t* umask = sm + Ly.umask;
+  volatile int* group_total = reinterpret_cast<volatile int*>(sm + Ly.misc);
+  volatile int* abort_flag = group_total + 1;
+  const uint32_t tslot = base_addr + Ly.misc + 8;
+  const uint32_t bars = base_addr + Ly.bars;
+  // mbarriers: full[3], empty[3], s_full[2], p_full[2], sbuf_free[2], q_full, o_full, o_free, done
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (3 + s); };
+  auto s_full = [&](int b) { return bars + 8u * (6 + b); };
+  auto p_full = [&](int b) { return bars + 8u * (8 + b); };
+  auto sbuf_free = [&](int b) { return bars + 8u * (10 + b); };
+  const uint32_t q_full = bars + 8u * 12, o_full = bars + 8u * 13, o_free = bars + 8u * 14, done_bar = bars + 8u * 15;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  griddep_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTuStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);                   // a commit after the block's P V
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(p_full(b), 4);                  // the softmax warps
+      mbar_init(sbuf_free(b), 1);               // a commit after the P V that read the buffer
+    }
+    mbar_init(q_full, 4);
+    mbar_init(o_full, 1);
+    mbar_init(o_free, 4);
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
+  }
+  if (warp == kTuMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tslot), "r"(kTuCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + Ly.misc + 8);
+  griddep_wait();
+
+  const int groups = p.B * p.G;
+  int n_base = 0;         // union index of the group's first block, counted over the CTA's groups
+  int gq = 0;             // groups with at least one block this CTA has done (they use the Q / O barriers)
+  int n_issued = 0;       // producer: copies issued
+  bool ok = true;
+
+  for (int grp = blockIdx.x; grp < groups; grp += gridDim.x) {
+    const int b = grp / p.G, g = grp - b * p.G;
+    const int L = p.seq_lens[b];
+    const bool len_ok = L >= p.Q && L >= 1 && L <= p.NB * kBlock;
+    // 1. (fused) selection of the group's rows; bitmaps cleared
+    for (int i = threadIdx.x; i < kUnWarps * nw; i += blockDim.x) bits[i] = 0u;
+    if (p.scores != nullptr) {
+      uint64_t* surv = reinterpret_cast<uint64_t*>(sm + Ly.surv) + warp * (kWarpSurvCap + 8);
+      for (int j = warp; j < p.Q; j += kTuWarps) {
+        const int64_t row_off = (static_cast<int64_t>(b) * p.Q + j) * p.G + g;
+        int32_t* out = p.sel_out + row_off * p.K;
+        if (!len_ok) {
+          for (int e = lane; e < p.K; e += 32) out[e] = -1;
+        } else {
+          warp_select_row(p.scores + row_off * p.NB, (L - p.Q + j) / kBlock, p.K, out, surv,
+                          reinterpret_cast<int*>(surv + kWarpSurvCap), lane);
+        }
+      }
+    }
+    __syncthreads();
+    // 2. each position's valid selected blocks into its bitmap
+    for (int j = warp; j < p.Q; j += kTuWarps) {
+      if (!len_ok) {
+        if (j == 0 && lane == 0) set_flag(p.flags, MSA_FLAG_BAD_SEQLEN);
+        continue;
+      }
+      const int ell = (L - p.Q + j) / kBlock;
+      const int32_t* sel = p.selected + ((static_cast<int64_t>(b) * p.Q + j) * p.G + g) * p.K;
+      for (int e = lane; e < p.K; e += 32) {
+        const int blk = sel[e];
+        if (blk < 0) continue;
+        if (blk > ell) { set_flag(p.flags, MSA_FLAG_BAD_BLOCK); continue; }
+        const int page = p.block_table[static_cast<int64_t>(b) * p.NB + blk];
+        if (page < 0 || page >= p.P) { set_flag(p.flags, MSA_FLAG_BAD_PAGE); continue; }
+        atomicOr(&bits[j * nw + (blk >> 5)], 1u << (blk & 31));
+      }
+    }
+    __syncthreads();
+    // 3. union, its running count per word, the ascending list and each block's positions
+    if (warp == 0) {
+      int run = 0;
+      for (int w0 = 0; w0 < nw; w0 += 32) {
+        const int w = w0 + lane;
+        uint32_t u = 0u;
+        if (w < nw)
+          for (int q = 0; q < p.Q; ++q) u |= bits[q * nw + w];
+        const int cnt = __popc(u);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(kAll, incl, o);
+          if (lane >= o) incl += t;
+        }
+        if (w < nw) {
+          ubits[w] = u;
+          prefix[w] = run + incl - cnt;
+          int at = run + incl - cnt;
+          for (uint32_t v = u; v != 0u; v &= v - 1u) {
+            const int bit = __ffs(v) - 1;
+            uint32_t m = 0u;
+            for (int q = 0; q < p.Q; ++q) m |= ((bits[q * nw + w] >> bit) & 1u) << q;
+            umask[at] = static_cast<uint8_t>(m);
+            ulist[at++] = (w << 5) + bit;
+          }
+        }
+        run += __shfl_sync(kAll, incl, 31);
+      }
+      if (lane == 0) *group_total = run;
+    }
+    __syncthreads();
+    const int total = *group_total;
+    const int last_blk = (L - 1) / kBlock;
+
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer --
+      auto l2_prefetch = [&](int i) {
+        if (i < total) {
+          const int page = p.block_table[static_cast<int64_t>(b) * p.NB + ulist[i]];
+          const int64_t off = (static_cast<int64_t>(page) * p.G + g) * (kBlock * kDim * 2);
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.k4 + off), "r"(kBlock * kDim * 2) : "memory");
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.v4 + off), "r"(kBlock * kDim * 2) : "memory");
+        }
+      };
+      if (lane == 0)
+        for (int i = kTuStages; i < kTuStages + kUnAhead - 1; ++i) l2_prefetch(i);
+      for (int i = 0; i < total && ok; ++i) {
+        if (lane == 0) {
+          const int n = n_base + i;
+          const int s = n % kTuStages;
+          if (!mbar_wait(empty(s), (static_cast<uint32_t>(n / kTuStages) & 1u) ^ 1u)) {
+            set_flag(p.flags, MSA_FLAG_TIMEOUT);
+            ok = false;
+          } else {
+            const int page = p.block_table[static_cast<int64_t>(b) * p.NB + ulist[i]];
+            const int y = static_cast<int>((static_cast<int64_t>(page) * p.G + g) * kBlock);
+            const uint32_t dst = base_addr + Ly.stages + s * kTileBytes;
+            mbar_arrive_expect_tx(full(s), kTileBytes);
+            tma_load_2d(dst, &tk, 0, y, full(s));
+            tma_load_2d(dst + kBoxBytes, &tk, 64, y, full(s));
+            tma_load_2d(dst + 2 * kBoxBytes, &tv, 0, y, full(s));
+            tma_load_2d(dst + 3 * kBoxBytes, &tv, 64, y, full(s));
+            l2_prefetch(i + kTuStages + kUnAhead - 1);
+            n_issued = n + 1;
+          }
+        }
+        ok = __shfl_sync(kAll, ok ? 1 : 0, 0) != 0;
+      }
+      n_issued = __shfl_sync(kAll, n_issued, 0);
+    } else if (warp == kTuMmaWarp) {
+      // ----------------------------------------------------------- MMA warp --
+      constexpr uint32_t id_s = tc_idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t id_o = tc_idesc_bf16(128, 128, 0, 1);
+      const bool leader = lane == 0;
+      auto issue_pv = [&](int i) -> bool {      // O += P V of union block i
+        const int n = n_base + i, bb = n & 1, s = n % kTuStages;
+        if (!mbar_wait(p_full(bb), static_cast<uint32_t>(n >> 1) & 1u)) return false;
+        if (i == 0 && gq > 0 && !mbar_wait(o_free, static_cast<uint32_t>(gq - 1) & 1u)) return false;
+        tc_fence_after();
+        if (leader) {
+          const uint32_t vt = base_addr + Ly.stages + static_cast<uint32_t>(s) * kTileBytes + 2 * kBoxBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tc_mma_ta(tmem + kTuO, tmem + kTuS + 128u * bb + 8u * kk, tc_desc(vt + kk * 2048u, kBoxBytes, 1024), id_o,
+                      !(i == 0 && kk == 0));
+          tc_commit(empty(s));
+          tc_commit(sbuf_free(bb));
+          if (i == total - 1) tc_commit(o_full);
+        }
+        __syncwarp();
+        return true;
+      };
+      if (total > 0 && !mbar_wait(q_full, static_cast<uint32_t>(gq) & 1u)) ok = false;
+      for (int i = 0; i < total && ok; ++i) {
+        const int n = n_base + i, bb = n & 1, s = n % kTuStages;
+        if (!mbar_wait(full(s), static_cast<uint32_t>(n / kTuStages) & 1u)) { ok = false; break; }
+        if (n >= 2 && !mbar_wait(sbuf_free(bb), static_cast<uint32_t>((n - 2) >> 1) & 1u)) { ok = false; break; }
+        tc_fence_after();
+        if (leader) {
+          const uint32_t kt = base_addr + Ly.stages + static_cast<uint32_t>(s) * kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tc_mma_ta(tmem + kTuS + 128u * bb, tmem + kTuQ + 8u * kk,
+                      tc_desc(kt + (kk >> 2) * kBoxBytes + (kk & 3) * 32u, 16, 1024), id_s, kk > 0);
+          tc_commit(s_full(bb));
+        }
+        __syncwarp();
+        if (i > 0 && !issue_pv(i - 1)) { ok = false; break; }
+      }
+      if (ok && total > 0 && !issue_pv(total - 1)) ok = false;
+    } else {
+      // ------------------------------------------------------- softmax warps --
+      const int r = 32 * (warp & 3) + lane;    // query row = TMEM lane
+      const int j = r >> 4, h = r & 15;
+      const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+      const bool row_live = len_ok && j < p.Q;
+      const int pj = L - p.Q + j;
+      const int ell = pj / kBlock;
+      const float mul = p.scale_log2;
+      const uint32_t wmask = 3u << (2 * (warp & 3));   // the two positions of this warp's rows
+      float m_ref = -INFINITY, l_sum = 0.f;
+      const int64_t head = (static_cast<int64_t>(b) * p.Q + (j < p.Q ? j : 0)) * p.H + static_cast<int64_t>(g) * kGroup + h;
+      if (total > 0) {
+        // the group's queries into tensor memory: row r = (position j, head h), bf16 pairs per column
+        const uint4* qr = reinterpret_cast<const uint4*>(p.q + head * kDim);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t qv[32];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint4 v = row_live ? qr[half * 8 + k] : make_uint4(0u, 0u, 0u, 0u);
+            qv[4 * k] = v.x; qv[4 * k + 1] = v.y; qv[4 * k + 2] = v.z; qv[4 * k + 3] = v.w;
+          }
+          tc_st32(tmem + lane_base + kTuQ + 32u * half, qv);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_full);
+      }
+      for (int i = 0; i < total && ok; ++i) {
+        const int n = n_base + i, bb = n & 1, s = n % kTuStages;
+        const int blk = ulist[i];
+        const uint32_t um = umask[i];
+        const uint32_t sbuf = tmem + lane_base + kTuS + 128u * bb;
+        if (!mbar_wait(s_full(bb), static_cast<uint32_t>(n >> 1) & 1u)) { ok = false; break; }
+        tc_fence_after();
+        if (um & wmask) {
+          const bool mine = ((um >> j) & 1u) != 0 && row_live;
+          uint32_t sr[4][32];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tc_ld32(sbuf + 32u * q, sr[q]);
+          // logits (log2 units), causal limit of this position, row maximum
+          float mx = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int t = blk * kBlock + 32 * q + k;
+              float x = __uint_as_float(sr[q][k]) * mul;
+              if (!mine || (blk == ell && t > pj)) x = -INFINITY;
+              sr[q][k] = __float_as_uint(x);
+              mx = fmaxf(mx, x);
+            }
+          }
+          const bool raise = mx > m_ref + kRescaleSlack;
+          const float m_new = raise ? mx : m_ref;
+          const float alpha = (raise && m_ref != -INFINITY) ? ex2_approx(m_ref - m_new) : 1.f;
+          if (__any_sync(kAll, raise && m_ref != -INFINITY)) {
+            // O *= alpha once the previous block's P V has landed
+            if (n >= 1 && !mbar_wait(sbuf_free((n - 1) & 1), static_cast<uint32_t>((n - 1) >> 1) & 1u)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t ov[32];
+              tc_ld32(tmem + lane_base + kTuO + 32u * q, ov);
+#pragma unroll
+              for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
+              tc_st32(tmem + lane_base + kTuO + 32u * q, ov);
+            }
+          }
+          m_ref = m_new;
+          l_sum *= alpha;
+          // P = 2^(x - m) in bf16 pairs over the buffer's first 64 columns
+          const float neg_ref = m_ref == -INFINITY ? 0.f : -m_ref;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const float p0 = ex2_approx(__uint_as_float(sr[q][2 * k]) + neg_ref);
+              const float p1 = ex2_approx(__uint_as_float(sr[q][2 * k + 1]) + neg_ref);
+              l_sum += p0 + p1;
+              pk[k] = pack_bf16x2(p0, p1);
+            }
+            tc_st16(sbuf + 16u * q, pk);
+          }
+        } else {
+          uint32_t zz[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) zz[k] = 0u;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tc_st16(sbuf + 16u * q, zz);
+        }
+        // V rows past the last cached token: zeros (thread r takes token row r)
+        if (blk == last_blk && blk * kBlock + r > L - 1) {
+          const uint32_t vrow = base_addr + Ly.stages + static_cast<uint32_t>(s) * kTileBytes + 2 * kBoxBytes +
+                                static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            st_shared_zero16(vrow + 16u * k);
+            st_shared_zero16(vrow + kBoxBytes + 16u * k);
+          }
+        }
+        fence_proxy_async_smem();
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(bb));
+      }
+      // the group's output rows
+      if (ok && total > 0) {
+        if (!mbar_wait(o_full, static_cast<uint32_t>(gq) & 1u)) {
+          ok = false;
+        } else {
+          tc_fence_after();
+          const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t ov[32];
+            tc_ld32(tmem + lane_base + kTuO + 32u * q, ov);
+            if (row_live) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int k = 0; k < 16; ++k)
+                pk[k] = pack_bf16x2(__uint_as_float(ov[2 * k]) * inv, __uint_as_float(ov[2 * k + 1]) * inv);
+              uint4* dst = reinterpret_cast<uint4*>(p.out + head * kDim + 32 * q);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(o_free);
+        }
+      }
+      if (row_live && total == 0) {                // no block: output 0, lse -inf
+        uint4* dst = reinterpret_cast<uint4*>(p.out + head * kDim);
+        for (int k = 0; k < 16; ++k) dst[k] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (row_live && p.lse != nullptr) p.lse[head] = l_sum > 0.f ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
+    }
+    if (!ok) *abort_flag = 1;
+    n_base += total;
+    if (total > 0) ++gq;
+    __syncthreads();                 // the next group rebuilds the bitmaps and the queries
+    if (*abort_flag) break;
+  }
+  if (*abort_flag && lane == 0) set_flag(p.flags, MSA_FLAG_TIMEOUT);
+  if (warp == 0 && lane == 0) {
+    // no copy of this CTA may still be in flight when it exits
+    for (int k = n_issued > kTuStages ? n_issued - kTuStages : 0; k < n_issued; ++k)
+      if (!mbar_wait(full(k % kTuStages), static_cast<uint32_t>((k / kTuStages) & 1))) break;
+  }
+  if (warp == kTuMmaWarp && lane == 0) {     // every MMA has finished before TMEM is freed
+    tc_commit(done_bar);
+    mbar_wait(done_bar, 0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kTuMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTuCols) : "memory");
+  }
+}
+
 size_t gqa_workspace_bytes(int B, int Q, int G, int K) {
   const size_t rows = static_cast<size_t>(B) * Q * G;
   return rows * K * kPartialFloats * sizeof(float) + rows * sizeof(unsigned long long);
@@ -2149,12 +2601,19 @@ static bool bf16_tcgen05_selected() {
 // With several query positions and bf16 K/V, the union form (one CTA per
 // (request, KV head), each block read once) is used when there are at least
 // three groups for every four SMs; with fewer the per-position rows spread
-// better over the SMs. MSA_MULTIPOS_ATTENTION=union or =rows in the environment
-// (read on every call) forces one form.
+// better over the SMs. MSA_MULTIPOS_ATTENTION=union, =union_mma or =rows in the
+// environment (read on every call) forces one form.
+// The union form runs on tcgen05 (sparse_gqa_union_tc_kernel);
+// MSA_MULTIPOS_ATTENTION=union_mma selects its mma.sync form instead.
+static bool multipos_union_tc_selected() {
+  const char* e = getenv("MSA_MULTIPOS_ATTENTION");
+  return e == nullptr || strcmp(e, "union_mma") != 0;
+}
+
 static bool multipos_union_selected(const GqaArgs& a, int sms) {
   if (a.Q < 2 || a.NB > kUnMaxNB) return false;
   const char* e = getenv("MSA_MULTIPOS_ATTENTION");
-  if (e != nullptr && strcmp(e, "union") == 0) return true;
+  if (e != nullptr && (strcmp(e, "union") == 0 || strcmp(e, "union_mma") == 0)) return true;
   if (e != nullptr && strcmp(e, "rows") == 0) return false;
   return 4ll * a.B * a.G >= 3ll * sms;
 }
@@ -2215,6 +2674,19 @@ cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRec
   if (!a.nvfp4 && !a.fp8 && !bf16_tcgen05_selected() && multipos_union_selected(a, sms)) {
     // several positions, bf16 K/V: the union of each group's blocks, one CTA per group
     const int nw = (a.NB + 31) / 32;
+    if (multipos_union_tc_selected()) {
+      const size_t tsm = tu_layout(nw).total + 1024;
+      const int64_t ngroups = static_cast<int64_t>(a.B) * a.G;
+      const int TC = static_cast<int>(ngroups < sms ? ngroups : sms);
+      err = cudaFuncSetAttribute(sparse_gqa_union_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(tsm));
+      if (err != cudaSuccess) return err;
+      err = launch_pdl(sparse_gqa_union_tc_kernel, dim3(TC), dim3(32 * kTuWarps), tsm, stream, tk, tv, p);
+      rec->set("%ssparse_gqa bf16_tma_tcgen05 union_of_positions grid=%d block=%d smem=%zu stages=%d groups=%lld",
+               a.scores != nullptr ? "select+" : "", TC, 32 * kTuWarps, tsm, kTuStages,
+               static_cast<long long>(ngroups));
+      return err != cudaSuccess ? err : cudaGetLastError();
+    }
     const size_t usmem = un_layout(nw).total + 1024;
     const int64_t groups = static_cast<int64_t>(a.B) * a.G;
     const int UC = static_cast<int>(groups < sms ? groups : sms);

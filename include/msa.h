@@ -289,9 +289,11 @@ size_t msa_sparse_gqa_workspace_size(const msa_dims_t* dims, msa_dtype_t kv_dtyp
  * With several query positions and bf16 K/V, the positions of a (request, KV
  * head) pair are attended together when there are at least three such pairs
  * for every four SMs: one CTA streams the union of their selected blocks once
- * and each position attends over its own blocks. MSA_MULTIPOS_ATTENTION=union
+ * and each position attends over its own blocks, on the tcgen05 tensor cores
+ * with the 8 positions' 128 query rows in one tile. MSA_MULTIPOS_ATTENTION=union
  * or =rows in the environment (read on every call) forces that form or the
- * per-position one; both give the same results within the same tolerances.
+ * per-position one (=union_mma: the union form on mma.sync); all give the same
+ * results within the same tolerances.
  * For bf16 K/V the environment variable MSA_BF16_ATTENTION=tcgen05, read on
  * every call, selects a tcgen05 form of the tile. It computes S^T = K.Q^T and
  * O^T = V^T.P^T with S and O in tensor memory and gives the same results

@@ -216,7 +216,7 @@ def test_large_logits(name, monkeypatch):
     parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
 
 
-@pytest.mark.parametrize("kv,mode", [("bf16", "rows"), ("fp8", "rows"), ("bf16", "union")])
+@pytest.mark.parametrize("kv,mode", [("bf16", "rows"), ("fp8", "rows"), ("bf16", "union"), ("bf16", "union_mma")])
 def test_repeated_steps_are_bitwise_identical(kv, mode, monkeypatch):
     """The same step six times in a row gives bit-identical outputs (the
     kernels' merges are deterministic and nothing they read changes): 8

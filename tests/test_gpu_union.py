@@ -13,6 +13,9 @@ import parity
 
 pytestmark = pytest.mark.gpu
 
+# the tcgen05 form (M = 128 query rows: 8 positions x 16 heads) and the mma.sync form
+FORMS = ["union", "union_mma"]
+
 W = synth.WORKLOADS
 
 CASES = {
@@ -30,10 +33,11 @@ def _check_union_ran():
     assert "union_of_positions" in msa.last_dispatch(), msa.last_dispatch()
 
 
+@pytest.mark.parametrize("form", FORMS)
 @pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("case", list(CASES))
-def test_union_matches_oracle(case, fused, monkeypatch):
-    monkeypatch.setenv("MSA_MULTIPOS_ATTENTION", "union")
+def test_union_matches_oracle(case, fused, form, monkeypatch):
+    monkeypatch.setenv("MSA_MULTIPOS_ATTENTION", form)
     w = CASES[case]
     dw = parity.build(w)
     dw.step_fused() if fused else dw.step_separate()
@@ -41,11 +45,12 @@ def test_union_matches_oracle(case, fused, monkeypatch):
     parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
 
 
-def test_union_edge_lengths(monkeypatch):
+@pytest.mark.parametrize("form", FORMS)
+def test_union_edge_lengths(form, monkeypatch):
     """Lengths below, at and just past block boundaries: the 8 positions' local
     blocks differ, some requests have fewer candidates than k - 1, one has
     none."""
-    monkeypatch.setenv("MSA_MULTIPOS_ATTENTION", "union")
+    monkeypatch.setenv("MSA_MULTIPOS_ATTENTION", form)
     lens = np.array([8, 9, 130, 135, 136, 1028, 2948, 2951, 2952], dtype=np.int32)
     w = synth.scaled(W["spec8"], batch=len(lens), ctx=None, ctx_range=None)
     dw = parity.build(w, lens=lens)
@@ -54,9 +59,10 @@ def test_union_edge_lengths(monkeypatch):
     parity.verify_workload(dw, w, lens, run_step=False)
 
 
+@pytest.mark.parametrize("form", FORMS)
 @pytest.mark.parametrize("fused", [False, True])
-def test_union_unwritten_slots_hold_nan(fused, monkeypatch):
-    monkeypatch.setenv("MSA_MULTIPOS_ATTENTION", "union")
+def test_union_unwritten_slots_hold_nan(fused, form, monkeypatch):
+    monkeypatch.setenv("MSA_MULTIPOS_ATTENTION", form)
     w = CASES["spec8"]
     assert (synth.seq_lens(w) % 128 != 0).all()
     dw = parity.build(w)
@@ -66,8 +72,9 @@ def test_union_unwritten_slots_hold_nan(fused, monkeypatch):
     parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
 
 
-def test_union_large_logits(monkeypatch):
-    monkeypatch.setenv("MSA_MULTIPOS_ATTENTION", "union")
+@pytest.mark.parametrize("form", FORMS)
+def test_union_large_logits(form, monkeypatch):
+    monkeypatch.setenv("MSA_MULTIPOS_ATTENTION", form)
     plain = synth.request
 
     def scaled_request(w, b, length):
@@ -83,13 +90,14 @@ def test_union_large_logits(monkeypatch):
     parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
 
 
-def test_union_persistent_groups_and_repeat(monkeypatch):
+@pytest.mark.parametrize("form", FORMS)
+def test_union_persistent_groups_and_repeat(form, monkeypatch):
     """More groups than CTAs (each CTA runs several groups in turn, its stages
     and tags carried across them), two steps in a row giving the same output,
     and the per-position form agreeing within the oracle tolerance."""
     w = synth.scaled(W["spec8"], batch=200, ctx=1400)
     dw = parity.build(w)
-    monkeypatch.setenv("MSA_MULTIPOS_ATTENTION", "union")
+    monkeypatch.setenv("MSA_MULTIPOS_ATTENTION", form)
     dw.step_separate()
     _check_union_ran()
     torch.cuda.synchronize()
@@ -107,10 +115,11 @@ def test_union_persistent_groups_and_repeat(monkeypatch):
     assert err.max().item() <= parity.OUT_MAX_ABS and err.mean().item() <= parity.OUT_MEAN_ABS
 
 
-def test_union_bad_inputs_are_flagged(monkeypatch):
+@pytest.mark.parametrize("form", FORMS)
+def test_union_bad_inputs_are_flagged(form, monkeypatch):
     """A selected block past a position's local block and a bad page id are
     flagged and skipped; the kernel neither traps nor hangs."""
-    monkeypatch.setenv("MSA_MULTIPOS_ATTENTION", "union")
+    monkeypatch.setenv("MSA_MULTIPOS_ATTENTION", form)
     w = CASES["spec8"]
     dw = parity.build(w)
     dw.step_separate()
