@@ -49,11 +49,14 @@ FALLBACK_HBM_GBS = 6800.0
 # workload and the hash of the kernel's sources when it was measured (a changed
 # kernel reports null until it is measured again). Summaries: profiles/.
 NCU_TRAFFIC = {
-    ("index_score", "b32_32k", "b355f71dbdd4de60"): 551650816 + 258048,
-    ("sparse_gqa", "b32_32k", "a1d657ef6852a159"): 134992128 + 123648,
-    ("index_score", "ragged", "b355f71dbdd4de60"): 2316355328 + 937728,
-    ("sparse_gqa", "ragged", "a1d657ef6852a159"): 270275072 + 466944,
-    ("sparse_gqa", "spec8", "a1d657ef6852a159"): 1057814784 + 3709696,
+    ("index_score", "ragged", "b355f71dbdd4de60"): 2316404736 + 872192,
+    ("sparse_gqa", "ragged", "fbbf06fc23aa2331"): 270277376 + 471040,
+    ("index_score", "b32_32k", "b355f71dbdd4de60"): 551692800 + 170240,
+    ("sparse_gqa", "b32_32k", "fbbf06fc23aa2331"): 134990592 + 118272,
+    ("index_score", "spec8", "b355f71dbdd4de60"): 1105678336 + 1441280,
+    ("sparse_gqa", "spec8", "fbbf06fc23aa2331"): 886568192 + 137472,
+    ("index_score", "nvfp4_256k", "b355f71dbdd4de60"): 2213757184 + 606976,
+    ("sparse_gqa", "nvfp4_256k", "fbbf06fc23aa2331"): 19318528 + 0,
 }
 
 # The headline workload (the largest configuration on one GPU: batch 64, ragged

@@ -1246,7 +1246,7 @@ __global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaPar
 constexpr int kUnWarps = 8;                      // consumer warps: one per query position (q_len <= 8)
 constexpr int kUnStages = 3;                     // 64 KB bf16 K/V tiles
 constexpr int kUnMaxNB = 8192;                   // block bitmaps kept in shared memory up to this many blocks
-constexpr int kUnAhead = 2;                      // union blocks prefetched into L2 beyond the stages
+constexpr int kUnAhead = 1;                      // union blocks prefetched into L2 beyond the stages (1: measured best)
 
 struct UnLayout {
   uint32_t stages, surv, bits, ubits, prefix, ulist, tags, bars, zero, total;
