@@ -77,6 +77,7 @@ struct GqaParams {
   uint32_t epoch;               // differs on every call; tags the tickets
   int B, Q, H, G, NB, P, K;
   int row_aligned;  // 1: every CTA owns whole rows; 0: balanced item ranges, rows may be split
+  int cluster_n;    // NVFP4 only: > 1 = each row split over one cluster of this many CTAs
   int64_t W;        // items = B * G * Q * K
 };
 
@@ -189,6 +190,37 @@ __device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, int la
 // async-proxy (bulk copy) writes to the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Thread-block cluster helpers. The barrier is the non-aligned form, so threads
+// of a warp may reach it from different places; every thread of the cluster
+// arrives at it, and each reaches it after bounded waits only.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// The address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
@@ -783,7 +815,7 @@ constexpr uint32_t kF4Codes = kBlock * kDim / 2;   // 8 KB of E2M1 codes per K o
 constexpr uint32_t kF4Scales = kBlock * kDim / 16; // 1 KB of E4M3 scales
 
 struct F4Layout {
-  uint32_t stages, vtile, comb_o, comb_ml, bars, total;
+  uint32_t stages, vtile, comb_o, comb_ml, xml, bars, total;
 };
 __host__ __device__ constexpr F4Layout f4_layout() {
   F4Layout s{};
@@ -791,7 +823,8 @@ __host__ __device__ constexpr F4Layout f4_layout() {
   s.vtile = kF4Stages * kFp4StageBytes;                     // fp16 V: two 128-row x 64-dim swizzled boxes
   s.comb_o = s.vtile + 2 * kBoxBytes;
   s.comb_ml = s.comb_o + kF4Warps * kGroup * kDim * 4;
-  s.bars = s.comb_ml + kF4Warps * kGroup * 2 * 4;
+  s.xml = s.comb_ml + kF4Warps * kGroup * 2 * 4;            // a cluster row's (m, l) per head
+  s.bars = s.xml + kGroup * 2 * 4;
   s.total = s.bars + (2 * kF4Stages + 2) * 8 + 16;          // + the last-arriver flag
   return s;
 }
@@ -827,8 +860,19 @@ __global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaPar
   griddep_wait();
 
   const int C = gridDim.x;
-  const int64_t x0 = p.W * blockIdx.x / C, x1 = p.W * (blockIdx.x + 1) / C;
-  if (x0 >= x1) return;
+  const bool clustered = p.cluster_n > 1;
+  const uint32_t crank = clustered ? cluster_rank() : 0u;
+  int64_t x0, x1;
+  if (clustered) {
+    // one row per cluster, its slots split evenly over the cluster's CTAs (K >= cluster_n)
+    const int64_t r = blockIdx.x / p.cluster_n;
+    x0 = r * p.K + static_cast<int64_t>(p.K) * crank / p.cluster_n;
+    x1 = r * p.K + static_cast<int64_t>(p.K) * (crank + 1) / p.cluster_n;
+  } else {
+    x0 = p.W * blockIdx.x / C;
+    x1 = p.W * (blockIdx.x + 1) / C;
+    if (x0 >= x1) return;
+  }
   if (p.scores != nullptr) {
     // Stage 2 inside this launch: every warp selects rows this CTA touches
     // (rows shared with other CTAs get the same result from each), staging its
@@ -958,7 +1002,9 @@ __global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaPar
 
   // Merges the eight warps' states of the current row; writes the output when
   // the CTA covered the whole row, a split-K partial otherwise (the CTA that
-  // delivers a row's last partial merges them all).
+  // delivers a row's last partial merges them all, or in a cluster every CTA
+  // its share of the heads).
+  bool cluster_done = false;          // this thread passed the cluster's two barriers
   auto end_segment = [&]() -> bool {
     float lt[2];
 #pragma unroll
@@ -1016,6 +1062,49 @@ __global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaPar
       *reinterpret_cast<uint4*>(p.out + head * kDim + d0) = pk;
       if (p.lse != nullptr && (tid & 15) == 0) p.lse[head] = ll > 0.f ? (mm + log2f(ll)) * kLn2 : -INFINITY;
     };
+    if (clustered) {
+      // The cluster's CTAs exchange their partials through distributed shared
+      // memory: CTA q finalises heads [q, q + 1) * 16 / cluster_n, reading the
+      // other CTAs' partials of those heads. A partial goes to this thread's
+      // own slot of warp 0's merge rows (read only by this thread above).
+      const int hpc = kGroup / p.cluster_n;
+      const bool mine = hh / hpc == static_cast<int>(crank);
+      float* xml = reinterpret_cast<float*>(sm + Ly.xml);
+      if (!mine) {
+        float4* dst = reinterpret_cast<float4*>(comb_o + hh * kDim + d0);
+        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        if ((tid & 15) == 0) {
+          xml[hh] = M;
+          xml[kGroup + hh] = Ls;
+        }
+      }
+      cluster_done = true;
+      cluster_sync_all();                 // every partial written
+      if (mine) {
+        const uint32_t po = smem_addr(comb_o + hh * kDim + d0);
+        const uint32_t pm = smem_addr(xml + hh), pl = smem_addr(xml + kGroup + hh);
+        for (int q = 0; q < p.cluster_n; ++q) {
+          if (q == static_cast<int>(crank)) continue;
+          const float Mq = ld_cluster_f32(cluster_map(pm, q));
+          if (Mq == -INFINITY) continue;
+          const float Lq = ld_cluster_f32(cluster_map(pl, q));
+          const float4 a = ld_cluster_f4(cluster_map(po, q));
+          const float4 b = ld_cluster_f4(cluster_map(po + 16, q));
+          const float Mn = fmaxf(M, Mq);
+          const float fs = M == -INFINITY ? 0.f : ex2_approx(M - Mn), fq = ex2_approx(Mq - Mn);
+          Ls = fs * Ls + fq * Lq;
+          acc[0] = fs * acc[0] + fq * a.x; acc[1] = fs * acc[1] + fq * a.y;
+          acc[2] = fs * acc[2] + fq * a.z; acc[3] = fs * acc[3] + fq * a.w;
+          acc[4] = fs * acc[4] + fq * b.x; acc[5] = fs * acc[5] + fq * b.y;
+          acc[6] = fs * acc[6] + fq * b.z; acc[7] = fs * acc[7] + fq * b.w;
+          M = Mn;
+        }
+        write_out(acc, M, Ls);
+      }
+      cluster_sync_all();                 // no CTA leaves while another reads its partials
+      return true;
+    }
     if (whole) {
       write_out(acc, M, Ls);
       return group_sync(smem_addr(&gbar[1]), gph[1], lane);
@@ -1220,6 +1309,12 @@ __global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaPar
     if (++kx == 32) { kx = 0; base += 32; cur = nxt; nxt = load_item(p, base + 32 + lane, x1, w == 0); }
   }
   if (ok && seg_row >= 0) ok = end_segment();
+  if (clustered && !cluster_done) {
+    // a wait gave up before the row's exchange: still pass both cluster
+    // barriers, which the other CTAs of the cluster wait on
+    cluster_sync_all();
+    cluster_sync_all();
+  }
   if (!ok && lane == 0) set_flag(p.flags, MSA_FLAG_TIMEOUT);
   if (w == 0 && lane == 0) {
     // no copy of this CTA may still be in flight when it exits
@@ -2618,6 +2713,57 @@ static bool multipos_union_selected(const GqaArgs& a, int sms) {
   return 4ll * a.B * a.G >= 3ll * sms;
 }
 
+// How many clusters of `cn` NVFP4 CTAs can be resident at once on this device
+// (cached per device and size).
+static int fp4_max_active_clusters(int cn, size_t smem) {
+  static std::atomic<int> cache[64][3];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const int slot = cn == 2 ? 0 : cn == 4 ? 1 : 2;
+  if (dev < 64) {
+    const int v = cache[dev][slot].load();
+    if (v > 0) return v - 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cn * 64));
+  cfg.blockDim = dim3(32 * kF4Warps);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cn);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, sparse_gqa_fp4_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  if (dev < 64) cache[dev][slot].store(n + 1);
+  return n;
+}
+
+// NVFP4 rows are split over the CTAs of a thread-block cluster and merged
+// through distributed shared memory when every row's cluster can be resident at
+// once: the largest cluster of 8, 4 or 2 CTAs (at most K, so every CTA has a
+// slot) that allows it. Otherwise item ranges are balanced over the SMs and
+// split rows merge through the workspace. MSA_NVFP4_SPLIT=tickets, =cluster2,
+// =cluster4 or =cluster8 in the environment (read on every call) forces a form.
+static int fp4_cluster_size(int64_t rows, int K, size_t smem) {
+  const char* e = getenv("MSA_NVFP4_SPLIT");
+  if (e != nullptr && strcmp(e, "tickets") == 0) return 1;
+  if (e != nullptr && strncmp(e, "cluster", 7) == 0) {
+    const int forced = atoi(e + 7);
+    if (forced == 2 || forced == 4 || forced == 8) return forced <= K ? forced : 1;
+  }
+  for (int cn = 8; cn >= 2; cn /= 2) {
+    if (cn > K) continue;
+    if (rows <= fp4_max_active_clusters(cn, smem)) return cn;
+  }
+  return 1;
+}
+
 cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRecord* rec) {
   GqaParams p;
   p.q = a.q;
@@ -2639,6 +2785,7 @@ cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRec
   p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
   p.B = a.B; p.Q = a.Q; p.H = a.H; p.G = a.G; p.NB = a.NB; p.P = a.P; p.K = a.K;
   p.W = static_cast<int64_t>(a.B) * a.G * a.Q * a.K;
+  p.cluster_n = 0;
   if (p.W == 0) {
     rec->set("sparse_gqa empty");
     return cudaSuccess;
@@ -2715,6 +2862,18 @@ cudaError_t launch_sparse_gqa(const GqaArgs& a, cudaStream_t stream, DispatchRec
     err = cudaFuncSetAttribute(sparse_gqa_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(wsmem));
     if (err != cudaSuccess) return err;
+    const int cn = fp4_cluster_size(rows, a.K, wsmem);
+    if (cn > 1) {
+      p.cluster_n = cn;
+      const int64_t grid = rows * cn;
+      err = launch_pdl_cluster(sparse_gqa_fp4_kernel, dim3(static_cast<unsigned>(grid)), dim3(32 * kF4Warps), wsmem,
+                               stream, cn, p);
+      rec->set("%ssparse_gqa nvfp4_regk_f16_mma 8warps cluster_split_dsmem_combine cluster=%d grid=%lld block=%d "
+               "smem=%zu stages=%d items=%lld",
+               a.scores != nullptr ? "select+" : "", cn, static_cast<long long>(grid), 32 * kF4Warps, wsmem,
+               kF4Stages, static_cast<long long>(p.W));
+      return err != cudaSuccess ? err : cudaGetLastError();
+    }
     err = launch_pdl(sparse_gqa_fp4_kernel, dim3(C), dim3(32 * kF4Warps), wsmem, stream, p);
     rec->set("%ssparse_gqa nvfp4_regk_f16_mma 8warps persistent split_k_fused_combine grid=%d block=%d smem=%zu "
              "stages=%d items=%lld",

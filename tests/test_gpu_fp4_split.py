@@ -1,0 +1,106 @@
+"""NVFP4 K/V attention in each of its split forms, against the oracle.
+
+The kernel splits a row's selected blocks over the CTAs of a thread-block
+cluster (2, 4 or 8 CTAs, partials merged through distributed shared memory)
+when every row's cluster fits on the GPU at once, and otherwise balances item
+ranges over the SMs and merges split rows through the workspace.
+MSA_NVFP4_SPLIT forces one form; each is checked on ragged tails, several
+positions, two KV heads, top-k values that do not divide evenly over the
+cluster, and lengths with fewer candidates than CTAs.
+"""
+import numpy as np
+import pytest
+import torch
+
+from block_sparse_attention_07_gb300 import msa, synth
+
+import parity
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+FORMS = ["auto", "tickets", "cluster2", "cluster4", "cluster8"]
+
+CASES = {
+    "b3": synth.scaled(W["nvfp4_256k"], batch=3, ctx=3000),
+    "q2": synth.scaled(W["nvfp4_256k"], batch=2, ctx=3001, q_len=2),
+    "g2": synth.scaled(W["nvfp4_256k"], batch=2, ctx=2700, n_heads=32, n_kv_heads=2, n_idx_heads=2),
+    "top5": synth.scaled(W["nvfp4_256k"], batch=2, ctx=2600, topk=5),
+    "top3": synth.scaled(W["nvfp4_256k"], batch=2, ctx=2500, topk=3),
+}
+
+
+def _expect_form(form, K):
+    d = msa.last_dispatch()
+    assert "nvfp4_regk_f16_mma" in d, d
+    if form == "tickets":
+        assert "split_k_fused_combine" in d, d
+    elif form.startswith("cluster"):
+        cn = int(form[len("cluster"):])
+        if cn <= K:
+            assert f"cluster={cn} " in d, d
+        else:
+            assert "split_k_fused_combine" in d, d
+
+
+def _set_form(form, monkeypatch):
+    if form == "auto":
+        monkeypatch.delenv("MSA_NVFP4_SPLIT", raising=False)
+    else:
+        monkeypatch.setenv("MSA_NVFP4_SPLIT", form)
+
+
+@pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("case", list(CASES))
+def test_fp4_split_matches_oracle(case, form, monkeypatch):
+    _set_form(form, monkeypatch)
+    w = CASES[case]
+    dw = parity.build(w)
+    dw.step_separate()
+    _expect_form(form, w.topk)
+    parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
+
+
+@pytest.mark.parametrize("form", FORMS)
+def test_fp4_split_edge_lengths(form, monkeypatch):
+    """No candidates, one block, block boundaries: many CTAs of a cluster hold
+    only empty slots, and some rows have a single valid block."""
+    _set_form(form, monkeypatch)
+    lens = np.array([1, 127, 128, 129, 1500, 2049], dtype=np.int32)
+    w = synth.scaled(W["nvfp4_256k"], batch=len(lens), ctx=None, ctx_range=None)
+    dw = parity.build(w, lens=lens)
+    dw.step_separate()
+    _expect_form(form, w.topk)
+    parity.verify_workload(dw, w, lens, run_step=False)
+
+
+@pytest.mark.parametrize("form", ["cluster2", "cluster8", "tickets"])
+def test_fp4_split_repeats_bitwise(form, monkeypatch):
+    """The same step six times gives bit-identical outputs, cache slots past
+    each length poisoned with NaN patterns."""
+    _set_form(form, monkeypatch)
+    lens = np.array([9, 130, 1028, 2951], dtype=np.int32)
+    w = synth.scaled(W["nvfp4_256k"], batch=len(lens), ctx=None, ctx_range=None)
+    dw = parity.build(w, lens=lens)
+    parity.poison_unwritten_slots(dw)
+    outs = []
+    for _ in range(6):
+        dw.step_separate()
+        torch.cuda.synchronize()
+        outs.append(dw.out.clone())
+    assert dw.check_flags() == 0
+    for k, o in enumerate(outs[1:], 1):
+        assert torch.equal(o, outs[0]), f"step {k} differs from step 0"
+    parity.verify_workload(dw, w, lens, run_step=False)
+
+
+def test_fp4_benchmark_batch_takes_a_cluster(monkeypatch):
+    """At the benchmark's batch (16 requests x 4 KV heads = 64 rows) every row's
+    cluster fits on the GPU at once, so the automatic choice is a cluster; the
+    output matches the oracle on sampled requests."""
+    monkeypatch.delenv("MSA_NVFP4_SPLIT", raising=False)
+    w = synth.scaled(W["nvfp4_256k"], ctx=2300)
+    dw = parity.build(w)
+    dw.step()
+    assert "cluster=" in msa.last_dispatch(), msa.last_dispatch()
+    parity.verify_workload(dw, w, synth.seq_lens(w), sample=[0, 7, len(dw.which) - 1], run_step=False)

@@ -22,17 +22,23 @@ W = synth.WORKLOADS
 
 GRAPH_CASES = {
     # bf16 KV: every CTA owns whole rows
-    "bf16": synth.scaled(W["b32_32k"], batch=3, ctx=2000),
+    "bf16": (synth.scaled(W["b32_32k"], batch=3, ctx=2000), None),
     # NVFP4 KV: rows split over CTAs and merged by the last arriver (tickets)
-    "nvfp4_split_rows": synth.scaled(W["nvfp4_256k"], batch=2, ctx=3000),
+    "nvfp4_split_rows": (synth.scaled(W["nvfp4_256k"], batch=2, ctx=3000), "tickets"),
+    # NVFP4 KV: each row split over a thread-block cluster (the automatic choice here)
+    "nvfp4_cluster": (synth.scaled(W["nvfp4_256k"], batch=2, ctx=3000), None),
     # NVFP4 index keys, 8 positions
-    "spec_fp4idx": synth.scaled(W["spec8"], batch=2, ctx=2600, idx_dtype="nvfp4"),
+    "spec_fp4idx": (synth.scaled(W["spec8"], batch=2, ctx=2600, idx_dtype="nvfp4"), None),
 }
 
 
 @pytest.mark.parametrize("name", list(GRAPH_CASES))
-def test_graph_replay_matches_eager_and_oracle(name):
-    w = GRAPH_CASES[name]
+def test_graph_replay_matches_eager_and_oracle(name, monkeypatch):
+    w, split = GRAPH_CASES[name]
+    if split is None:
+        monkeypatch.delenv("MSA_NVFP4_SPLIT", raising=False)
+    else:
+        monkeypatch.setenv("MSA_NVFP4_SPLIT", split)
     dw = parity.build(w)
     dw.step()
     torch.cuda.synchronize()
@@ -89,11 +95,12 @@ def test_layer_reusing_selection(name, graph):
     assert not torch.equal(layer.out, src.out)
 
 
-def test_two_streams_at_once():
+def test_two_streams_at_once(monkeypatch):
     """Two independent decode steps in flight on two streams at once: an NVFP4
     one whose rows are merged through tickets, and a bf16 one. Each has its own
     workspace and caches, and both must still match the oracle and repeat
     bit for bit."""
+    monkeypatch.setenv("MSA_NVFP4_SPLIT", "tickets")
     wa = synth.scaled(W["nvfp4_256k"], batch=2, ctx=3000)
     wb = synth.scaled(W["b32_32k"], batch=3, ctx=2000)
     da, db = parity.build(wa), parity.build(wb)

@@ -44,12 +44,13 @@ def test_noalloc_matches_workspace_entry_point(name, changes):
         assert np.abs(l - ref_lse).max() <= parity.LSE_ABS, f"call {call}"
 
 
-def test_noalloc_split_rows_across_changing_shapes():
-    """NVFP4 K/V rows are split over CTAs and merged through the scratch array.
-    A large batch, then a small one with other lengths, then the large one
-    again: each call finds the previous call's partials and tickets in the
-    array (laid out for another shape) and must still match the workspace
-    entry point."""
+def test_noalloc_split_rows_across_changing_shapes(monkeypatch):
+    """NVFP4 K/V rows are split over CTAs and merged through the scratch array
+    (the balanced form, forced for the small batch too). A large batch, then a
+    small one with other lengths, then the large one again: each call finds
+    the previous call's partials and tickets in the array (laid out for
+    another shape) and must still match the workspace entry point."""
+    monkeypatch.setenv("MSA_NVFP4_SPLIT", "tickets")
     big = parity.build(synth.scaled(synth.WORKLOADS["nvfp4_256k"], batch=64, ctx=3000))
     small = parity.build(synth.scaled(synth.WORKLOADS["nvfp4_256k"], batch=3, ctx=None, ctx_range=(900, 5000),
                                       seed=20261301))
