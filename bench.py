@@ -50,13 +50,13 @@ FALLBACK_HBM_GBS = 6800.0
 # kernel reports null until it is measured again). Summaries: profiles/.
 NCU_TRAFFIC = {
     ("index_score", "ragged", "b355f71dbdd4de60"): 2316404736 + 872192,
-    ("sparse_gqa", "ragged", "fbbf06fc23aa2331"): 270277376 + 471040,
+    ("sparse_gqa", "ragged", "1e309e3339da89c4"): 270274560 + 548096,
     ("index_score", "b32_32k", "b355f71dbdd4de60"): 551692800 + 170240,
-    ("sparse_gqa", "b32_32k", "fbbf06fc23aa2331"): 134990592 + 118272,
+    ("sparse_gqa", "b32_32k", "1e309e3339da89c4"): 134992384 + 159232,
     ("index_score", "spec8", "b355f71dbdd4de60"): 1105678336 + 1441280,
-    ("sparse_gqa", "spec8", "fbbf06fc23aa2331"): 886568192 + 137472,
+    ("sparse_gqa", "spec8", "1e309e3339da89c4"): 886429440 + 190208,
     ("index_score", "nvfp4_256k", "b355f71dbdd4de60"): 2213757184 + 606976,
-    ("sparse_gqa", "nvfp4_256k", "fbbf06fc23aa2331"): 19318528 + 0,
+    ("sparse_gqa", "nvfp4_256k", "1e309e3339da89c4"): 19318784 + 1280,
 }
 
 # The headline workload (the largest configuration on one GPU: batch 64, ragged

@@ -133,9 +133,9 @@ __device__ __forceinline__ ItemInfo load_item(const GqaParams& p, int64_t x, int
   const int e = static_cast<int>(static_cast<uint32_t>(x) - r * static_cast<uint32_t>(p.K));
   const RowPos rp = row_pos(p, r);
   it.g = rp.g;
+  const int L = p.seq_lens[rp.b];          // loaded alongside the selection, not after it
   it.blk = p.selected[((static_cast<int64_t>(rp.b) * p.Q + rp.j) * p.G + rp.g) * p.K + e];
   if (it.blk < 0) return it;
-  const int L = p.seq_lens[rp.b];
   if (L < p.Q || L > p.NB * kBlock || L < 1) {
     if (report) set_flag(p.flags, MSA_FLAG_BAD_SEQLEN);
     return it;
@@ -200,27 +200,39 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait;" ::: "memory"); }
+// Asynchronous stores into another CTA's shared memory (`addr` from
+// cluster_map), each completing its bytes on the mbarrier at `rbar` in that CTA.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+               ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_v2(uint32_t addr, float a, float b, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+               ::"r"(addr), "f"(a), "f"(b), "r"(rbar)
+               : "memory");
+}
+// Non-blocking test of an mbarrier phase (try_wait may suspend the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 // The address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
-}
-__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
 }
 
 __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
@@ -814,8 +826,16 @@ constexpr int kF4Stages = 6;
 constexpr uint32_t kF4Codes = kBlock * kDim / 2;   // 8 KB of E2M1 codes per K or V block
 constexpr uint32_t kF4Scales = kBlock * kDim / 16; // 1 KB of E4M3 scales
 
+// A cluster row's receive buffer: per sending CTA and finalised head, the 128
+// output sums, then m and l (a 528-byte stride keeps the vector stores aligned).
+constexpr int kXStride = kDim + 4;
+constexpr uint32_t kXRecvBytes = 7 * 2 * kXStride * 4;   // the largest of (n - 1) x (16 / n) heads, n = 2, 4, 8
+__host__ __device__ constexpr uint32_t cluster_expected_bytes(int n) {
+  return static_cast<uint32_t>((n - 1) * (kGroup / n) * (kGroup * 32 + 8));   // 16 x 32 B + m, l per head
+}
+
 struct F4Layout {
-  uint32_t stages, vtile, comb_o, comb_ml, xml, bars, total;
+  uint32_t stages, vtile, comb_o, comb_ml, xrecv, bars, total;
 };
 __host__ __device__ constexpr F4Layout f4_layout() {
   F4Layout s{};
@@ -823,9 +843,9 @@ __host__ __device__ constexpr F4Layout f4_layout() {
   s.vtile = kF4Stages * kFp4StageBytes;                     // fp16 V: two 128-row x 64-dim swizzled boxes
   s.comb_o = s.vtile + 2 * kBoxBytes;
   s.comb_ml = s.comb_o + kF4Warps * kGroup * kDim * 4;
-  s.xml = s.comb_ml + kF4Warps * kGroup * 2 * 4;            // a cluster row's (m, l) per head
-  s.bars = s.xml + kGroup * 2 * 4;
-  s.total = s.bars + (2 * kF4Stages + 2) * 8 + 16;          // + the last-arriver flag
+  s.xrecv = s.comb_ml + kF4Warps * kGroup * 2 * 4;
+  s.bars = s.xrecv + kXRecvBytes;
+  s.total = s.bars + (2 * kF4Stages + 2) * 8 + 16 + 8;      // + the last-arriver flag, the cluster exchange barrier
   return s;
 }
 
@@ -843,8 +863,10 @@ __global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaPar
   float* comb_m = reinterpret_cast<float*>(sm + Ly.comb_ml);
   float* comb_l = comb_m + kF4Warps * kGroup;
   int* last_flag = reinterpret_cast<int*>(sm + Ly.bars + (2 * kF4Stages + 2) * 8);
+  uint64_t* xbar = reinterpret_cast<uint64_t*>(sm + Ly.bars + (2 * kF4Stages + 2) * 8 + 16);
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gr = lane >> 2, c = lane & 3;
+  const bool clustered = p.cluster_n > 1;
 
   griddep_launch_dependents();
   if (threadIdx.x == 0) {
@@ -854,13 +876,20 @@ __global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaPar
     }
     mbar_init(smem_addr(&gbar[0]), kF4Warps);
     mbar_init(smem_addr(&gbar[1]), kF4Warps);
+    if (clustered) {
+      // armed now with the bytes the other CTAs will store into the receive buffer
+      mbar_init(smem_addr(xbar), 1);
+      mbar_arrive_expect_tx(smem_addr(xbar), cluster_expected_bytes(p.cluster_n));
+    }
     fence_mbar_init();
   }
   __syncthreads();
+  // The other CTAs store into this CTA's receive buffer only after every CTA
+  // of the cluster passed this point (waited for at the row's end).
+  if (clustered) cluster_arrive_relaxed();
   griddep_wait();
 
   const int C = gridDim.x;
-  const bool clustered = p.cluster_n > 1;
   const uint32_t crank = clustered ? cluster_rank() : 0u;
   int64_t x0, x1;
   if (clustered) {
@@ -923,7 +952,7 @@ __global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaPar
       int go = 0;
       if (lane == 0) {
         if (is < need) go = mbar_wait(smem_addr(&empty[s]), par) ? 1 : -1;
-        else go = mbar_try_wait(smem_addr(&empty[s]), par) ? 1 : 0;
+        else go = mbar_test_wait(smem_addr(&empty[s]), par) ? 1 : 0;
         if (go == 1) {
           const uint32_t fb = smem_addr(&full[s]);
           const uint32_t dst = base_addr + Ly.stages + s * kStageBytes;
@@ -1004,7 +1033,7 @@ __global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaPar
   // the CTA covered the whole row, a split-K partial otherwise (the CTA that
   // delivers a row's last partial merges them all, or in a cluster every CTA
   // its share of the heads).
-  bool cluster_done = false;          // this thread passed the cluster's two barriers
+  bool cluster_done = false;          // this thread took part in the cluster's exchange
   auto end_segment = [&]() -> bool {
     float lt[2];
 #pragma unroll
@@ -1063,34 +1092,35 @@ __global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaPar
       if (p.lse != nullptr && (tid & 15) == 0) p.lse[head] = ll > 0.f ? (mm + log2f(ll)) * kLn2 : -INFINITY;
     };
     if (clustered) {
-      // The cluster's CTAs exchange their partials through distributed shared
-      // memory: CTA q finalises heads [q, q + 1) * 16 / cluster_n, reading the
-      // other CTAs' partials of those heads. A partial goes to this thread's
-      // own slot of warp 0's merge rows (read only by this thread above).
+      // CTA q finalises heads [q, q + 1) * 16 / cluster_n. Every other CTA
+      // stores its partials of those heads straight into q's receive buffer
+      // (asynchronous stores that complete bytes on q's exchange barrier, armed
+      // at the start); q waits for the barrier, merges in sender order and
+      // writes the output.
       const int hpc = kGroup / p.cluster_n;
-      const bool mine = hh / hpc == static_cast<int>(crank);
-      float* xml = reinterpret_cast<float*>(sm + Ly.xml);
-      if (!mine) {
-        float4* dst = reinterpret_cast<float4*>(comb_o + hh * kDim + d0);
-        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        if ((tid & 15) == 0) {
-          xml[hh] = M;
-          xml[kGroup + hh] = Ls;
-        }
-      }
+      const int dest = hh / hpc, hl = hh - dest * hpc;
+      const int me = static_cast<int>(crank);
+      const uint32_t xrecv = base_addr + Ly.xrecv;
       cluster_done = true;
-      cluster_sync_all();                 // every partial written
-      if (mine) {
-        const uint32_t po = smem_addr(comb_o + hh * kDim + d0);
-        const uint32_t pm = smem_addr(xml + hh), pl = smem_addr(xml + kGroup + hh);
-        for (int q = 0; q < p.cluster_n; ++q) {
-          if (q == static_cast<int>(crank)) continue;
-          const float Mq = ld_cluster_f32(cluster_map(pm, q));
+      cluster_wait();                     // every CTA's exchange barrier is armed
+      if (dest != me) {
+        const int j = me < dest ? me : me - 1;                  // this CTA's sender slot at dest
+        const uint32_t slot = xrecv + static_cast<uint32_t>((j * hpc + hl) * kXStride) * 4u;
+        const uint32_t rbar = cluster_map(smem_addr(xbar), dest);
+        st_async_v4(cluster_map(slot + d0 * 4, dest), acc[0], acc[1], acc[2], acc[3], rbar);
+        st_async_v4(cluster_map(slot + d0 * 4 + 16, dest), acc[4], acc[5], acc[6], acc[7], rbar);
+        if ((tid & 15) == 0) st_async_v2(cluster_map(slot + kDim * 4, dest), M, Ls, rbar);
+      }
+      bool got = true;
+      if (dest == me) {
+        got = mbar_wait(smem_addr(xbar), 0u);
+        const float* xr = reinterpret_cast<const float*>(sm + Ly.xrecv);
+        for (int j = 0; got && j < p.cluster_n - 1; ++j) {
+          const float* pq = xr + (j * hpc + hl) * kXStride;
+          const float Mq = pq[kDim], Lq = pq[kDim + 1];
           if (Mq == -INFINITY) continue;
-          const float Lq = ld_cluster_f32(cluster_map(pl, q));
-          const float4 a = ld_cluster_f4(cluster_map(po, q));
-          const float4 b = ld_cluster_f4(cluster_map(po + 16, q));
+          const float4 a = *reinterpret_cast<const float4*>(pq + d0);
+          const float4 b = *reinterpret_cast<const float4*>(pq + d0 + 4);
           const float Mn = fmaxf(M, Mq);
           const float fs = M == -INFINITY ? 0.f : ex2_approx(M - Mn), fq = ex2_approx(Mq - Mn);
           Ls = fs * Ls + fq * Lq;
@@ -1100,10 +1130,12 @@ __global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaPar
           acc[6] = fs * acc[6] + fq * b.z; acc[7] = fs * acc[7] + fq * b.w;
           M = Mn;
         }
-        write_out(acc, M, Ls);
+        if (got) write_out(acc, M, Ls);
       }
-      cluster_sync_all();                 // no CTA leaves while another reads its partials
-      return true;
+      // no CTA leaves while another may still store into it
+      cluster_arrive_relaxed();
+      cluster_wait();
+      return got;
     }
     if (whole) {
       write_out(acc, M, Ls);
@@ -1310,10 +1342,12 @@ __global__ void __launch_bounds__(32 * kF4Warps, 1) sparse_gqa_fp4_kernel(GqaPar
   }
   if (ok && seg_row >= 0) ok = end_segment();
   if (clustered && !cluster_done) {
-    // a wait gave up before the row's exchange: still pass both cluster
-    // barriers, which the other CTAs of the cluster wait on
-    cluster_sync_all();
-    cluster_sync_all();
+    // a wait gave up before the row's exchange (the other CTAs' waits for
+    // this CTA's partials then give up too, flagged): still pass the cluster
+    // barriers that they wait on before leaving
+    cluster_wait();
+    cluster_arrive_relaxed();
+    cluster_wait();
   }
   if (!ok && lane == 0) set_flag(p.flags, MSA_FLAG_TIMEOUT);
   if (w == 0 && lane == 0) {
