@@ -299,6 +299,13 @@ size_t msa_sparse_gqa_workspace_size(const msa_dims_t* dims, msa_dtype_t kv_dtyp
  * O^T = V^T.P^T with S and O in tensor memory and gives the same results
  * within the same tolerances, but it is slower at 16 heads per KV head. The
  * default is the mma.sync tile.
+ * For NVFP4 K/V, when every row's cluster fits on the device at once, each
+ * (request, position, KV head) row is split over a thread-block cluster of 8,
+ * 4 or 2 CTAs whose partials are merged in distributed shared memory (no
+ * workspace use); otherwise the selected blocks are balanced over all SMs and
+ * split rows merge through the workspace. MSA_NVFP4_SPLIT=tickets, =cluster2,
+ * =cluster4 or =cluster8 in the environment (read on every call) forces a
+ * form; all give the same results within the same tolerances.
  * q: bf16 [B, Q, H, D]. out: bf16 [B, Q, H, D]. lse: fp32 [B, Q, H] or NULL.
  * workspace: device scratch of at least msa_sparse_gqa_workspace_size bytes
  * (B * Q * G * (topk * 8,320 + 8)), 256-byte aligned: split-K partials and one
