@@ -15,9 +15,11 @@
 //     (conflict-free ldmatrix); each of four consumer warps owns 32 tokens of
 //     every block; QK^T and PV run on m16n8k16 tensor-core mma. At a row's end
 //     the CTA merges its warps' online-softmax states and writes the output.
-//   sparse_gqa_fp4_kernel (NVFP4): eight consumer warps of 16 tokens, item
-//     ranges balanced over the SMs, split rows merged by the CTA that
-//     delivers the last partial.
+//   sparse_gqa_fp4_kernel (NVFP4): eight consumer warps of 16 tokens; each
+//     row split over the CTAs of a thread-block cluster that merge in
+//     distributed shared memory, or (when the rows' clusters do not all fit
+//     at once) item ranges balanced over the SMs, split rows merged by the
+//     CTA that delivers the last partial.
 //   sparse_gqa_union_kernel (bf16, several query positions): the union of a
 //     (request, KV head) group's blocks streamed once, one warp per position.
 //   sparse_gqa_tc_kernel (bf16, opt-in): the tile on tcgen05 with S and O in
@@ -814,11 +816,16 @@ __global__ void __launch_bounds__(32 * (1 + kCWarps), 1)
 // loaded with the same dims. V is expanded (E2M1 x E4M3 is exact in fp16) into
 // the warp's rows of a swizzled fp16 tile, rows past the causal limit written
 // as zeros, and read with ldmatrix.trans for P V; the stage is released after
-// Q K^T. The fp32 global scales multiply the logits and the output. Item
-// ranges are balanced over the CTAs and split rows merged through the
-// workspace, as in sparse_gqa_kernel. (The same eight-warp form for FP8 K/V
-// measured slower than four warps on whole rows, 32.3 against 24.8 us on
-// 32 x 32K: that conversion is bound by the ALU pipe, not by latency.)
+// Q K^T. The fp32 global scales multiply the logits and the output.
+// Work split: with few rows (every row's cluster resident at once), row r
+// runs on cluster r of n = 2, 4 or 8 CTAs, CTA q taking slots [q K / n,
+// (q + 1) K / n) and finalising heads [q, q + 1) 16 / n; the other CTAs push
+// their merged partials of those heads into its receive buffer with st.async
+// stores that complete bytes on its exchange barrier. Otherwise item ranges
+// are balanced over the CTAs and split rows merged through the workspace, as
+// in sparse_gqa_kernel. (The same eight-warp form for FP8 K/V measured slower
+// than four warps on whole rows, 32.3 against 24.8 us on 32 x 32K: there the
+// tensor and ALU pipes are both near saturation.)
 
 constexpr int kF4Warps = 8;
 constexpr int kF4Tok = kBlock / kF4Warps;          // 16 tokens per warp and block
