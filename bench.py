@@ -28,6 +28,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -46,17 +47,18 @@ METRIC = "MSA decode query-tokens/s at 1 GB300; achieved HBM GB/s vs peak per ke
 FALLBACK_HBM_GBS = 6800.0
 
 # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, keyed by kernel,
-# workload and the hash of the kernel's sources when it was measured (a changed
-# kernel reports null until it is measured again). Summaries: profiles/.
+# workload and the hash of the kernel's sources (comments and blank space left
+# out) when it was measured: a changed kernel reports null until it is measured
+# again. Summaries: profiles/.
 NCU_TRAFFIC = {
-    ("index_score", "ragged", "b355f71dbdd4de60"): 2316404736 + 872192,
-    ("sparse_gqa", "ragged", "1e309e3339da89c4"): 270274560 + 548096,
-    ("index_score", "b32_32k", "b355f71dbdd4de60"): 551692800 + 170240,
-    ("sparse_gqa", "b32_32k", "1e309e3339da89c4"): 134992384 + 159232,
-    ("index_score", "spec8", "b355f71dbdd4de60"): 1105678336 + 1441280,
-    ("sparse_gqa", "spec8", "1e309e3339da89c4"): 886429440 + 190208,
-    ("index_score", "nvfp4_256k", "b355f71dbdd4de60"): 2213757184 + 606976,
-    ("sparse_gqa", "nvfp4_256k", "1e309e3339da89c4"): 19318784 + 1280,
+    ("index_score", "ragged", "72980f2bc6a8b2b7"): 2316404736 + 872192,
+    ("sparse_gqa", "ragged", "0d0bc7b089cf32ce"): 270274560 + 548096,
+    ("index_score", "b32_32k", "72980f2bc6a8b2b7"): 551692800 + 170240,
+    ("sparse_gqa", "b32_32k", "0d0bc7b089cf32ce"): 134992384 + 159232,
+    ("index_score", "spec8", "72980f2bc6a8b2b7"): 1105678336 + 1441280,
+    ("sparse_gqa", "spec8", "0d0bc7b089cf32ce"): 886429440 + 190208,
+    ("index_score", "nvfp4_256k", "72980f2bc6a8b2b7"): 2213757184 + 606976,
+    ("sparse_gqa", "nvfp4_256k", "0d0bc7b089cf32ce"): 19318784 + 1280,
 }
 
 # The headline workload (the largest configuration on one GPU: batch 64, ragged
@@ -65,11 +67,19 @@ DEFAULT_WORKLOAD = "ragged"
 DEFAULT_CONFIGS = "b32_32k,spec8,nvfp4_256k"
 
 
+def _code_only(text):
+    """The source without its comments and blank space, so that a comment edit
+    leaves a measured kernel's key unchanged."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def _src_hash(*names):
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "block_sparse_attention_07_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "block_sparse_attention_07_gb300", "csrc", n), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
