@@ -62,6 +62,20 @@ def test_fp4_split_matches_oracle(case, form, monkeypatch):
 
 
 @pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("case", ["b3", "q2"])
+def test_fp4_split_with_selection_in_launch(case, form, monkeypatch):
+    """The selection inside the attention launch: every CTA of a row selects
+    that row's blocks (the same result from each) before reading them back."""
+    _set_form(form, monkeypatch)
+    w = CASES[case]
+    dw = parity.build(w)
+    dw.step_fused()
+    assert msa.last_dispatch().startswith("select+"), msa.last_dispatch()
+    _expect_form(form, w.topk)
+    parity.verify_workload(dw, w, synth.seq_lens(w), run_step=False)
+
+
+@pytest.mark.parametrize("form", FORMS)
 def test_fp4_split_edge_lengths(form, monkeypatch):
     """No candidates, one block, block boundaries: many CTAs of a cluster hold
     only empty slots, and some rows have a single valid block."""
