@@ -2779,7 +2779,7 @@ static int fp4_max_active_clusters(int cn, size_t smem) {
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, sparse_gqa_fp4_kernel, &cfg) != cudaSuccess) {
     cudaGetLastError();
-    n = 0;
+    return 0;                          // not cached: a later call asks again
   }
   if (dev < 64) cache[dev][slot].store(n + 1);
   return n;

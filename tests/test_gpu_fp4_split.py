@@ -118,3 +118,37 @@ def test_fp4_benchmark_batch_takes_a_cluster(monkeypatch):
     dw.step()
     assert "cluster=" in msa.last_dispatch(), msa.last_dispatch()
     parity.verify_workload(dw, w, synth.seq_lens(w), sample=[0, 7, len(dw.which) - 1], run_step=False)
+
+
+_CAPTURE_FIRST = r"""
+import torch
+from block_sparse_attention_07_gb300 import msa, synth
+from block_sparse_attention_07_gb300.workload import DeviceWorkload
+w = synth.scaled(synth.WORKLOADS["nvfp4_256k"], batch=3, ctx=2100)
+dw = DeviceWorkload(w, "cuda")
+g = dw.capture(dw.step)            # the first attention call of the process is captured
+g.replay()
+torch.cuda.synchronize()
+assert dw.check_flags() == 0
+assert "cluster=" in msa.last_dispatch(), msa.last_dispatch()
+replayed = dw.out.clone()
+dw.step()
+torch.cuda.synchronize()
+assert torch.equal(replayed, dw.out)
+print("ok")
+"""
+
+
+def test_fp4_cluster_choice_under_capture():
+    """A fresh process whose first NVFP4 attention call is made under CUDA
+    graph capture: the cluster-size query then runs inside the capture, and
+    the replay equals an eager step."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ)
+    env.pop("MSA_NVFP4_SPLIT", None)
+    r = subprocess.run([sys.executable, "-c", _CAPTURE_FIRST], cwd=root, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
