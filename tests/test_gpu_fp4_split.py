@@ -27,6 +27,8 @@ CASES = {
     "g2": synth.scaled(W["nvfp4_256k"], batch=2, ctx=2700, n_heads=32, n_kv_heads=2, n_idx_heads=2),
     "top5": synth.scaled(W["nvfp4_256k"], batch=2, ctx=2600, topk=5),
     "top3": synth.scaled(W["nvfp4_256k"], batch=2, ctx=2500, topk=3),
+    # 8 positions straddling a block end: 64 rows, clusters of two CTAs by default
+    "q8": synth.scaled(W["spec8"], batch=2, ctx=2693, kv_dtype="nvfp4"),
 }
 
 
