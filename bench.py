@@ -52,13 +52,13 @@ FALLBACK_HBM_GBS = 6800.0
 # again. Summaries: profiles/.
 NCU_TRAFFIC = {
     ("index_score", "ragged", "72980f2bc6a8b2b7"): 2316404736 + 872192,
-    ("sparse_gqa", "ragged", "0d0bc7b089cf32ce"): 270274560 + 548096,
+    ("sparse_gqa", "ragged", "9279da445860967d"): 270273024 + 555008,
     ("index_score", "b32_32k", "72980f2bc6a8b2b7"): 551692800 + 170240,
-    ("sparse_gqa", "b32_32k", "0d0bc7b089cf32ce"): 134992384 + 159232,
+    ("sparse_gqa", "b32_32k", "9279da445860967d"): 134991104 + 344320,
     ("index_score", "spec8", "72980f2bc6a8b2b7"): 1105678336 + 1441280,
-    ("sparse_gqa", "spec8", "0d0bc7b089cf32ce"): 886429440 + 190208,
+    ("sparse_gqa", "spec8", "9279da445860967d"): 886477312 + 436736,
     ("index_score", "nvfp4_256k", "72980f2bc6a8b2b7"): 2213757184 + 606976,
-    ("sparse_gqa", "nvfp4_256k", "0d0bc7b089cf32ce"): 19318784 + 1280,
+    ("sparse_gqa", "nvfp4_256k", "9279da445860967d"): 19318272 + 0,
 }
 
 # The headline workload (the largest configuration on one GPU: batch 64, ragged
