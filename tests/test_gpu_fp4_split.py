@@ -154,3 +154,17 @@ def test_fp4_cluster_choice_under_capture():
     r = subprocess.run([sys.executable, "-c", _CAPTURE_FIRST], cwd=root, env=env, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
+
+
+@pytest.mark.parametrize("batch", [18, 19, 20, 38])
+def test_fp4_around_the_cluster_capacity(batch, monkeypatch):
+    """Batches whose 4 B rows sit around the number of two-CTA clusters that fit
+    on the GPU at once (and around the four-CTA limit at 38): whichever form
+    the launcher picks matches the oracle on sampled requests."""
+    monkeypatch.delenv("MSA_NVFP4_SPLIT", raising=False)
+    w = synth.scaled(W["nvfp4_256k"], batch=batch, ctx=1700)
+    dw = parity.build(w)
+    dw.step()
+    d = msa.last_dispatch()
+    assert "cluster=" in d or "split_k_fused_combine" in d, d
+    parity.verify_workload(dw, w, synth.seq_lens(w), sample=[0, batch // 2, batch - 1], run_step=False)
