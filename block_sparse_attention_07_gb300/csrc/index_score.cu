@@ -23,6 +23,8 @@
 // runs of a key row. The warps of a head merge their column maxima through a
 // shared-memory slot per stage: the last to arrive (by a ticket counter) writes
 // the score, so none waits for another.
+#include <atomic>
+
 #include "insert_rows.cuh"
 
 namespace msa {
@@ -47,8 +49,38 @@ struct IdxParams {
   float global_scale;       // NVFP4 keys: fp32 per-tensor scale
   int B, Q, I, NB, P;
   int ins_on;               // 1: also insert the step's new tokens (one per request, Q = 1)
+  uint64_t epoch;           // grows from call to call; tags the work-queue words
   InsertParams ins;
 };
+
+// Work split of the FP8 / NVFP4 kernels: the first units are divided evenly
+// over the CTAs; the last 1 / kDynShare of them are handed out at run time in
+// chunks of kDynChunk consecutive units, so CTAs whose pages arrived faster
+// take more and all end together. The queue is one pair of words per launch
+// slot (the call's epoch modulo kQueueSlots): the next chunk and the CTAs that
+// have finished, each holding epoch << kCountBits | count. Epochs grow from
+// call to call, so each CTA first raises both words to at least that base (a
+// word left by an earlier call restarts from 0) and then counts with plain
+// atomic adds. The CTA that finishes last sets both words back to the base, so
+// a replay of a captured graph (whose epoch is fixed at capture) starts from 0.
+constexpr int kDynShare = 8;
+constexpr int kDynChunk = 2;
+constexpr int kQueueSlots = 64;
+constexpr int kCountBits = 24;        // counts stay below 2^23 (units / kDynChunk, CTAs)
+__device__ unsigned long long g_idx_queue[kQueueSlots][2];
+
+__device__ __forceinline__ unsigned long long epoch_base(uint64_t epoch) {
+  return static_cast<unsigned long long>(epoch) << kCountBits;
+}
+// The count at w before adding one, or -1 if the word belongs to another epoch (flagged).
+__device__ __forceinline__ int64_t epoch_fetch_add(unsigned long long* w, uint64_t epoch, uint32_t* flags) {
+  const unsigned long long old = atomicAdd(w, 1ull);
+  if ((old >> kCountBits) != static_cast<unsigned long long>(epoch)) {
+    set_flag(flags, MSA_FLAG_TIMEOUT);
+    return -1;
+  }
+  return static_cast<int64_t>(old & ((1ull << kCountBits) - 1));
+}
 
 // The insert fused into the index launch (one query position): token t is
 // request t's token at position L_t - 1, so it lands in the request's local
@@ -159,7 +191,8 @@ __global__ void __launch_bounds__(kIdxThreads, kFp4Keys ? kFp4CtasPerSm : 1) ind
   int* valid = reinterpret_cast<int*>(empty + kStages);
   float* part = reinterpret_cast<float*>(valid + kStages);          // [stage][head][warp of pair][8 columns]
   uint32_t* ticket = reinterpret_cast<uint32_t*>(part + kStages * kMaxIdxHeads * kWarpsPerHead * 8);
-  int* pref = reinterpret_cast<int*>(ticket + kStages * kMaxIdxHeads);
+  int* sunit = reinterpret_cast<int*>(ticket + kStages * kMaxIdxHeads);   // unit of each stage, -1: no more
+  int* pref = sunit + kStages;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_launch_dependents();
@@ -181,58 +214,86 @@ __global__ void __launch_bounds__(kIdxThreads, kFp4Keys ? kFp4CtasPerSm : 1) ind
   }
 
   const int64_t U = pref[p.B];
-  const int64_t u0 = U * blockIdx.x / gridDim.x, u1 = U * (blockIdx.x + 1) / gridDim.x;
-  if (u0 >= u1) return;
-  const int b_first = find_request(pref, p.B, u0);
+  const int64_t S = U - U / kDynShare;                 // units [S, U) go through the queue
+  const int64_t u0 = S * blockIdx.x / gridDim.x, u1 = S * (blockIdx.x + 1) / gridDim.x;
+  const int64_t n_static = u1 - u0;
+  const int b_first = u0 < U ? find_request(pref, p.B, u0) : 0;
+  unsigned long long* queue = g_idx_queue[p.epoch % kQueueSlots];
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer --
     // The whole warp fetches the page ids of the next 32 units at once (one
-    // chunk ahead); lane 0 issues the copies.
+    // chunk ahead); lane 0 issues the copies and records each stage's unit.
+    // Then the queue's chunks, and a last stage marked -1.
     const uint64_t pol = l2_evict_first_policy();
     const uint8_t* keys = static_cast<const uint8_t*>(p.keys);
-    auto page_of = [&](int64_t u) -> int {
-      if (u >= u1) return -1;
+    auto page_of = [&](int64_t u, int64_t end) -> int {
+      if (u >= end) return -1;
       const int bb = find_request(pref, p.B, u);
       return p.block_table[static_cast<int64_t>(bb) * p.NB + (u - pref[bb])];
     };
-    int cur = page_of(u0 + lane);
     int64_t i = 0;
     bool ok = true;
-    for (int64_t base = u0; base < u1 && ok; base += 32) {
-      const int nxt = page_of(base + 32 + lane);
-      const int n = static_cast<int>(u1 - base < 32 ? u1 - base : 32);
-      for (int k = 0; k < n; ++k) {
-        const int page = __shfl_sync(kFull, cur, k);
-        if (lane == 0) {
-          const int s = static_cast<int>(i % kStages);
-          if (!mbar_wait(smem_addr(&empty[s]), static_cast<uint32_t>(((i / kStages) & 1) ^ 1))) {
-            set_flag(p.flags, MSA_FLAG_TIMEOUT);
-            ok = false;
+    // lane 0: waits for stage i to be free, then fills it with unit u's page (u < 0: the end mark)
+    auto issue = [&](int64_t u, int page) {
+      if (lane == 0) {
+        const int s = static_cast<int>(i % kStages);
+        if (!mbar_wait(smem_addr(&empty[s]), static_cast<uint32_t>(((i / kStages) & 1) ^ 1))) {
+          set_flag(p.flags, MSA_FLAG_TIMEOUT);
+          ok = false;
+        } else {
+          const uint32_t fb = smem_addr(&full[s]);
+          sunit[s] = static_cast<int>(u);
+          if (u < 0 || page < 0 || page >= p.P) {
+            if (u >= 0) set_flag(p.flags, MSA_FLAG_BAD_PAGE);
+            valid[s] = 0;
+            mbar_arrive(fb);
           } else {
-            const uint32_t fb = smem_addr(&full[s]);
-            if (page < 0 || page >= p.P) {
-              set_flag(p.flags, MSA_FLAG_BAD_PAGE);
-              valid[s] = 0;
-              mbar_arrive(fb);
-            } else {
-              valid[s] = 1;
-              const uint32_t dst = smem_addr(smem + s * stage_bytes);
-              mbar_arrive_expect_tx(fb, stage_bytes);
-              bulk_g2s(dst, keys + static_cast<int64_t>(page) * key_bytes, key_bytes, fb, pol);
-              bulk_g2s(dst + key_bytes, static_cast<const uint8_t*>(p.scale) + static_cast<int64_t>(page) * scale_bytes,
-                       scale_bytes, fb, pol);
-            }
+            valid[s] = 1;
+            const uint32_t dst = smem_addr(smem + s * stage_bytes);
+            mbar_arrive_expect_tx(fb, stage_bytes);
+            bulk_g2s(dst, keys + static_cast<int64_t>(page) * key_bytes, key_bytes, fb, pol);
+            bulk_g2s(dst + key_bytes, static_cast<const uint8_t*>(p.scale) + static_cast<int64_t>(page) * scale_bytes,
+                     scale_bytes, fb, pol);
           }
         }
-        ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        ++i;
       }
+      ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+      ++i;
+    };
+    int cur = page_of(u0 + lane, u1);
+    for (int64_t base = u0; base < u1 && ok; base += 32) {
+      const int nxt = page_of(base + 32 + lane, u1);
+      const int n = static_cast<int>(u1 - base < 32 ? u1 - base : 32);
+      for (int k = 0; k < n && ok; ++k) issue(base + k, __shfl_sync(kFull, cur, k));
       cur = nxt;
     }
-    // Do not leave while copies into this CTA's shared memory may be in flight.
     if (lane == 0) {
+      atomicMax(&queue[0], epoch_base(p.epoch));
+      atomicMax(&queue[1], epoch_base(p.epoch));
+    }
+    while (ok) {
+      int64_t c0 = -1;
+      if (lane == 0) {
+        const int64_t cnt = epoch_fetch_add(&queue[0], p.epoch, p.flags);
+        c0 = cnt < 0 ? -1 : S + cnt * kDynChunk;
+        if (c0 >= U) c0 = -1;
+      }
+      c0 = __shfl_sync(kFull, c0, 0);
+      if (c0 < 0) break;
+      const int64_t c1 = c0 + kDynChunk < U ? c0 + kDynChunk : U;
+      const int pg = page_of(c0 + lane, c1);
+      for (int64_t u = c0; u < c1 && ok; ++u) issue(u, __shfl_sync(kFull, pg, static_cast<int>(u - c0)));
+    }
+    if (ok) issue(-1, -1);
+    if (lane == 0) {
+      // this CTA takes no more chunks; the last to finish clears the queue words
+      const int64_t done = epoch_fetch_add(&queue[1], p.epoch, p.flags);
+      if (done == static_cast<int64_t>(gridDim.x) - 1) {
+        atomicExch(&queue[0], epoch_base(p.epoch));
+        atomicExch(&queue[1], epoch_base(p.epoch));
+      }
+      // Do not leave while copies into this CTA's shared memory may be in flight.
       const int64_t first = i > kStages ? i - kStages : 0;
       for (int64_t k = first; k < i; ++k)
         if (!mbar_wait(smem_addr(&full[k % kStages]), static_cast<uint32_t>((k / kStages) & 1))) break;
@@ -250,65 +311,80 @@ __global__ void __launch_bounds__(kIdxThreads, kFp4Keys ? kFp4CtasPerSm : 1) ind
   int ell_col0 = 0, ell_col1 = 0;
   int cur_b = -1;
   int b = b_first;
-  int64_t i = 0;
-  for (int64_t u = u0; u < u1; ++u, ++i) {
-    while (u >= pref[b + 1]) ++b;
-    const int n = static_cast<int>(u - pref[b]);
-    if (b != cur_b) {
-      const int L = p.seq_lens[b];
-      // Index-query fragment of position gr for this request and head.
-      float qv[32];
-      if (kGroupCols || gr < p.Q) {
-        // dims this thread feeds to the mma: FP8 keys 16c..16c+15 and 64+16c..64+16c+15
-        // (two 16-byte runs of a key row), NVFP4 keys 32c..32c+31 (one 16-byte run)
-        const uint16_t* qp = qbase + ((static_cast<int64_t>(b) * p.Q + (kGroupCols ? 0 : gr)) * I + g) * kDim;
-        const int o0 = kFp4Keys ? 32 * c : 16 * c, o1 = kFp4Keys ? 32 * c + 16 : 64 + 16 * c;
-        const uint4 a0 = *reinterpret_cast<const uint4*>(qp + o0);
-        const uint4 a1 = *reinterpret_cast<const uint4*>(qp + o0 + 8);
-        const uint4 a2 = *reinterpret_cast<const uint4*>(qp + o1);
-        const uint4 a3 = *reinterpret_cast<const uint4*>(qp + o1 + 8);
-        const uint32_t w[16] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w,
-                                a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
+  // the index-query fragments of request b (loaded when the request changes)
+  auto load_query = [&]() {
+    const int L = p.seq_lens[b];
+    // Index-query fragment of position gr for this request and head.
+    float qv[32];
+    if (kGroupCols || gr < p.Q) {
+      // dims this thread feeds to the mma: FP8 keys 16c..16c+15 and 64+16c..64+16c+15
+      // (two 16-byte runs of a key row), NVFP4 keys 32c..32c+31 (one 16-byte run)
+      const uint16_t* qp = qbase + ((static_cast<int64_t>(b) * p.Q + (kGroupCols ? 0 : gr)) * I + g) * kDim;
+      const int o0 = kFp4Keys ? 32 * c : 16 * c, o1 = kFp4Keys ? 32 * c + 16 : 64 + 16 * c;
+      const uint4 a0 = *reinterpret_cast<const uint4*>(qp + o0);
+      const uint4 a1 = *reinterpret_cast<const uint4*>(qp + o0 + 8);
+      const uint4 a2 = *reinterpret_cast<const uint4*>(qp + o1);
+      const uint4 a3 = *reinterpret_cast<const uint4*>(qp + o1 + 8);
+      const uint32_t w[16] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w,
+                              a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          qv[2 * k] = bf16_bits_to_f32(w[k] & 0xFFFF);
-          qv[2 * k + 1] = bf16_bits_to_f32(w[k] >> 16);
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) qv[k] = 0.f;
+      for (int k = 0; k < 16; ++k) {
+        qv[2 * k] = bf16_bits_to_f32(w[k] & 0xFFFF);
+        qv[2 * k + 1] = bf16_bits_to_f32(w[k] >> 16);
       }
-      float amax = 0.f;
+    } else {
 #pragma unroll
-      for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(qv[k]));
-      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-      const int sh = fp16_shift_for(amax);
-      const float f = exp2_int(sh);
-      const float inv = (kGroupCols || gr < p.Q) ? exp2_int(-sh) * (kFp4Keys ? p.global_scale : 1.f) : 0.f;
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        // k-step s covers this thread's dims 32c+4s..32c+4s+3 (group 2c + s/4)
-        const bool live = !kGroupCols || gr == 2 * c + (s >> 2);
-        qb[s][0] = live ? pack_f16x2(qv[4 * s] * f, qv[4 * s + 1] * f) : 0u;
-        qb[s][1] = live ? pack_f16x2(qv[4 * s + 2] * f, qv[4 * s + 3] * f) : 0u;
-      }
-      if (kGroupCols) {
-        inv_col0 = inv_col1 = inv;
-      } else {
-        inv_col0 = __shfl_sync(kFull, inv, 8 * c);
-        inv_col1 = __shfl_sync(kFull, inv, 8 * c + 4);
-      }
-      ell_col0 = (L - p.Q + 2 * c) / kBlock;
-      ell_col1 = (L - p.Q + 2 * c + 1) / kBlock;
-      cur_b = b;
+      for (int k = 0; k < 32; ++k) qv[k] = 0.f;
     }
-
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(qv[k]));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+    const int sh = fp16_shift_for(amax);
+    const float f = exp2_int(sh);
+    const float inv = (kGroupCols || gr < p.Q) ? exp2_int(-sh) * (kFp4Keys ? p.global_scale : 1.f) : 0.f;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      // k-step s covers this thread's dims 32c+4s..32c+4s+3 (group 2c + s/4)
+      const bool live = !kGroupCols || gr == 2 * c + (s >> 2);
+      qb[s][0] = live ? pack_f16x2(qv[4 * s] * f, qv[4 * s + 1] * f) : 0u;
+      qb[s][1] = live ? pack_f16x2(qv[4 * s + 2] * f, qv[4 * s + 3] * f) : 0u;
+    }
+    if (kGroupCols) {
+      inv_col0 = inv_col1 = inv;
+    } else {
+      inv_col0 = __shfl_sync(kFull, inv, 8 * c);
+      inv_col1 = __shfl_sync(kFull, inv, 8 * c + 4);
+    }
+    ell_col0 = (L - p.Q + 2 * c) / kBlock;
+    ell_col1 = (L - p.Q + 2 * c + 1) / kBlock;
+    cur_b = b;
+  };
+  for (int64_t i = 0;; ++i) {
+    // units of the static range are known in advance, so their request's
+    // queries load while the page is in flight; a queue unit is read from its stage
     const int s = static_cast<int>(i % kStages);
-    if (!mbar_wait(smem_addr(&full[s]), static_cast<uint32_t>((i / kStages) & 1))) {
-      if (lane == 0) set_flag(p.flags, MSA_FLAG_TIMEOUT);
-      break;
+    int64_t u;
+    if (i < n_static) {
+      u = u0 + i;
+      while (u >= pref[b + 1]) ++b;
+      if (b != cur_b) load_query();
+      if (!mbar_wait(smem_addr(&full[s]), static_cast<uint32_t>((i / kStages) & 1))) {
+        if (lane == 0) set_flag(p.flags, MSA_FLAG_TIMEOUT);
+        break;
+      }
+    } else {
+      if (!mbar_wait(smem_addr(&full[s]), static_cast<uint32_t>((i / kStages) & 1))) {
+        if (lane == 0) set_flag(p.flags, MSA_FLAG_TIMEOUT);
+        break;
+      }
+      u = sunit[s];
+      if (u < 0) break;                          // no more units
+      if (u < pref[b] || u >= pref[b + 1]) b = find_request(pref, p.B, u);
+      if (b != cur_b) load_query();
     }
+    const int n = static_cast<int>(u - pref[b]);
     float m0 = -INFINITY, m1 = -INFINITY;
     if (valid[s] && !kFp4Keys) {
       const uint8_t* kb = smem + s * stage_bytes + g * (kBlock * kDim);
@@ -537,6 +613,8 @@ cudaError_t launch_index_score(const IndexArgs& a, const InsertArgs* ins, cudaSt
   IdxParams p{a.q, a.keys, a.scale, a.block_table, a.seq_lens, a.scores, a.flags, a.global_scale,
               a.B, a.Q, a.I, a.NB, a.P};
   p.ins_on = 0;
+  static std::atomic<uint64_t> epoch{1};
+  p.epoch = epoch.fetch_add(1);                      // grows from call to call (queue words, above)
   if (ins != nullptr) {
     if (a.Q != 1) return cudaErrorInvalidValue;   // the caller checks it
     p.ins_on = 1;
@@ -549,7 +627,7 @@ cudaError_t launch_index_score(const IndexArgs& a, const InsertArgs* ins, cudaSt
     const size_t stage = a.fp4 ? static_cast<size_t>(a.I) * (key_bytes_per_head<true>() + scale_bytes_per_head<true>())
                                : static_cast<size_t>(a.I) * (key_bytes_per_head<false>() + scale_bytes_per_head<false>());
     const size_t smem = stages * stage + 2 * stages * 8 + stages * 4 +
-                        stages * kMaxIdxHeads * (kWarpsPerHead * 8 * 4 + 4) + (a.B + 1) * 4;
+                        stages * kMaxIdxHeads * (kWarpsPerHead * 8 * 4 + 4) + stages * 4 + (a.B + 1) * 4;
     auto kern = !a.fp4 ? index_score_fp8_kernel<kIdxStages, false, false>
                 : a.Q == 1 ? index_score_fp8_kernel<kIdxStagesFp4, true, true>
                            : index_score_fp8_kernel<kIdxStagesFp4, true, false>;
