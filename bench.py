@@ -51,13 +51,13 @@ FALLBACK_HBM_GBS = 6800.0
 # out) when it was measured: a changed kernel reports null until it is measured
 # again. Summaries: profiles/.
 NCU_TRAFFIC = {
-    ("index_score", "ragged", "72980f2bc6a8b2b7"): 2316404736 + 872192,
+    ("index_score", "ragged", "460154432d806f6c"): 2316344576 + 956160,
     ("sparse_gqa", "ragged", "9279da445860967d"): 270273024 + 555008,
-    ("index_score", "b32_32k", "72980f2bc6a8b2b7"): 551692800 + 170240,
+    ("index_score", "b32_32k", "460154432d806f6c"): 551647232 + 200192,
     ("sparse_gqa", "b32_32k", "9279da445860967d"): 134991104 + 344320,
-    ("index_score", "spec8", "72980f2bc6a8b2b7"): 1105678336 + 1441280,
+    ("index_score", "spec8", "460154432d806f6c"): 1105680128 + 1737472,
     ("sparse_gqa", "spec8", "9279da445860967d"): 886477312 + 436736,
-    ("index_score", "nvfp4_256k", "72980f2bc6a8b2b7"): 2213757184 + 606976,
+    ("index_score", "nvfp4_256k", "460154432d806f6c"): 2213759744 + 645888,
     ("sparse_gqa", "nvfp4_256k", "9279da445860967d"): 19318272 + 0,
 }
 
