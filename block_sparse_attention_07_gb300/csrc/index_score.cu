@@ -153,15 +153,17 @@ __device__ __forceinline__ int find_request(const int* pref, int B, int64_t u) {
   return lo;
 }
 
-// Sets scores[b, j, g, n] = -inf for every n >= units(b) (never written by a unit).
-__device__ void fill_tails(const IdxParams& p, const int* pref) {
-  const int64_t per_b = static_cast<int64_t>(p.Q) * p.I * p.NB;
-  const int64_t total = per_b * p.B;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; x < total; x += stride) {
-    const int b = static_cast<int>(x / per_b);
-    const int n = static_cast<int>(x % p.NB);
-    if (n >= pref[b + 1] - pref[b]) p.scores[x] = -INFINITY;
+// Sets scores[b, j, g, n] = -inf for every n >= units(b) (never written by a
+// unit); warp `first` of `count` takes every count-th row of NB scores, its
+// lanes adjacent scores.
+__device__ void fill_tails(const IdxParams& p, const int* pref, int64_t first, int64_t count) {
+  const int lane = threadIdx.x & 31;
+  const int rows_per_b = p.Q * p.I;
+  const int64_t rows = static_cast<int64_t>(rows_per_b) * p.B;
+  for (int64_t r = first; r < rows; r += count) {
+    const int b = static_cast<int>(r / rows_per_b);
+    float* row = p.scores + r * p.NB;
+    for (int n = pref[b + 1] - pref[b] + lane; n < p.NB; n += 32) row[n] = -INFINITY;
   }
 }
 
@@ -207,10 +209,11 @@ __global__ void __launch_bounds__(kIdxThreads, kFp4Keys ? kFp4CtasPerSm : 1) ind
   }
   for (int x = threadIdx.x; x < kStages * kMaxIdxHeads; x += blockDim.x) ticket[x] = 0u;
   __syncthreads();
-  fill_tails(p, pref);
-  if (p.ins_on && warp > 0) {
+  if (warp > 0) {
+    // the consumer warps fill the score tails (and insert) while the producer starts streaming
     const int64_t nc = blockDim.x / 32 - 1;
-    fused_insert(p, static_cast<int64_t>(blockIdx.x) * nc + (warp - 1), nc * gridDim.x, lane);
+    fill_tails(p, pref, static_cast<int64_t>(blockIdx.x) * nc + (warp - 1), nc * gridDim.x);
+    if (p.ins_on) fused_insert(p, static_cast<int64_t>(blockIdx.x) * nc + (warp - 1), nc * gridDim.x, lane);
   }
 
   const int64_t U = pref[p.B];
@@ -548,7 +551,7 @@ __global__ void __launch_bounds__(kBlock) index_score_f32_kernel(IdxParams p) {
   if (p.ins_on) fused_insert(p, static_cast<int64_t>(blockIdx.x) * 4 + warp, static_cast<int64_t>(gridDim.x) * 4, lane);
   if (warp == 0) build_prefix(p, pref, blockIdx.x == 0);
   __syncthreads();
-  fill_tails(p, pref);
+  fill_tails(p, pref, static_cast<int64_t>(blockIdx.x) * 4 + warp, static_cast<int64_t>(gridDim.x) * 4);
   const int64_t total = static_cast<int64_t>(pref[p.B]) * p.I;
   const float* qg = static_cast<const float*>(p.q);
   const float* keys = static_cast<const float*>(p.keys);
