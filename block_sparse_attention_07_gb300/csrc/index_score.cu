@@ -8,8 +8,9 @@
 // score scale is applied.
 //
 // FP8 / NVFP4 paths: a persistent kernel, one CTA per SM (two for NVFP4 keys,
-// whose pages are half the size). Work units are
-// the (request, block) pairs that some position of the request can select.
+// whose pages are half the size). Work units are the (request, block) pairs
+// that some position of the request can select; seven eighths of them are
+// split evenly over the CTAs and the rest handed out at run time (below).
 // A producer thread streams each unit's page (I heads x 128 tokens x 128 B of
 // E4M3 keys, contiguous, plus I x 512 B of per-token scales) into a ring of
 // shared-memory stages with bulk copies completed on mbarriers. One consumer
