@@ -51,6 +51,7 @@ struct IdxParams {
   int B, Q, I, NB, P;
   int ins_on;               // 1: also insert the step's new tokens (one per request, Q = 1)
   uint64_t epoch;           // grows from call to call; tags the work-queue words
+  int slot;                 // the call's work-queue slot
   InsertParams ins;
 };
 
@@ -58,17 +59,19 @@ struct IdxParams {
 // over the CTAs; the last 1 / kDynShare of them are handed out at run time in
 // chunks of kDynChunk consecutive units, so CTAs whose pages arrived faster
 // take more and all end together. The queue is one pair of words per launch
-// slot (the call's epoch modulo kQueueSlots): the next chunk and the CTAs that
-// have finished, each holding epoch << kCountBits | count. Epochs grow from
-// call to call, so each CTA first raises both words to at least that base (a
-// word left by an earlier call restarts from 0) and then counts with plain
-// atomic adds. The CTA that finishes last sets both words back to the base, so
-// a replay of a captured graph (whose epoch is fixed at capture) starts from 0.
+// slot: the next chunk and the CTAs that have finished, each holding
+// epoch << kCountBits | count. Epochs grow from call to call, so each CTA first
+// raises both words to at least that base (a word left by an earlier call
+// restarts from 0) and then counts with plain atomic adds. The CTA that
+// finishes last sets both words back to the base, so a replay of a captured
+// graph (whose epoch is fixed at capture) starts from 0. Direct calls take the
+// slots 0 .. kQueueSlots - 1 in turn and launches captured into a graph the
+// slots after them, so a direct call never raises a captured launch's words.
 constexpr int kDynShare = 8;
 constexpr int kDynChunk = 2;
 constexpr int kQueueSlots = 64;
 constexpr int kCountBits = 24;        // counts stay below 2^23 (units / kDynChunk, CTAs)
-__device__ unsigned long long g_idx_queue[kQueueSlots][2];
+__device__ unsigned long long g_idx_queue[2 * kQueueSlots][2];
 
 __device__ __forceinline__ unsigned long long epoch_base(uint64_t epoch) {
   return static_cast<unsigned long long>(epoch) << kCountBits;
@@ -222,7 +225,7 @@ __global__ void __launch_bounds__(kIdxThreads, kFp4Keys ? kFp4CtasPerSm : 1) ind
   const int64_t u0 = S * blockIdx.x / gridDim.x, u1 = S * (blockIdx.x + 1) / gridDim.x;
   const int64_t n_static = u1 - u0;
   const int b_first = u0 < U ? find_request(pref, p.B, u0) : 0;
-  unsigned long long* queue = g_idx_queue[p.epoch % kQueueSlots];
+  unsigned long long* queue = g_idx_queue[p.slot];
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer --
@@ -618,7 +621,12 @@ cudaError_t launch_index_score(const IndexArgs& a, const InsertArgs* ins, cudaSt
               a.B, a.Q, a.I, a.NB, a.P};
   p.ins_on = 0;
   static std::atomic<uint64_t> epoch{1};
+  static std::atomic<uint32_t> captured{0};
   p.epoch = epoch.fetch_add(1);                      // grows from call to call (queue words, above)
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &capture) != cudaSuccess) capture = cudaStreamCaptureStatusNone;
+  p.slot = capture == cudaStreamCaptureStatusActive ? kQueueSlots + static_cast<int>(captured.fetch_add(1) % kQueueSlots)
+                                                    : static_cast<int>(p.epoch % kQueueSlots);
   if (ins != nullptr) {
     if (a.Q != 1) return cudaErrorInvalidValue;   // the caller checks it
     p.ins_on = 1;

@@ -228,11 +228,13 @@ msa_status_t msa_qk_norm_rope_insert(const msa_dims_t* dims, const void* q, cons
  * MSA_BF16 with an MSA_FP8_E4M3 or MSA_NVFP4 one). block_table: int32 [B, NB].
  * seq_lens: int32 [B]. scores: fp32 [B, Q, I, NB].
  * With FP8 or NVFP4 keys the last eighth of the blocks is handed out to the
- * CTAs at run time from a queue in a library-owned device array, one of 64
- * slots per call in turn: at most 64 such calls may run at once. The CTA that
- * finishes last resets its slot, so a captured graph replays cleanly; after a
- * launch that raised MSA_FLAG_TIMEOUT, capture such a graph again before
- * replaying it. The scores do not depend on which CTA scored a block.
+ * CTAs at run time from a queue in a library-owned device array: direct calls
+ * take one of 64 slots in turn (at most 64 may run at once), and launches
+ * captured into CUDA graphs one of 64 other slots in turn (at most 64 captured
+ * launches may be in use). The CTA that finishes last resets its slot, so a
+ * captured graph replays cleanly; after a launch that raised MSA_FLAG_TIMEOUT,
+ * capture such a graph again before replaying it. The scores do not depend on
+ * which CTA scored a block.
  */
 msa_status_t msa_index_score(const msa_dims_t* dims, const void* idx_q, msa_dtype_t q_dtype,
                              const msa_index_cache_t* idx_cache, const int32_t* block_table,

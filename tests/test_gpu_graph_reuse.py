@@ -121,3 +121,25 @@ def test_two_streams_at_once(monkeypatch):
                 assert torch.equal(x, y)
     parity.verify_workload(da, wa, synth.seq_lens(wa), run_step=False)
     parity.verify_workload(db, wb, synth.seq_lens(wb), run_step=False)
+
+
+def test_graph_replays_after_many_direct_calls():
+    """The index launch hands out its last blocks from a queue slot; a captured
+    graph keeps its slot while more than 64 direct calls cycle through theirs,
+    and two captured graphs replay in turn, each equal to an eager step."""
+    w = synth.scaled(W["b32_32k"], batch=3, ctx=2600)
+    dw = parity.build(w)
+    dw.step()
+    torch.cuda.synchronize()
+    eager = dw.scores.clone()
+    g1 = dw.capture(dw.step)
+    g2 = dw.capture(dw.step)
+    for _ in range(70):                     # direct calls through every direct-call slot
+        dw.index_score()
+    torch.cuda.synchronize()
+    for g in (g1, g2, g1, g2):
+        dw.scores.fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(dw.scores, eager)
+    assert dw.check_flags() == 0
