@@ -51,13 +51,13 @@ FALLBACK_HBM_GBS = 6800.0
 # out) when it was measured: a changed kernel reports null until it is measured
 # again. Summaries: profiles/.
 NCU_TRAFFIC = {
-    ("index_score", "ragged", "29b705e991a3ee27"): 2316349440 + 977152,
+    ("index_score", "ragged", "2752585a1a31559d"): 2316357120 + 973312,
     ("sparse_gqa", "ragged", "9279da445860967d"): 270273024 + 555008,
-    ("index_score", "b32_32k", "29b705e991a3ee27"): 551644160 + 155392,
+    ("index_score", "b32_32k", "2752585a1a31559d"): 551655680 + 210688,
     ("sparse_gqa", "b32_32k", "9279da445860967d"): 134991104 + 344320,
-    ("index_score", "spec8", "29b705e991a3ee27"): 1105681408 + 1740544,
+    ("index_score", "spec8", "2752585a1a31559d"): 1105795328 + 1702144,
     ("sparse_gqa", "spec8", "9279da445860967d"): 886477312 + 436736,
-    ("index_score", "nvfp4_256k", "29b705e991a3ee27"): 2213771008 + 573696,
+    ("index_score", "nvfp4_256k", "2752585a1a31559d"): 2213771520 + 564480,
     ("sparse_gqa", "nvfp4_256k", "9279da445860967d"): 19318272 + 0,
 }
 
